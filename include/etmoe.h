@@ -1,0 +1,153 @@
+/*
+ * etmoe.h -- C ABI of libetmoe.so, the Event-Tensor MoE megakernel library
+ * for GB300 (sm_103a).
+ *
+ * What the library computes is the plain definition of each layer; what it
+ * changes is the schedule.  Sources (restated, not quoted):
+ *  - "Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
+ *    Kernels" (episode summary of "Event Tensor: A Unified Abstraction for
+ *    Compiling Dynamic Megakernel"): dependencies between tiled tasks are
+ *    tracked by events instead of kernel boundaries; split-K partial sums are
+ *    combined through events; a batch size kept symbolic lets one compiled
+ *    kernel serve every token count; MoE routing produces data-dependent
+ *    event counters and triggers tasks from the router output; static
+ *    scheduling suits dense, predictable work and dynamic scheduling suits
+ *    irregular MoE work.
+ *  - "Megakernels ch. 5 - Event Tensor et le dynamisme", section 5.5:
+ *    obstacle 1 (a waiter spins until its counter reaches a target; with
+ *    dynamism that target must be computed on the GPU at run time, before
+ *    the wait) and obstacle 3 (unpredictable task sizes need an online,
+ *    atomic work queue).
+ *
+ * Conventions for every call:
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *    stated otherwise.  The library never allocates device memory and never
+ *    synchronises in the compute calls; work is enqueued on `stream` (a
+ *    cudaStream_t passed as void*; NULL is the legacy default stream).
+ *  - bf16 tensors are row-major IEEE bfloat16; weights use the Linear layout
+ *    [out_features, in_features] (the inner dimension is contiguous), except
+ *    the router weight, which is [H, E] (hidden-major) as it is given.
+ *  - Each call needs a caller-owned workspace of *_workspace_bytes(...)
+ *    bytes, 256-byte aligned and ZEROED ONCE when it is allocated.  The
+ *    kernels return every counter in it to zero before they exit, so a
+ *    workspace can be reused by any number of later calls on one stream.
+ *    Two calls that run concurrently must not share a workspace.
+ *  - Return codes: ET_OK, or a synchronous validation error (nothing was
+ *    launched).  Errors found on the device (a bounded wait that ran out, a
+ *    device token count above its maximum) are recorded in a sticky status
+ *    word inside the workspace; read it with et_status().
+ *  - Token counts stay symbolic: pass d_T (a device int32) to have the kernel
+ *    read the count at run time, so that one launch -- or one captured CUDA
+ *    graph -- serves every count 0 <= T <= T_max without host involvement.
+ *    With d_T == NULL the host value T is used.
+ *
+ * Supported shapes: H and F multiples of 128; 1 <= k <= min(E, 8);
+ * 1 <= E <= 256; 0 <= T <= T_max.  Anything else returns ET_ERR_UNSUPPORTED
+ * or ET_ERR_INVALID.  T == 0 launches nothing and leaves `out` untouched.
+ */
+#ifndef ETMOE_H
+#define ETMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum et_status_code {
+    ET_OK = 0,
+    ET_ERR_INVALID = 1,     /* null pointer, negative size, T > T_max, k > E ... */
+    ET_ERR_WORKSPACE = 2,   /* workspace missing, too small or misaligned */
+    ET_ERR_UNSUPPORTED = 3, /* shape outside the supported tiling */
+    ET_ERR_CUDA = 4,        /* a CUDA runtime call failed (see et_last_error_string) */
+    ET_ERR_TIMEOUT = 5,     /* device: a bounded event or barrier wait ran out */
+    ET_ERR_BOUNDS = 6       /* device: the device-side count exceeded its maximum */
+};
+
+/* Optional knobs; pass NULL for the defaults. */
+typedef struct et_opts {
+    uint32_t timeout_us; /* bound on every device-side wait; 0 = 200000 us */
+    uint32_t reserved;
+    int32_t fault_mode;  /* test hook, 0 = off; 1 = the producer task chosen by
+                            fault_arg skips its event release, so that its
+                            consumers must time out cleanly */
+    int32_t fault_arg;
+} et_opts;
+
+/* ------------------------------------------------------------------------
+ * MoE layer: router top-k -> per-expert counts -> SwiGLU expert FFN ->
+ * weighted combine, in one persistent cooperative launch.
+ *
+ *   logits[t,e] = sum_h x[t,h] * w_router[h,e] (+ router_bias[e]), fp32 in a
+ *                 fixed order (32 strided partial sums, then a halving tree),
+ *                 so routing is reproducible bit for bit;
+ *   idx[t,:]    = the k largest logits, ties to the lower expert index;
+ *   w[t,:]      = softmax over those k logits;
+ *   h           = bf16( silu(x Wg[e]^T) * (x Wu[e]^T) ),  y = bf16( h Wd[e]^T );
+ *   out[t]      = bf16( sum_j w[t,j] * y[t,j] ).
+ *
+ * x bf16 [T,H]; w_router bf16 [H,E]; router_bias fp32 [E] or NULL;
+ * w_gate, w_up bf16 [E,F,H]; w_down bf16 [E,H,F]; out bf16 [T,H].
+ * Optional outputs (NULL to skip): topk_idx int32 [T,k], topk_w fp32 [T,k],
+ * expert_counts int32 [E], perm int32 [T*k] (perm[off[e]+r] = t*k+j for the
+ * r-th token, ascending, routed to e; off = exclusive prefix sum of counts).
+ * ---------------------------------------------------------------------- */
+size_t et_moe_workspace_bytes(int T_max, int H, int F, int E, int k);
+
+int et_moe_layer(const void* x, const void* w_router, const float* router_bias,
+                 const void* w_gate, const void* w_up, const void* w_down, void* out,
+                 int32_t* topk_idx, float* topk_w, int32_t* expert_counts, int32_t* perm,
+                 int T, const int32_t* d_T, int T_max, int H, int F, int E, int k,
+                 void* workspace, size_t workspace_bytes, const et_opts* opts, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Split-K GEMM with event-counter reduction:
+ *   Y[M,N] = bf16( sum_{s<split} X[:,K_s] Wt[:,K_s]^T ),  K_s = s-th of `split`
+ * equal K chunks.  Each (row tile, column tile, split) is one task; the task
+ * that brings a tile's counter to `split` sums the fp32 partials in split
+ * order and stores Y.  X bf16 [M_max,K] (rows >= M are never read into Y);
+ * Wt bf16 [N,K]; Y bf16 [M,N].  N % 128 == 0, K % (64*split) == 0,
+ * 1 <= split <= 16.
+ * ---------------------------------------------------------------------- */
+size_t et_splitk_workspace_bytes(int M_max, int N, int K, int split);
+
+int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t* d_M, int M_max,
+                   int N, int K, int split, void* workspace, size_t workspace_bytes,
+                   const et_opts* opts, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Dense dependent MLP chain, statically scheduled (tasks bound to CTAs):
+ *   xhat = bf16( x / sqrt(mean(x^2) + eps) * gamma )
+ *   out  = bf16( bf16( silu(xhat Wg^T) * (xhat Wu^T) ) Wd^T )
+ * x bf16 [B,H]; gamma bf16 [H]; w_gate, w_up bf16 [F,H]; w_down bf16 [H,F];
+ * out bf16 [B,H].  Down tiles wait on per-chunk event counters of the
+ * gate/up tiles, not on a kernel boundary.
+ * ---------------------------------------------------------------------- */
+size_t et_mlp_workspace_bytes(int B_max, int H, int F);
+
+int et_mlp_chain(const void* x, const void* gamma, float eps, const void* w_gate,
+                 const void* w_up, const void* w_down, void* out, int B, const int32_t* d_B,
+                 int B_max, int H, int F, void* workspace, size_t workspace_bytes,
+                 const et_opts* opts, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Status of the device side.  Synchronises `stream`, then copies the sticky
+ * status word of `workspace` to *code_out / *detail_out (host pointers).
+ * detail identifies where a wait ran out.  For tests and diagnostics only.
+ * et_reset_status clears the word (enqueued on `stream`, no sync).
+ * ---------------------------------------------------------------------- */
+int et_status(const void* workspace, void* stream, int32_t* code_out, int32_t* detail_out);
+int et_reset_status(void* workspace, void* stream);
+
+/* Message for the last error returned on this host thread ("" if none). */
+const char* et_last_error_string(void);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int et_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ETMOE_H */

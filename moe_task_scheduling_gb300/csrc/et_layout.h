@@ -1,0 +1,150 @@
+// et_layout.h -- workspace header, kernel argument blocks and tiling
+// constants shared by the host launcher and the kernels of libetmoe.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/etmoe.h"
+
+namespace et {
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------- tiling constants
+
+constexpr int kThreads = 256;        // 8 warps: 0 TMA, 1 MMA/TMEM, 2-3 spare, 4-7 epilogue
+constexpr int kEpiWarp0 = 4;         // epilogue warp w reads TMEM lanes 32*(w-4) ..
+constexpr int kTileM = 128;          // weight rows per tile (UMMA M)
+constexpr int kBlockK = 64;          // bf16 elements per k-block = one 128-byte swizzle row
+constexpr int kABytes = kTileM * kBlockK * 2;   // 16 KB weight tile
+constexpr int kBBoxRows = 16;        // activation rows per TMA box
+constexpr int kMaxStages = 8;
+constexpr int kTmemCols = 512;       // accumulator 0 at column 0, accumulator 1 at 256
+constexpr int kAcc1Col = 256;
+constexpr int kSmemLimit = 232448;   // 227 KB of opt-in dynamic shared memory per CTA
+constexpr int kSplitMax = 8;         // largest split of the MoE / MLP down projection
+
+// MoE
+constexpr int kMoeNMax = 128;        // token rows per expert tile (UMMA N)
+constexpr int kRouterTile = 16;      // tokens per router / permute task
+constexpr int kCombineTile = 16;     // tokens per combine task
+constexpr int kMoeSplitRowsCap = 512;  // split the down projection only up to T*k rows
+
+// split-K GEMM and MLP chain: up to 256 token rows per tile
+constexpr int kWideNMax = 256;
+
+// ---------------------------------------------------------------- workspace header
+
+// The first 256 bytes of every workspace.  Everything but the sticky status
+// word is returned to zero by the last CTA of each launch.
+struct EtHeader {
+    int32_t status_code;    // sticky first device error (et_status_code)
+    int32_t status_detail;  // where it happened
+    int32_t abort;          // non-zero: every bounded wait gives up
+    int32_t exit_count;     // CTAs that left the task loop
+    int32_t q_head;         // next task index to pop (dynamic queue)
+    int32_t q_ready;        // the scan task has published the queue
+    int32_t q_total;        // number of published queue entries
+    int32_t total_mt;       // expert row tiles this call (published by the scan)
+    int32_t ev_router;      // router tiles done
+    int32_t ev_perm;        // permute tiles done
+    int32_t ev_ydone;       // expert output tiles complete
+    int32_t ev_norm;        // RMSNorm tasks done (MLP chain)
+    int32_t split;          // split of the down projection chosen this call
+    int32_t reserved[51];
+};
+static_assert(sizeof(EtHeader) == 256, "header is 256 bytes");
+
+constexpr int kHeaderBytes = 256;
+
+// detail codes: where a wait ran out (low byte) and the CTA (upper bits)
+enum WaitWhere {
+    kWhereEmpty = 1,
+    kWhereFull = 2,
+    kWhereAcc = 3,
+    kWhereQueue = 4,
+    kWhereRouter = 5,
+    kWherePerm = 6,
+    kWhereH = 7,
+    kWhereY = 8,
+    kWhereNorm = 9,
+    kWhereBoundsT = 10
+};
+
+// Task descriptor of the dynamic queue: {type, a, b, c}
+enum TaskType { kTaskExit = 0, kTaskRouter = 1, kTaskScan = 2, kTaskPermute = 3,
+                kTaskGateUp = 4, kTaskDown = 5, kTaskCombine = 6, kTaskNorm = 7,
+                kTaskSplitK = 8 };
+
+// ---------------------------------------------------------------- kernel argument blocks
+
+struct MoeArgs {
+    const bf16* x;        // [T, H]
+    const bf16* wr;       // [H, E]
+    const float* bias;    // [E] or null
+    bf16* out;            // [T, H]
+    int32_t* idx;         // [T_max, k]   (caller's buffer or workspace)
+    float* gw;            // [T_max, k]
+    int32_t* cnt;         // [E]
+    int32_t* perm;        // [T_max * k]
+    const int32_t* d_T;   // device token count or null
+    int T_host, T_max, H, F, E, k;
+    EtHeader* hdr;
+    int32_t* ev_h;        // [mt_max * kSplitMax]
+    int32_t* ev_y;        // [mt_max * (H/128)]
+    int32_t* hist;        // [r_max * E]: per router tile expert histogram
+    int32_t* base;        // [r_max * E]: first permuted row of each (tile, expert)
+    int32_t* off;         // [E + 1]
+    int32_t* pos;         // [T_max * k]: permuted row of (t, j)
+    int32_t* g_expert;    // [mt_max]: expert of row tile g
+    int32_t* g_row0;      // [mt_max]: first permuted row of tile g
+    int32_t* g_rows;      // [mt_max]: valid rows of tile g
+    int32_t* g_n;         // [mt_max]: UMMA N of tile g
+    int4* queue;          // [q_max]
+    bf16* xp;             // [T_max*k, H]: x rows in permuted order
+    bf16* h;              // [T_max*k, F]
+    bf16* y;              // [T_max*k, H]
+    float* partial;       // [kSplitMax, split_rows_cap, H]
+    int mt_max, q_max, split_rows_cap, r_max;
+    int stages, num_ctas;
+    uint64_t timeout_ns;
+    int fault_mode, fault_arg;
+};
+
+struct SplitKArgs {
+    bf16* Y;              // [M, N]
+    const int32_t* d_M;
+    int M_host, M_max, N, K, split;
+    EtHeader* hdr;
+    int32_t* ev;          // [ceil(M_max/256) * N/128], self-resetting
+    float* partial;       // [split, M_max, N]
+    int stages, num_ctas;
+    uint64_t timeout_ns;
+    int fault_mode, fault_arg;
+};
+
+struct MlpArgs {
+    const bf16* x;        // [B, H]
+    const bf16* gamma;    // [H]
+    float eps;
+    bf16* out;            // [B, H]
+    const int32_t* d_B;
+    int B_host, B_max, H, F;
+    EtHeader* hdr;
+    bf16* xhat;           // [B_max, H]
+    bf16* h;              // [B_max, F]
+    int32_t* ev_h;        // [mt_max * kSplitMax]
+    int32_t* ev_y;        // [mt_max * H/128], self-resetting
+    float* partial;       // [kSplitMax, B_max, H]
+    int mt_max;
+    int stages, num_ctas;
+    uint64_t timeout_ns;
+    int fault_mode, fault_arg;
+};
+
+// Shared-memory geometry of one pipeline stage: [A0 16K][A1 16K][B nmax*128].
+__host__ __device__ constexpr int stage_bytes(int nmax) { return 2 * kABytes + nmax * 128; }
+
+}  // namespace et

@@ -1,0 +1,468 @@
+// etmoe_api.cu -- the C ABI of libetmoe.so: argument checks, workspace
+// carve-up, TMA tensor maps, and one cooperative launch per call.  No call
+// here allocates device memory or synchronises, except et_status.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "et_gemm.cuh"
+
+namespace et {
+cudaError_t launch_moe(const MoeArgs&, const CUtensorMap*, int, int, cudaStream_t);
+cudaError_t prepare_moe(int);
+cudaError_t launch_splitk(const SplitKArgs&, const CUtensorMap*, int, int, cudaStream_t);
+cudaError_t prepare_splitk(int);
+cudaError_t launch_mlp(const MlpArgs&, const CUtensorMap*, int, int, cudaStream_t);
+cudaError_t prepare_mlp(int);
+}  // namespace et
+
+using namespace et;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+    g_last_error = msg;
+    return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+    return fail(ET_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    bool moe = false, splitk = false, mlp = false;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+template <class T>
+bool aligned(const void* p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Per-device one-time set-up: SM count, kernel attributes, the driver's
+// tensor-map encoder (fetched through the runtime, so the library does not
+// link libcuda and loads on machines without a GPU).
+int device_state(DeviceState** out, int* dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ET_ERR_CUDA, "device index out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(ET_ERR_UNSUPPORTED, "libetmoe is built for sm_103a (GB300) only; device is sm_" +
+                                                std::to_string(major) + std::to_string(minor));
+        e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return fail(ET_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        st.ready = true;
+    }
+    *out = &st;
+    if (dev_out) *dev_out = dev;
+    return ET_OK;
+}
+
+// Row-major bf16 matrix [rows, cols] as a 2-D tensor map with 64-column,
+// box_rows-row boxes and the 128-byte swizzle (one swizzle row = 64 bf16).
+int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+             const char* what) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(ET_ERR_CUDA, std::string("cuTensorMapEncodeTiled failed for ") + what +
+                                     " (code " + std::to_string(static_cast<int>(r)) + ")");
+    return ET_OK;
+}
+
+uint64_t timeout_ns_of(const et_opts* o) {
+    const uint32_t us = (o && o->timeout_us) ? o->timeout_us : 200000u;
+    return static_cast<uint64_t>(us) * 1000ull;
+}
+
+int stages_for(int nmax) {
+    const int avail = kSmemLimit - 1024 - static_cast<int>(sizeof(Ctl));
+    int s = avail / stage_bytes(nmax);
+    return s > kMaxStages ? kMaxStages : s;
+}
+
+struct Carve {
+    size_t off = kHeaderBytes;
+    size_t take(size_t bytes, size_t align = 256) {
+        off = round_up(off, align);
+        const size_t r = off;
+        off += round_up(bytes, 16);
+        return r;
+    }
+};
+
+// ---------------------------------------------------------------- MoE layout
+
+struct MoeLayout {
+    int Tk, r_max, mt_max, q_max, split_cap;
+    size_t ev_h, ev_y, hist, base, idx, gw, cnt, off, pos, perm, g_expert, g_row0, g_rows, g_n,
+        queue, xp, h, y, partial, total;
+};
+
+MoeLayout moe_layout(int T_max, int H, int F, int E, int k) {
+    MoeLayout L{};
+    L.Tk = T_max * k;
+    L.r_max = ceil_div(T_max, kRouterTile);
+    L.mt_max = ceil_div(L.Tk, kMoeNMax) + E;
+    const int FT = F / kTileM, HT = H / kTileM;
+    L.q_max = L.r_max + L.mt_max * FT + L.mt_max * kSplitMax * HT + ceil_div(T_max, kCombineTile);
+    L.split_cap = L.Tk < kMoeSplitRowsCap ? L.Tk : kMoeSplitRowsCap;
+    Carve c;
+    L.ev_h = c.take(sizeof(int) * L.mt_max * kSplitMax);
+    L.ev_y = c.take(sizeof(int) * L.mt_max * HT);
+    L.hist = c.take(sizeof(int) * L.r_max * E);
+    L.base = c.take(sizeof(int) * L.r_max * E);
+    L.idx = c.take(sizeof(int) * L.Tk);
+    L.gw = c.take(sizeof(float) * L.Tk);
+    L.cnt = c.take(sizeof(int) * E);
+    L.off = c.take(sizeof(int) * (E + 1));
+    L.pos = c.take(sizeof(int) * L.Tk);
+    L.perm = c.take(sizeof(int) * L.Tk);
+    L.g_expert = c.take(sizeof(int) * L.mt_max);
+    L.g_row0 = c.take(sizeof(int) * L.mt_max);
+    L.g_rows = c.take(sizeof(int) * L.mt_max);
+    L.g_n = c.take(sizeof(int) * L.mt_max);
+    L.queue = c.take(sizeof(int4) * L.q_max);
+    L.xp = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
+    L.h = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * F, 1024);
+    L.y = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
+    L.partial = c.take(sizeof(float) * static_cast<size_t>(kSplitMax) * L.split_cap * H, 1024);
+    L.total = round_up(c.off, 256);
+    return L;
+}
+
+bool moe_shape_ok(int T_max, int H, int F, int E, int k, std::string* why) {
+    if (T_max < 1 || T_max > 65536) { *why = "T_max must be in [1, 65536]"; return false; }
+    if (H < 128 || H % 128 || F < 128 || F % 128) { *why = "H and F must be positive multiples of 128"; return false; }
+    if (H > 65536 || F > 65536) { *why = "H and F must be <= 65536"; return false; }
+    if (E < 1 || E > 256) { *why = "E must be in [1, 256]"; return false; }
+    if (k < 1 || k > 8 || k > E) { *why = "k must be in [1, min(E, 8)]"; return false; }
+    if (static_cast<long long>(E) * F >= (1ll << 31) || static_cast<long long>(E) * H >= (1ll << 31)) {
+        *why = "E*F and E*H must fit in int32"; return false;
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------- split-K layout
+
+struct SplitKLayout {
+    size_t ev, partial, total;
+};
+
+SplitKLayout splitk_layout(int M_max, int N, int K, int split) {
+    (void)K;
+    SplitKLayout L{};
+    Carve c;
+    L.ev = c.take(sizeof(int) * static_cast<size_t>(ceil_div(M_max, kWideNMax)) * (N / kTileM));
+    L.partial = c.take(sizeof(float) * static_cast<size_t>(split > 1 ? split : 0) * M_max * N, 1024);
+    L.total = round_up(c.off, 256);
+    return L;
+}
+
+// ---------------------------------------------------------------- MLP layout
+
+struct MlpLayout {
+    int mt_max;
+    size_t xhat, h, ev_h, ev_y, partial, total;
+};
+
+MlpLayout mlp_layout(int B_max, int H, int F) {
+    MlpLayout L{};
+    L.mt_max = ceil_div(B_max, kWideNMax);
+    Carve c;
+    L.ev_h = c.take(sizeof(int) * L.mt_max * kSplitMax);
+    L.ev_y = c.take(sizeof(int) * L.mt_max * (H / kTileM));
+    L.xhat = c.take(sizeof(uint16_t) * static_cast<size_t>(B_max) * H, 1024);
+    L.h = c.take(sizeof(uint16_t) * static_cast<size_t>(B_max) * F, 1024);
+    L.partial = c.take(sizeof(float) * static_cast<size_t>(kSplitMax) * B_max * H, 1024);
+    L.total = round_up(c.off, 256);
+    return L;
+}
+
+int check_ws(void* ws, size_t have, size_t need) {
+    if (!ws) return fail(ET_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned<void>(ws, 256)) return fail(ET_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (have < need)
+        return fail(ET_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) +
+                                          " bytes, got " + std::to_string(have));
+    return ET_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int et_version(void) { return 100; }
+
+const char* et_last_error_string(void) { return g_last_error.c_str(); }
+
+size_t et_moe_workspace_bytes(int T_max, int H, int F, int E, int k) {
+    std::string why;
+    if (!moe_shape_ok(T_max, H, F, E, k, &why)) return 0;
+    return moe_layout(T_max, H, F, E, k).total;
+}
+
+int et_moe_layer(const void* x, const void* w_router, const float* router_bias, const void* w_gate,
+                 const void* w_up, const void* w_down, void* out, int32_t* topk_idx, float* topk_w,
+                 int32_t* expert_counts, int32_t* perm, int T, const int32_t* d_T, int T_max, int H,
+                 int F, int E, int k, void* workspace, size_t workspace_bytes, const et_opts* opts,
+                 void* stream) {
+    g_last_error.clear();
+    std::string why;
+    if (!moe_shape_ok(T_max, H, F, E, k, &why)) return fail(ET_ERR_UNSUPPORTED, why);
+    if (!x || !w_router || !w_gate || !w_up || !w_down || !out)
+        return fail(ET_ERR_INVALID, "x, w_router, w_gate, w_up, w_down and out must be non-NULL");
+    if (!d_T && (T < 0 || T > T_max)) return fail(ET_ERR_INVALID, "T must be in [0, T_max]");
+    const void* need16[] = {x, w_router, w_gate, w_up, w_down, out};
+    for (const void* p : need16)
+        if (!aligned<void>(p, 16)) return fail(ET_ERR_INVALID, "tensors must be 16-byte aligned");
+    const MoeLayout L = moe_layout(T_max, H, F, E, k);
+    int rc = check_ws(workspace, workspace_bytes, L.total);
+    if (rc) return rc;
+    if (!d_T && T == 0) return ET_OK;
+
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st, nullptr))) return rc;
+    const int stages = stages_for(kMoeNMax);
+    const int smem = smem_bytes_for(stages, kMoeNMax);
+    if (!st->moe) {
+        cudaError_t e = prepare_moe(smem);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(moe)");
+        st->moe = true;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    MoeArgs a{};
+    a.x = static_cast<const bf16*>(x);
+    a.wr = static_cast<const bf16*>(w_router);
+    a.bias = router_bias;
+    a.out = static_cast<bf16*>(out);
+    a.idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + L.idx);
+    a.gw = topk_w ? topk_w : reinterpret_cast<float*>(ws + L.gw);
+    a.cnt = expert_counts ? expert_counts : reinterpret_cast<int32_t*>(ws + L.cnt);
+    a.perm = perm ? perm : reinterpret_cast<int32_t*>(ws + L.perm);
+    a.d_T = d_T;
+    a.T_host = T;
+    a.T_max = T_max;
+    a.H = H;
+    a.F = F;
+    a.E = E;
+    a.k = k;
+    a.hdr = reinterpret_cast<EtHeader*>(ws);
+    a.ev_h = reinterpret_cast<int32_t*>(ws + L.ev_h);
+    a.ev_y = reinterpret_cast<int32_t*>(ws + L.ev_y);
+    a.hist = reinterpret_cast<int32_t*>(ws + L.hist);
+    a.base = reinterpret_cast<int32_t*>(ws + L.base);
+    a.off = reinterpret_cast<int32_t*>(ws + L.off);
+    a.pos = reinterpret_cast<int32_t*>(ws + L.pos);
+    a.g_expert = reinterpret_cast<int32_t*>(ws + L.g_expert);
+    a.g_row0 = reinterpret_cast<int32_t*>(ws + L.g_row0);
+    a.g_rows = reinterpret_cast<int32_t*>(ws + L.g_rows);
+    a.g_n = reinterpret_cast<int32_t*>(ws + L.g_n);
+    a.queue = reinterpret_cast<int4*>(ws + L.queue);
+    a.xp = reinterpret_cast<bf16*>(ws + L.xp);
+    a.h = reinterpret_cast<bf16*>(ws + L.h);
+    a.y = reinterpret_cast<bf16*>(ws + L.y);
+    a.partial = reinterpret_cast<float*>(ws + L.partial);
+    a.mt_max = L.mt_max;
+    a.q_max = L.q_max;
+    a.split_rows_cap = L.split_cap;
+    a.r_max = L.r_max;
+    a.stages = stages;
+    a.num_ctas = st->sms;
+    a.timeout_ns = timeout_ns_of(opts);
+    a.fault_mode = opts ? opts->fault_mode : 0;
+    a.fault_arg = opts ? opts->fault_arg : 0;
+
+    CUtensorMap maps[5];
+    const uint64_t EF = static_cast<uint64_t>(E) * F, EH = static_cast<uint64_t>(E) * H;
+    if ((rc = make_map(&maps[0], w_gate, EF, H, kTileM, "w_gate"))) return rc;
+    if ((rc = make_map(&maps[1], w_up, EF, H, kTileM, "w_up"))) return rc;
+    if ((rc = make_map(&maps[2], w_down, EH, F, kTileM, "w_down"))) return rc;
+    if ((rc = make_map(&maps[3], a.xp, L.Tk, H, kBBoxRows, "permuted x"))) return rc;
+    if ((rc = make_map(&maps[4], a.h, L.Tk, F, kBBoxRows, "h"))) return rc;
+    cudaError_t e = launch_moe(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "launch of the MoE megakernel");
+    return ET_OK;
+}
+
+size_t et_splitk_workspace_bytes(int M_max, int N, int K, int split) {
+    if (M_max < 1 || N < 128 || N % 128 || split < 1 || split > 16 || K < 64 || K % (64 * split))
+        return 0;
+    return splitk_layout(M_max, N, K, split).total;
+}
+
+int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t* d_M, int M_max,
+                   int N, int K, int split, void* workspace, size_t workspace_bytes,
+                   const et_opts* opts, void* stream) {
+    g_last_error.clear();
+    if (M_max < 1 || M_max > (1 << 20)) return fail(ET_ERR_INVALID, "M_max must be in [1, 2^20]");
+    if (N < 128 || N % 128 || N > (1 << 20))
+        return fail(ET_ERR_UNSUPPORTED, "N must be a positive multiple of 128");
+    if (split < 1 || split > 16) return fail(ET_ERR_UNSUPPORTED, "split must be in [1, 16]");
+    if (K < 64 || K % (64 * split) || K > (1 << 22))
+        return fail(ET_ERR_UNSUPPORTED, "K must be a positive multiple of 64*split");
+    if (!X || !Wt || !Y) return fail(ET_ERR_INVALID, "X, Wt and Y must be non-NULL");
+    if (!aligned<void>(X, 16) || !aligned<void>(Wt, 16) || !aligned<void>(Y, 16))
+        return fail(ET_ERR_INVALID, "tensors must be 16-byte aligned");
+    if (!d_M && (M < 0 || M > M_max)) return fail(ET_ERR_INVALID, "M must be in [0, M_max]");
+    const SplitKLayout L = splitk_layout(M_max, N, K, split);
+    int rc = check_ws(workspace, workspace_bytes, L.total);
+    if (rc) return rc;
+    if (!d_M && M == 0) return ET_OK;
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st, nullptr))) return rc;
+    const int stages = stages_for(kWideNMax);
+    const int smem = smem_bytes_for(stages, kWideNMax);
+    if (!st->splitk) {
+        cudaError_t e = prepare_splitk(smem);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(splitk)");
+        st->splitk = true;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    SplitKArgs a{};
+    a.Y = static_cast<bf16*>(Y);
+    a.d_M = d_M;
+    a.M_host = M;
+    a.M_max = M_max;
+    a.N = N;
+    a.K = K;
+    a.split = split;
+    a.hdr = reinterpret_cast<EtHeader*>(ws);
+    a.ev = reinterpret_cast<int32_t*>(ws + L.ev);
+    a.partial = reinterpret_cast<float*>(ws + L.partial);
+    a.stages = stages;
+    a.num_ctas = st->sms;
+    a.timeout_ns = timeout_ns_of(opts);
+    a.fault_mode = opts ? opts->fault_mode : 0;
+    a.fault_arg = opts ? opts->fault_arg : 0;
+    CUtensorMap maps[2];
+    if ((rc = make_map(&maps[0], Wt, N, K, kTileM, "Wt"))) return rc;
+    if ((rc = make_map(&maps[1], X, M_max, K, kBBoxRows, "X"))) return rc;
+    cudaError_t e = launch_splitk(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "launch of the split-K kernel");
+    return ET_OK;
+}
+
+size_t et_mlp_workspace_bytes(int B_max, int H, int F) {
+    if (B_max < 1 || B_max > 65536 || H < 128 || H % 128 || F < 128 || F % 128) return 0;
+    return mlp_layout(B_max, H, F).total;
+}
+
+int et_mlp_chain(const void* x, const void* gamma, float eps, const void* w_gate, const void* w_up,
+                 const void* w_down, void* out, int B, const int32_t* d_B, int B_max, int H, int F,
+                 void* workspace, size_t workspace_bytes, const et_opts* opts, void* stream) {
+    g_last_error.clear();
+    if (B_max < 1 || B_max > 65536) return fail(ET_ERR_INVALID, "B_max must be in [1, 65536]");
+    if (H < 128 || H % 128 || F < 128 || F % 128 || H > 65536 || F > 65536)
+        return fail(ET_ERR_UNSUPPORTED, "H and F must be positive multiples of 128 (<= 65536)");
+    if (!x || !gamma || !w_gate || !w_up || !w_down || !out)
+        return fail(ET_ERR_INVALID, "x, gamma, w_gate, w_up, w_down and out must be non-NULL");
+    const void* need16[] = {x, gamma, w_gate, w_up, w_down, out};
+    for (const void* p : need16)
+        if (!aligned<void>(p, 16)) return fail(ET_ERR_INVALID, "tensors must be 16-byte aligned");
+    if (!(eps >= 0.0f)) return fail(ET_ERR_INVALID, "eps must be >= 0");
+    if (!d_B && (B < 0 || B > B_max)) return fail(ET_ERR_INVALID, "B must be in [0, B_max]");
+    const MlpLayout L = mlp_layout(B_max, H, F);
+    int rc = check_ws(workspace, workspace_bytes, L.total);
+    if (rc) return rc;
+    if (!d_B && B == 0) return ET_OK;
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st, nullptr))) return rc;
+    const int stages = stages_for(kWideNMax);
+    const int smem = smem_bytes_for(stages, kWideNMax);
+    if (!st->mlp) {
+        cudaError_t e = prepare_mlp(smem);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(mlp)");
+        st->mlp = true;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    MlpArgs a{};
+    a.x = static_cast<const bf16*>(x);
+    a.gamma = static_cast<const bf16*>(gamma);
+    a.eps = eps;
+    a.out = static_cast<bf16*>(out);
+    a.d_B = d_B;
+    a.B_host = B;
+    a.B_max = B_max;
+    a.H = H;
+    a.F = F;
+    a.hdr = reinterpret_cast<EtHeader*>(ws);
+    a.xhat = reinterpret_cast<bf16*>(ws + L.xhat);
+    a.h = reinterpret_cast<bf16*>(ws + L.h);
+    a.ev_h = reinterpret_cast<int32_t*>(ws + L.ev_h);
+    a.ev_y = reinterpret_cast<int32_t*>(ws + L.ev_y);
+    a.partial = reinterpret_cast<float*>(ws + L.partial);
+    a.mt_max = L.mt_max;
+    a.stages = stages;
+    a.num_ctas = st->sms;
+    a.timeout_ns = timeout_ns_of(opts);
+    a.fault_mode = opts ? opts->fault_mode : 0;
+    a.fault_arg = opts ? opts->fault_arg : 0;
+    CUtensorMap maps[5];
+    if ((rc = make_map(&maps[0], w_gate, F, H, kTileM, "w_gate"))) return rc;
+    if ((rc = make_map(&maps[1], w_up, F, H, kTileM, "w_up"))) return rc;
+    if ((rc = make_map(&maps[2], w_down, H, F, kTileM, "w_down"))) return rc;
+    if ((rc = make_map(&maps[3], a.xhat, B_max, H, kBBoxRows, "xhat"))) return rc;
+    if ((rc = make_map(&maps[4], a.h, B_max, F, kBBoxRows, "h"))) return rc;
+    cudaError_t e = launch_mlp(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "launch of the MLP chain kernel");
+    return ET_OK;
+}
+
+int et_status(const void* workspace, void* stream, int32_t* code_out, int32_t* detail_out) {
+    g_last_error.clear();
+    if (!workspace || !code_out) return fail(ET_ERR_INVALID, "workspace and code_out must be non-NULL");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    int32_t word[2] = {0, 0};
+    e = cudaMemcpy(word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpy(status)");
+    *code_out = word[0];
+    if (detail_out) *detail_out = word[1];
+    return ET_OK;
+}
+
+int et_reset_status(void* workspace, void* stream) {
+    g_last_error.clear();
+    if (!workspace) return fail(ET_ERR_INVALID, "workspace is NULL");
+    cudaError_t e = cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    return ET_OK;
+}
+
+}  // extern "C"

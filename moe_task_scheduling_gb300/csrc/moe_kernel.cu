@@ -1,0 +1,573 @@
+// moe_kernel.cu -- the MoE layer as one persistent megakernel whose tiled
+// tasks are ordered by device-resident event counters, not kernel boundaries.
+//
+// Task graph (one dynamic queue, popped with an atomic head; index order is
+// a topological order, so every wait is on a task that a live CTA already
+// popped -- the grid is cooperative, all CTAs are resident):
+//   [0, R)      ROUTER r   fixed-order fp32 logits, top-k, gate weights and
+//                          a per-tile expert histogram;       releases ev_router
+//   R           SCAN       waits ev_router >= R (target computed from the
+//                          device token count), builds counts, offsets, the
+//                          expert row tiles and the split of the down
+//                          projection, then fills the queue:
+//   queue:      PERMUTE r  stable scatter of the tile's rows; releases ev_perm
+//               GATEUP g,f SwiGLU tile of expert row-tile g, F-tile f
+//                          (waits ev_perm >= R); releases ev_h[g][chunk(f)]
+//               DOWN g,s,n down-projection tile, F-chunk s (waits
+//                          ev_h[g][s] >= F-tiles per chunk); with a split the
+//                          last arriver on ev_y[g][n] sums the fp32 partials
+//                          in chunk order; releases ev_ydone
+//               COMBINE c  waits ev_ydone >= tiles, out = sum_j w * y.
+//
+// Sources: "Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
+// Kernels" (MoE routing gives data-dependent event counters that trigger
+// tasks; split-K partials summed through events; symbolic batch size) and
+// "Megakernels ch. 5 - Event Tensor et le dynamisme" section 5.5 (targets
+// computed on the GPU before waiting; online balancing with atomics).
+#include "et_gemm.cuh"
+
+namespace et {
+
+struct MoeMaps {
+    const CUtensorMap* wg;
+    const CUtensorMap* wu;
+    const CUtensorMap* wd;
+    const CUtensorMap* xp;
+    const CUtensorMap* h;
+};
+
+__device__ __forceinline__ void unpack8(const uint4& raw, float (&v)[8]) {
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b2[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+    uint4 raw;
+    __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b2[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    return raw;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+// ------------------------------------------------------------------ ROUTER
+
+// Logits of up to 16 tokens against all E experts.  Lane l of a warp owns
+// partial sum l of 8 tokens x 8 experts and accumulates h = l, l+32, ... in
+// ascending order with fp32 fma (exact bf16 products, so fma == mul+add);
+// the halving shuffle tree (16, 8, 4, 2, 1) then adds p[l] + p[l+off].  This
+// is the fixed order that makes routing bit-reproducible.
+__device__ __noinline__ void router_task(const MoeArgs& p, int T, int r, uint8_t* smem) {
+    const int E = p.E, H = p.H, k = p.k;
+    float* lg = reinterpret_cast<float*>(smem);                                // [16][E]
+    int* hs = reinterpret_cast<int*>(smem + kRouterTile * 256 * sizeof(float));  // [E]
+    const int t0 = r * kRouterTile, nt = min(kRouterTile, T - t0);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int e = threadIdx.x; e < E; e += kThreads) hs[e] = 0;
+    const int neb = ceil_div(E, 8), ntb = ceil_div(nt, 8);
+    const bool vec = (E % 8) == 0;
+    for (int job = warp; job < neb * ntb; job += kThreads / 32) {
+        const int tb = job / neb, eb = job % neb;
+        const int tbase = t0 + tb * 8, ebase = eb * 8;
+        const int tn = min(8, t0 + nt - tbase), en = min(8, E - ebase);
+        float acc[8][8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+#pragma unroll
+            for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
+        const bf16* xrow = p.x + static_cast<size_t>(tbase) * H;
+        for (int h = lane; h < H; h += 32) {
+            float wv[8];
+            if (vec) {
+                const uint4 raw =
+                    __ldg(reinterpret_cast<const uint4*>(p.wr + static_cast<size_t>(h) * E + ebase));
+                unpack8(raw, wv);
+            } else {
+#pragma unroll
+                for (int b = 0; b < 8; ++b)
+                    wv[b] = b < en ? bf2f(p.wr[static_cast<size_t>(h) * E + ebase + b]) : 0.0f;
+            }
+#pragma unroll
+            for (int a = 0; a < 8; ++a) {
+                const float xv = a < tn ? bf2f(xrow[static_cast<size_t>(a) * H + h]) : 0.0f;
+#pragma unroll
+                for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xv, wv[b], acc[a][b]);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int b = 0; b < 8; ++b)
+                    acc[a][b] = acc[a][b] + __shfl_down_sync(0xffffffffu, acc[a][b], off);
+        if (lane == 0) {
+            for (int a = 0; a < tn; ++a)
+                for (int b = 0; b < en; ++b) {
+                    float L = acc[a][b];
+                    if (p.bias) L = L + p.bias[ebase + b];
+                    lg[(tb * 8 + a) * E + ebase + b] = L;
+                }
+        }
+    }
+    __syncthreads();
+    // top-k per token (warp per token): order (logit desc, index asc)
+    for (int tt = warp; tt < nt; tt += kThreads / 32) {
+        const float* L = lg + tt * E;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? L[e] : 0.0f;
+        }
+        uint32_t taken = 0;
+        float selL[8];
+        int selE[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j >= k) break;
+            float bv = 0.0f;
+            int be = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !((taken >> i) & 1u)) {
+                    if (be == 0x7fffffff || v[i] > bv || (v[i] == bv && e < be)) {
+                        bv = v[i];
+                        be = e;
+                    }
+                }
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                if (oe != 0x7fffffff &&
+                    (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            selL[j] = bv;
+            selE[j] = be;
+        }
+        if (lane == 0) {
+            const int t = t0 + tt;
+            float ex[8], z = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= k) break;
+                ex[j] = expf(selL[j] - selL[0]);
+                z += ex[j];
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= k) break;
+                p.idx[static_cast<size_t>(t) * k + j] = selE[j];
+                p.gw[static_cast<size_t>(t) * k + j] = ex[j] / z;
+                atomicAdd(&hs[selE[j]], 1);
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) p.hist[static_cast<size_t>(r) * E + e] = hs[e];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        red_release_add(&p.hdr->ev_router, 1);
+    }
+}
+
+// ------------------------------------------------------------------ SCAN
+
+// Counts, offsets, expert row tiles, split choice, and the task queue.  The
+// targets the later waits use (R permute tiles; F-tiles per chunk; the total
+// number of output tiles) are all derived here, on the device, from the
+// routing of this very call.
+__device__ __noinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem, Ctl* ctl,
+                                       const WaitCtx& wc) {
+    const int E = p.E, k = p.k, R = ceil_div(T, kRouterTile);
+    if (threadIdx.x == 0) ctl->flag = ev_wait_geq(wc, &p.hdr->ev_router, R, kWhereRouter) ? 1 : 0;
+    __syncthreads();
+    if (!ctl->flag) return false;
+    int* cnt_s = reinterpret_cast<int*>(smem);  // [256]
+    int* off_s = cnt_s + 256;                   // [257]
+    int* n_s = off_s + 264;                     // [256]
+    int* mtb_s = n_s + 256;                     // [257]
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        int run = 0;
+        for (int r = 0; r < R; ++r) {
+            const int c = __ldcg(p.hist + static_cast<size_t>(r) * E + e);
+            p.base[static_cast<size_t>(r) * E + e] = run;
+            run += c;
+        }
+        cnt_s[e] = run;
+    }
+    __syncthreads();
+    const int FT = p.F / kTileM, HT = p.H / kTileM;
+    if (threadIdx.x == 0) {
+        off_s[0] = 0;
+        mtb_s[0] = 0;
+        for (int e = 0; e < E; ++e) {
+            const int c = cnt_s[e];
+            off_s[e + 1] = off_s[e] + c;
+            const int n = c == 0 ? 0 : min(kMoeNMax, (c + 15) / 16 * 16);
+            n_s[e] = n;
+            mtb_s[e + 1] = mtb_s[e] + (c == 0 ? 0 : ceil_div(c, n));
+        }
+        const int total_mt = mtb_s[E];
+        int S = 1;
+        if (T * k <= p.split_rows_cap && total_mt > 0) {
+            const int down = total_mt * HT;
+            int best = 1;
+            for (int d = 2; d <= kSplitMax; ++d) {
+                if (FT % d) continue;
+                best = d;
+                if (down * d >= p.num_ctas) break;
+            }
+            S = best;
+        }
+        ctl->scratch[0] = total_mt;
+        ctl->scratch[1] = S;
+    }
+    __syncthreads();
+    const int total_mt = ctl->scratch[0], S = ctl->scratch[1];
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        p.cnt[e] = cnt_s[e];
+        p.off[e] = off_s[e];
+        if (e == E - 1) p.off[E] = off_s[E];
+        for (int r = 0; r < R; ++r) p.base[static_cast<size_t>(r) * E + e] += off_s[e];
+        const int n = n_s[e];
+        for (int g = mtb_s[e], mt = 0; g < mtb_s[e + 1]; ++g, ++mt) {
+            p.g_expert[g] = e;
+            p.g_row0[g] = off_s[e] + mt * n;
+            p.g_rows[g] = min(n, cnt_s[e] - mt * n);
+            p.g_n[g] = n;
+        }
+    }
+    const int n_perm = R, n_gu = total_mt * FT, n_dn = total_mt * S * HT,
+              n_cb = ceil_div(T, kCombineTile);
+    const int total = n_perm + n_gu + n_dn + n_cb;
+    if (total > p.q_max) {  // cannot happen for a valid workspace; fail loudly
+        if (threadIdx.x == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereQueue);
+        return false;
+    }
+    for (int q = threadIdx.x; q < total; q += kThreads) {
+        int4 d;
+        if (q < n_perm) {
+            d = make_int4(kTaskPermute, q, 0, 0);
+        } else if (q < n_perm + n_gu) {
+            const int i = q - n_perm;
+            d = make_int4(kTaskGateUp, i / FT, i % FT, 0);
+        } else if (q < n_perm + n_gu + n_dn) {
+            const int i = q - n_perm - n_gu;
+            const int g = i / (S * HT), rem = i % (S * HT);
+            d = make_int4(kTaskDown, g, rem / HT, rem % HT);
+        } else {
+            d = make_int4(kTaskCombine, q - n_perm - n_gu - n_dn, 0, 0);
+        }
+        p.queue[q] = d;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        p.hdr->total_mt = total_mt;
+        p.hdr->split = S;
+        p.hdr->q_total = total;
+        __threadfence();
+        st_release(&p.hdr->q_ready, 1);
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ PERMUTE
+
+// Stable dispatch of router tile r: row (t, j) goes to off[e] + (rank of t
+// among this call's tokens routed to e), and its x row is copied there.
+__device__ __noinline__ void permute_task(const MoeArgs& p, int T, int r, uint8_t* smem) {
+    const int k = p.k, E = p.E, H = p.H;
+    const int t0 = r * kRouterTile, nt = min(kRouterTile, T - t0), nent = nt * k;
+    int* ie = reinterpret_cast<int*>(smem);  // [128]
+    int* slot = ie + 128;                    // [128]
+    for (int i = threadIdx.x; i < nent; i += kThreads)
+        ie[i] = __ldcg(p.idx + static_cast<size_t>(t0) * k + i);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nent; i += kThreads) {
+        const int e = ie[i], tl = i / k;
+        int rank = 0;
+        for (int i2 = 0; i2 < tl * k; ++i2) rank += (ie[i2] == e);
+        const int pp = __ldcg(p.base + static_cast<size_t>(r) * E + e) + rank;
+        p.perm[pp] = t0 * k + i;
+        p.pos[static_cast<size_t>(t0) * k + i] = pp;
+        slot[i] = pp;
+    }
+    __syncthreads();
+    const int vpr = H / 8;
+    for (int v = threadIdx.x; v < nent * vpr; v += kThreads) {
+        const int i = v / vpr, c = v % vpr;
+        const int t = t0 + i / k;
+        const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H) + c);
+        reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(slot[i]) * H)[c] = val;
+    }
+    fence_proxy_async_global();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        red_release_add(&p.hdr->ev_perm, 1);
+    }
+}
+
+// ------------------------------------------------------------------ COMBINE
+
+__device__ __noinline__ bool combine_task(const MoeArgs& p, int T, int c, Ctl* ctl,
+                                          const WaitCtx& wc) {
+    const int H = p.H, k = p.k;
+    if (threadIdx.x == 0) {
+        const int target = ld_relaxed(&p.hdr->total_mt) * (H / kTileM);
+        ctl->flag = ev_wait_geq(wc, &p.hdr->ev_ydone, target, kWhereY) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!ctl->flag) return false;
+    const int t0 = c * kCombineTile, nt = min(kCombineTile, T - t0), vpr = H / 8;
+    for (int v = threadIdx.x; v < nt * vpr; v += kThreads) {
+        const int t = t0 + v / vpr, cc = v % vpr;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const float wj = __ldcg(p.gw + static_cast<size_t>(t) * k + j);
+            const int row = __ldcg(p.pos + static_cast<size_t>(t) * k + j);
+            const uint4 raw = __ldcg(reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(row) * H) + cc);
+            float yv[8];
+            unpack8(raw, yv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, yv[i], acc[i]);
+        }
+        reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * H)[cc] = pack8(acc);
+    }
+    __syncthreads();
+    return true;
+}
+
+// ------------------------------------------------------------------ queue pop
+
+__device__ __noinline__ int4 pop_task(const MoeArgs& p, const WaitCtx& wc, int R) {
+    const int4 none = make_int4(kTaskExit, 0, 0, 0);
+    if (aborted(wc)) return none;
+    const int i = atomicAdd(&p.hdr->q_head, 1);
+    if (i < R) return make_int4(kTaskRouter, i, 0, 0);
+    if (i == R) return make_int4(kTaskScan, 0, 0, 0);
+    const int j = i - R - 1;
+    if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return none;
+    if (j >= ld_relaxed(&p.hdr->q_total)) return none;
+    return __ldcg(p.queue + j);
+}
+
+// ------------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+moe_megakernel(const __grid_constant__ MoeArgs p, const __grid_constant__ CUtensorMap tm_wg,
+               const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ CUtensorMap tm_wd,
+               const __grid_constant__ CUtensorMap tm_xp, const __grid_constant__ CUtensorMap tm_h) {
+    extern __shared__ uint8_t smem_raw[];
+    Ring ring;
+    Ctl* ctl = cta_setup(smem_raw, p.stages, kMoeNMax, ring);
+    const WaitCtx wc{p.hdr, p.timeout_ns};
+    const MoeMaps maps{&tm_wg, &tm_wu, &tm_wd, &tm_xp, &tm_h};
+    const uint32_t tmem = ctl->tmem_base;
+    Pipe pipe;
+
+    int T = p.d_T ? *reinterpret_cast<const volatile int32_t*>(p.d_T) : p.T_host;
+    if (T < 0 || T > p.T_max) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereBoundsT);
+        T = 0;
+    }
+    const int R = ceil_div(T, kRouterTile);
+    const int FT = p.F / kTileM, HT = p.H / kTileM;
+    if (threadIdx.x == 0) {
+        tma_prefetch_map(&tm_wg);
+        tma_prefetch_map(&tm_wu);
+        tma_prefetch_map(&tm_wd);
+        tma_prefetch_map(&tm_xp);
+        tma_prefetch_map(&tm_h);
+    }
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_b = policy_evict_last();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    (void)warp;
+    (void)lane;
+
+    bool ok = true;
+    for (;;) {
+        if (threadIdx.x == 0) {
+            ctl->fail = 0;
+            ctl->task = pop_task(p, wc, R);
+        }
+        __syncthreads();
+        const int4 tk = ctl->task;
+        if (tk.x == kTaskExit) break;
+
+        if (tk.x == kTaskRouter) {
+            router_task(p, T, tk.y, ring.base);
+        } else if (tk.x == kTaskScan) {
+            if (!scan_task(p, T, ring.base, ctl, wc)) ok = false;
+        } else if (tk.x == kTaskPermute) {
+            permute_task(p, T, tk.y, ring.base);
+        } else if (tk.x == kTaskCombine) {
+            if (!combine_task(p, T, tk.y, ctl, wc)) ok = false;
+        } else if (tk.x == kTaskGateUp) {
+            const int g = tk.y, ft = tk.z;
+            const int e = __ldcg(p.g_expert + g), row0 = __ldcg(p.g_row0 + g);
+            const int rows = __ldcg(p.g_rows + g), n = __ldcg(p.g_n + g);
+            const int S = ld_relaxed(&p.hdr->split);
+            GemmTask t{maps.wg, maps.wu, maps.xp, e * p.F + ft * kTileM, row0, 0, p.H / kBlockK,
+                       n, 1, &p.hdr->ev_perm, R, kWherePerm};
+            const int F = p.F;
+            bf16* hout = p.h;
+            ok = run_gemm_task(t, ctl, ring, pipe, tmem, wc, pol_w, pol_b, [&](int q, int ln) {
+                const int f = ft * kTileM + q * 32 + ln;
+                const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+                for (int c0 = 0; c0 < n; c0 += 16) {
+                    float gv[16], uv[16];
+                    tmem_ld16(lane_base + c0, gv);
+                    tmem_ld16(lane_base + kAcc1Col + c0, uv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        if (c0 + c < rows)
+                            hout[static_cast<size_t>(row0 + c0 + c) * F + f] =
+                                __float2bfloat16_rn(silu_mul(gv[c], uv[c]));
+                }
+                fence_proxy_async_global();
+            });
+            if (ok && threadIdx.x == 0) {
+                const bool skip = p.fault_mode == 1 && g * FT + ft == p.fault_arg;
+                __threadfence();
+                if (!skip) red_release_add(&p.ev_h[g * kSplitMax + ft / (FT / S)], 1);
+            }
+        } else if (tk.x == kTaskDown) {
+            const int g = tk.y, s = tk.z, ht = tk.w;
+            const int e = __ldcg(p.g_expert + g), row0 = __ldcg(p.g_row0 + g);
+            const int rows = __ldcg(p.g_rows + g), n = __ldcg(p.g_n + g);
+            const int S = ld_relaxed(&p.hdr->split);
+            const int fchunk = p.F / S;
+            GemmTask t{maps.wd, nullptr, maps.h, e * p.H + ht * kTileM, row0,
+                       s * (fchunk / kBlockK), fchunk / kBlockK, n, n <= 64 ? 2 : 1,
+                       &p.ev_h[g * kSplitMax + s], FT / S, kWhereH};
+            const int H = p.H, cap = p.split_rows_cap;
+            bf16* yout = p.y;
+            float* part = p.partial;
+            ok = run_gemm_task(t, ctl, ring, pipe, tmem, wc, pol_w, pol_b, [&](int q, int ln) {
+                const int hh = ht * kTileM + q * 32 + ln;
+                const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+                for (int c0 = 0; c0 < n; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(lane_base + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        if (c0 + c >= rows) continue;
+                        const size_t row = static_cast<size_t>(row0 + c0 + c);
+                        if (S == 1)
+                            yout[row * H + hh] = __float2bfloat16_rn(v[c]);
+                        else
+                            part[(static_cast<size_t>(s) * cap + row) * H + hh] = v[c];
+                    }
+                }
+            });
+            if (ok) {
+                if (S > 1) {
+                    if (threadIdx.x == 0) {
+                        __threadfence();
+                        const int old = atom_acq_rel_add(&p.ev_y[g * HT + ht], 1);
+                        ctl->flag = (old == S - 1) ? 1 : 0;
+                    }
+                    __syncthreads();
+                    if (ctl->flag) {  // last arriver: sum partials in chunk order
+                        for (int i = threadIdx.x; i < rows * kTileM; i += kThreads) {
+                            const size_t row = static_cast<size_t>(row0 + i / kTileM);
+                            const int hh = ht * kTileM + (i % kTileM);
+                            float sum = 0.0f;
+                            for (int s2 = 0; s2 < S; ++s2)
+                                sum += __ldcg(part + (static_cast<size_t>(s2) * cap + row) * H + hh);
+                            yout[row * H + hh] = __float2bfloat16_rn(sum);
+                        }
+                        __syncthreads();
+                        if (threadIdx.x == 0) {
+                            __threadfence();
+                            red_release_add(&p.hdr->ev_ydone, 1);
+                        }
+                    }
+                } else if (threadIdx.x == 0) {
+                    __threadfence();
+                    red_release_add(&p.hdr->ev_ydone, 1);
+                }
+            }
+        }
+        __syncthreads();
+        if (ctl->fail) ok = false;
+        if (!ok) break;
+    }
+
+    if (!ok) drain_after_failure(ctl, ring, pipe);
+    cta_teardown(ctl);
+
+    // Exit protocol: the last CTA out returns every counter to zero.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        ctl->flag = (atomicAdd(&p.hdr->exit_count, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (ctl->flag) {
+        __threadfence();
+        const bool clean = ld_relaxed(&p.hdr->abort) == 0 && ld_relaxed(&p.hdr->q_ready) != 0;
+        const int mt = clean ? ld_relaxed(&p.hdr->total_mt) : p.mt_max;
+        for (int i = threadIdx.x; i < mt * kSplitMax; i += kThreads) p.ev_h[i] = 0;
+        for (int i = threadIdx.x; i < mt * HT; i += kThreads) p.ev_y[i] = 0;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            EtHeader* hd = p.hdr;
+            hd->q_head = 0;
+            hd->q_ready = 0;
+            hd->q_total = 0;
+            hd->total_mt = 0;
+            hd->ev_router = 0;
+            hd->ev_perm = 0;
+            hd->ev_ydone = 0;
+            hd->split = 0;
+            hd->abort = 0;
+            __threadfence();
+            hd->exit_count = 0;
+        }
+    }
+}
+
+// Host-side launch (called by the C ABI after validation).
+cudaError_t launch_moe(const MoeArgs& a, const CUtensorMap* maps, int grid, int smem,
+                       cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_megakernel, a, maps[0], maps[1], maps[2], maps[3],
+                              maps[4]);
+}
+
+cudaError_t prepare_moe(int smem) {
+    return cudaFuncSetAttribute(moe_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+}  // namespace et
