@@ -86,6 +86,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -210,6 +214,11 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Named barrier among `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -235,7 +244,7 @@ __device__ __forceinline__ void raise_error(const WaitCtx& c, int code, int deta
 
 // Spin (with back-off) until *ctr >= target.  Returns false if the budget ran
 // out (records ET_ERR_TIMEOUT with `where`) or another CTA aborted.
-static __device__ __noinline__ bool ev_wait_geq(const WaitCtx& c, const int* ctr, int target, int where) {
+__device__ __forceinline__ bool ev_wait_geq(const WaitCtx& c, const int* ctr, int target, int where) {
     if (ld_acquire(ctr) >= target) return true;
     const uint64_t t0 = globaltimer_ns();
     uint32_t ns = 32;
@@ -252,7 +261,7 @@ static __device__ __noinline__ bool ev_wait_geq(const WaitCtx& c, const int* ctr
 }
 
 // Bounded mbarrier phase wait (same contract as ev_wait_geq).
-static __device__ __noinline__ bool mbar_wait(const WaitCtx& c, uint64_t* bar, uint32_t parity,
+__device__ __forceinline__ bool mbar_wait(const WaitCtx& c, uint64_t* bar, uint32_t parity,
                                        int where) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -270,7 +279,7 @@ static __device__ __noinline__ bool mbar_wait(const WaitCtx& c, uint64_t* bar, u
 
 // Wait without raising: used while unwinding after an abort, with a short
 // budget, to let this CTA's own copies and MMAs land before it exits.
-static __device__ __noinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
         if (globaltimer_ns() - t0 > budget_ns) return false;

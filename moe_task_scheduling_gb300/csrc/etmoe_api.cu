@@ -12,10 +12,16 @@
 namespace et {
 cudaError_t launch_moe(const MoeArgs&, const CUtensorMap*, int, int, cudaStream_t);
 cudaError_t prepare_moe(int);
+int moe_stages();
+int moe_smem_bytes();
 cudaError_t launch_splitk(const SplitKArgs&, const CUtensorMap*, int, int, cudaStream_t);
 cudaError_t prepare_splitk(int);
+int splitk_stages();
+int splitk_smem_bytes();
 cudaError_t launch_mlp(const MlpArgs&, const CUtensorMap*, int, int, cudaStream_t);
 cudaError_t prepare_mlp(int);
+int mlp_stages();
+int mlp_smem_bytes();
 }  // namespace et
 
 using namespace et;
@@ -108,12 +114,6 @@ int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uin
 uint64_t timeout_ns_of(const et_opts* o) {
     const uint32_t us = (o && o->timeout_us) ? o->timeout_us : 200000u;
     return static_cast<uint64_t>(us) * 1000ull;
-}
-
-int stages_for(int nmax) {
-    const int avail = kSmemLimit - 1024 - static_cast<int>(sizeof(Ctl));
-    int s = avail / stage_bytes(nmax);
-    return s > kMaxStages ? kMaxStages : s;
 }
 
 struct Carve {
@@ -258,8 +258,8 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
 
     DeviceState* st = nullptr;
     if ((rc = device_state(&st, nullptr))) return rc;
-    const int stages = stages_for(kMoeNMax);
-    const int smem = smem_bytes_for(stages, kMoeNMax);
+    const int stages = moe_stages();
+    const int smem = moe_smem_bytes();
     if (!st->moe) {
         cudaError_t e = prepare_moe(smem);
         if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(moe)");
@@ -346,8 +346,8 @@ int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t*
     if (!d_M && M == 0) return ET_OK;
     DeviceState* st = nullptr;
     if ((rc = device_state(&st, nullptr))) return rc;
-    const int stages = stages_for(kWideNMax);
-    const int smem = smem_bytes_for(stages, kWideNMax);
+    const int stages = splitk_stages();
+    const int smem = splitk_smem_bytes();
     if (!st->splitk) {
         cudaError_t e = prepare_splitk(smem);
         if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(splitk)");
@@ -403,8 +403,8 @@ int et_mlp_chain(const void* x, const void* gamma, float eps, const void* w_gate
     if (!d_B && B == 0) return ET_OK;
     DeviceState* st = nullptr;
     if ((rc = device_state(&st, nullptr))) return rc;
-    const int stages = stages_for(kWideNMax);
-    const int smem = smem_bytes_for(stages, kWideNMax);
+    const int stages = mlp_stages();
+    const int smem = mlp_smem_bytes();
     if (!st->mlp) {
         cudaError_t e = prepare_mlp(smem);
         if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(mlp)");

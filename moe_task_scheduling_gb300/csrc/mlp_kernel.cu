@@ -8,9 +8,10 @@
 //   [NR, NR + MT*FT)        GATEUP m,f  waits ev_norm >= NR; releases ev_h[m][chunk(f)]
 //   [.., + MT*S*HT)         DOWN m,s,n  waits ev_h[m][s] >= F-tiles per chunk;
 //                                       split partials meet on ev_y[m][n]
-// so every wait is on a lower index, which a resident CTA reaches first.
-// The targets (NR, F-tiles per chunk) are computed on the device from the
-// batch size, which may itself be read from device memory.
+// so every wait is on a lower index, which a resident CTA reaches first (the
+// launch is cooperative: all CTAs are resident).  The targets (NR, F-tiles
+// per chunk) are computed on the device from the batch size, which may itself
+// be read from device memory.
 //
 // Source: "Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
 // Kernels" -- static scheduling is the right choice for predictable dense
@@ -19,13 +20,49 @@
 
 namespace et {
 
-constexpr int kNormRows = 8;  // one warp per row
+constexpr int kNormRows = 8;  // two rows per worker warp
 
-__device__ __noinline__ void norm_task(const MlpArgs& p, int B, int i) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = i * kNormRows + warp;
+struct MlpPlan {
+    int B, NR, MT, FT, HT, S, n_gu, n_dn, total, nbuf;
+    uint32_t u_off;
+};
+
+struct MlpTile {
+    int kind;  // 0 norm, 1 gate/up, 2 down
+    int i, mt, ft, s, ht, rows, n;
+};
+
+__device__ __forceinline__ MlpTile mlp_tile(const MlpPlan& P, int task) {
+    MlpTile t{};
+    if (task < P.NR) {
+        t.kind = 0;
+        t.i = task;
+        return t;
+    }
+    if (task < P.NR + P.n_gu) {
+        t.kind = 1;
+        t.i = task - P.NR;
+        t.mt = t.i / P.FT;
+        t.ft = t.i % P.FT;
+    } else {
+        t.kind = 2;
+        t.i = task - P.NR - P.n_gu;
+        t.mt = t.i / (P.S * P.HT);
+        const int rem = t.i % (P.S * P.HT);
+        t.s = rem / P.HT;
+        t.ht = rem % P.HT;
+    }
+    t.rows = min(kWideNMax, P.B - t.mt * kWideNMax);
+    t.n = (t.rows + 15) / 16 * 16;
+    return t;
+}
+
+__device__ __forceinline__ void norm_rows(const MlpArgs& p, int B, int i) {
+    const int wwarp = (threadIdx.x >> 5) - kEpiWarp0, lane = threadIdx.x & 31;
     const int H = p.H;
-    if (row < B) {
+    for (int r = 0; r < kNormRows / (kWorkers / 32); ++r) {
+        const int row = i * kNormRows + wwarp * (kNormRows / (kWorkers / 32)) + r;
+        if (row >= B) break;
         const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(row) * H);
         float ss = 0.0f;
         for (int c = lane; c < H / 8; c += 32) {
@@ -58,148 +95,167 @@ __device__ __noinline__ void norm_task(const MlpArgs& p, int B, int i) {
             outr[c] = o;
         }
     }
-    fence_proxy_async_global();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        red_release_add(&p.hdr->ev_norm, 1);
-    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-mlp_chain_kernel(const __grid_constant__ MlpArgs p, const __grid_constant__ CUtensorMap tm_wg,
-                 const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ CUtensorMap tm_wd,
-                 const __grid_constant__ CUtensorMap tm_xhat,
-                 const __grid_constant__ CUtensorMap tm_h) {
+mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
+                 const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xhat,
+                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ MlpArgs p) {
     extern __shared__ uint8_t smem_raw[];
-    Ring ring;
-    Ctl* ctl = cta_setup(smem_raw, p.stages, kWideNMax, ring);
+    Stages stg;
+    uint8_t* scratch;
+    Ctl* ctl = cta_setup(smem_raw, p.stages, kWideNMax, 0, stg, &scratch);
     const WaitCtx wc{p.hdr, p.timeout_ns};
     const uint32_t tmem = ctl->tmem_base;
-    Pipe pipe;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    int B = p.d_B ? *reinterpret_cast<const volatile int32_t*>(p.d_B) : p.B_host;
-    if (B < 0 || B > p.B_max) {
+    MlpPlan P;
+    P.B = p.B_host;
+    if (p.d_B) P.B = *reinterpret_cast<const volatile int32_t*>(p.d_B);
+    if (P.B < 0 || P.B > p.B_max) {
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereBoundsT);
-        B = 0;
+        P.B = 0;
     }
-    if (threadIdx.x == 0) {
-        tma_prefetch_map(&tm_wg);
-        tma_prefetch_map(&tm_wu);
-        tma_prefetch_map(&tm_wd);
-        tma_prefetch_map(&tm_xhat);
-        tma_prefetch_map(&tm_h);
-    }
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_b = policy_evict_last();
-    const int H = p.H, F = p.F;
-    const int FT = F / kTileM, HT = H / kTileM;
-    const int NR = ceil_div(B, kNormRows);
-    const int MT = ceil_div(B, kWideNMax);
+    P.FT = p.F / kTileM;
+    P.HT = p.H / kTileM;
+    P.NR = ceil_div(P.B, kNormRows);
+    P.MT = ceil_div(P.B, kWideNMax);
     // split of the down projection: the smallest divisor of FT (<= 8) that
     // gives at least one down task per CTA, else the largest such divisor
-    int S = 1;
-    if (MT > 0) {
+    P.S = 1;
+    if (P.MT > 0) {
         for (int d = 2; d <= kSplitMax; ++d) {
-            if (FT % d) continue;
-            S = d;
-            if (MT * HT * d >= static_cast<int>(gridDim.x)) break;
+            if (P.FT % d) continue;
+            P.S = d;
+            if (P.MT * P.HT * d >= static_cast<int>(gridDim.x)) break;
         }
     }
-    const int n_gu = MT * FT, n_dn = MT * S * HT;
-    const int total = NR + n_gu + n_dn;
+    P.n_gu = P.MT * P.FT;
+    P.n_dn = P.MT * P.S * P.HT;
+    P.total = P.NR + P.n_gu + P.n_dn;
+    // two accumulator buffers when both gate/up accumulators fit in 256 columns
+    P.nbuf = P.B <= kWideNMax / 2 ? 2 : 1;
+    P.u_off = P.nbuf == 2 ? kAccBufCols / 2 : kAccBufCols;
 
-    bool ok = true;
-    for (int task = blockIdx.x; task < total; task += gridDim.x) {
-        if (threadIdx.x == 0) ctl->fail = 0;
-        __syncthreads();
-        if (task < NR) {
-            norm_task(p, B, task);
-            continue;
+    auto gemm_of = [&](const MlpTile& t) {
+        if (t.kind == 1)
+            return GemmTask{&tm_wg, &tm_wu, &tm_xhat, t.ft * kTileM, t.mt * kWideNMax, 0,
+                            p.H / kBlockK, t.n, 1, &p.hdr->ev_norm, P.NR, kWhereNorm};
+        const int fchunk = p.F / P.S;
+        return GemmTask{&tm_wd, nullptr, &tm_h, t.ht * kTileM, t.mt * kWideNMax,
+                        t.s * (fchunk / kBlockK), fchunk / kBlockK, t.n,
+                        t.n <= kWideNMax / 2 ? 2 : 1, &p.ev_h[t.mt * kSplitMax + t.s], P.FT / P.S,
+                        kWhereH};
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
+            uint32_t it = 0;
+            for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
+                const MlpTile t = mlp_tile(P, task);
+                if (t.kind == 0) continue;
+                if (!produce_task(gemm_of(t), stg, ctl, it, wc, pol_w, pol_b)) break;
+            }
         }
-        if (task < NR + n_gu) {
-            const int i = task - NR, mt = i / FT, ft = i % FT;
-            const int rows = min(kWideNMax, B - mt * kWideNMax), n = (rows + 15) / 16 * 16;
-            GemmTask t{&tm_wg, &tm_wu, &tm_xhat, ft * kTileM, mt * kWideNMax, 0, H / kBlockK, n, 1,
-                       &p.hdr->ev_norm, NR, kWhereNorm};
-            bf16* hout = p.h;
-            const int m0 = mt * kWideNMax;
-            ok = run_gemm_task(t, ctl, ring, pipe, tmem, wc, pol_w, pol_b, [&](int q, int ln) {
-                const int f = ft * kTileM + q * 32 + ln;
-                const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-                for (int c0 = 0; c0 < n; c0 += 16) {
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, g = 0;
+            for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
+                const MlpTile t = mlp_tile(P, task);
+                if (t.kind == 0) continue;
+                if (!mma_task(gemm_of(t), stg, ctl, it, g, P.nbuf, P.u_off, tmem, wc)) break;
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kEpiWarp0) {
+        const int q = warp - kEpiWarp0, wtid = threadIdx.x - kEpiWarp0 * 32;
+        const int H = p.H, F = p.F;
+        uint32_t g = 0, wseq = 0;
+        for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
+            const MlpTile t = mlp_tile(P, task);
+            if (t.kind == 0) {
+                norm_rows(p, P.B, t.i);
+                fence_proxy_async_global();
+                worker_sync();
+                if (wtid == 0) {
+                    __threadfence();
+                    red_release_add(&p.hdr->ev_norm, 1);
+                }
+                continue;
+            }
+            uint32_t acc;
+            if (!epi_acquire(ctl, g, P.nbuf, tmem, wc, acc, wseq)) break;
+            const uint32_t lane_base = acc + (static_cast<uint32_t>(q * 32) << 16);
+            const size_t m0 = static_cast<size_t>(t.mt) * kWideNMax;
+            if (t.kind == 1) {
+                const int f = t.ft * kTileM + q * 32 + lane;
+                for (int c0 = 0; c0 < t.n; c0 += 16) {
                     float gv[16], uv[16];
                     tmem_ld16(lane_base + c0, gv);
-                    tmem_ld16(lane_base + kAcc1Col + c0, uv);
+                    tmem_ld16(lane_base + P.u_off + c0, uv);
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        if (c0 + c < rows)
-                            hout[static_cast<size_t>(m0 + c0 + c) * F + f] =
+                        if (c0 + c < t.rows)
+                            p.h[(m0 + c0 + c) * F + f] =
                                 __float2bfloat16_rn(gv[c] / (1.0f + __expf(-gv[c])) * uv[c]);
                 }
-                fence_proxy_async_global();
-            });
-            if (!ok) break;
-            if (threadIdx.x == 0) {
-                const bool skip = p.fault_mode == 1 && i == p.fault_arg;
-                __threadfence();
-                if (!skip) red_release_add(&p.ev_h[mt * kSplitMax + ft / (FT / S)], 1);
+                epi_release(ctl, g, P.nbuf);
+                ++g;
+                fence_proxy_async_global();  // h is read back by TMA
+                worker_sync();
+                if (wtid == 0) {
+                    const bool skip = p.fault_mode == 1 && t.i == p.fault_arg;
+                    __threadfence();
+                    if (!skip) red_release_add(&p.ev_h[t.mt * kSplitMax + t.ft / (P.FT / P.S)], 1);
+                }
+                continue;
             }
-            continue;
-        }
-        const int i = task - NR - n_gu;
-        const int mt = i / (S * HT), rem = i % (S * HT), s = rem / HT, ht = rem % HT;
-        const int rows = min(kWideNMax, B - mt * kWideNMax), n = (rows + 15) / 16 * 16;
-        const int fchunk = F / S;
-        GemmTask t{&tm_wd, nullptr, &tm_h, ht * kTileM, mt * kWideNMax, s * (fchunk / kBlockK),
-                   fchunk / kBlockK, n, n <= kWideNMax / 2 ? 2 : 1, &p.ev_h[mt * kSplitMax + s],
-                   FT / S, kWhereH};
-        bf16* out = p.out;
-        float* part = p.partial;
-        const int m0 = mt * kWideNMax, Bmax = p.B_max;
-        ok = run_gemm_task(t, ctl, ring, pipe, tmem, wc, pol_w, pol_b, [&](int q, int ln) {
-            const int hh = ht * kTileM + q * 32 + ln;
-            const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            for (int c0 = 0; c0 < n; c0 += 16) {
+            // down projection tile
+            const int hh = t.ht * kTileM + q * 32 + lane;
+            for (int c0 = 0; c0 < t.n; c0 += 16) {
                 float v[16];
                 tmem_ld16(lane_base + c0, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    if (c0 + c >= rows) continue;
-                    const size_t m = static_cast<size_t>(m0 + c0 + c);
-                    if (S == 1)
-                        out[m * H + hh] = __float2bfloat16_rn(v[c]);
+                    if (c0 + c >= t.rows) continue;
+                    const size_t m = m0 + c0 + c;
+                    if (P.S == 1)
+                        p.out[m * H + hh] = __float2bfloat16_rn(v[c]);
                     else
-                        part[(static_cast<size_t>(s) * Bmax + m) * H + hh] = v[c];
+                        p.partial[(static_cast<size_t>(t.s) * p.B_max + m) * H + hh] = v[c];
                 }
             }
-        });
-        if (!ok) break;
-        if (S > 1) {
-            int* ev = p.ev_y + mt * HT + ht;
-            if (threadIdx.x == 0) {
-                __threadfence();
-                ctl->flag = (atom_acq_rel_add(ev, 1) == S - 1) ? 1 : 0;
-            }
-            __syncthreads();
-            if (ctl->flag) {
-                for (int j = threadIdx.x; j < rows * kTileM; j += kThreads) {
-                    const size_t m = static_cast<size_t>(m0 + j / kTileM);
-                    const int hh = ht * kTileM + (j % kTileM);
-                    float sum = 0.0f;
-                    for (int s2 = 0; s2 < S; ++s2)
-                        sum += __ldcg(part + (static_cast<size_t>(s2) * Bmax + m) * H + hh);
-                    out[m * H + hh] = __float2bfloat16_rn(sum);
+            epi_release(ctl, g, P.nbuf);
+            ++g;
+            if (P.S > 1) {
+                int* ev = p.ev_y + t.mt * P.HT + t.ht;
+                worker_sync();
+                if (wtid == 0) {
+                    __threadfence();
+                    ctl->flag = (atom_acq_rel_add(ev, 1) == P.S - 1) ? 1 : 0;
                 }
-                if (threadIdx.x == 0) *ev = 0;
+                worker_sync();
+                if (ctl->flag) {
+                    for (int j = wtid; j < t.rows * kTileM; j += kWorkers) {
+                        const size_t m = m0 + j / kTileM;
+                        const int c = t.ht * kTileM + (j % kTileM);
+                        float sum = 0.0f;
+                        for (int s2 = 0; s2 < P.S; ++s2)
+                            sum += __ldcg(p.partial + (static_cast<size_t>(s2) * p.B_max + m) * H + c);
+                        p.out[m * H + c] = __float2bfloat16_rn(sum);
+                    }
+                    if (wtid == 0) *ev = 0;
+                }
             }
-            __syncthreads();
         }
     }
-    if (!ok) drain_after_failure(ctl, ring, pipe);
-    cta_teardown(ctl);
+
+    const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
+    cta_teardown(ctl, stg, aborted_run);
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -208,11 +264,11 @@ mlp_chain_kernel(const __grid_constant__ MlpArgs p, const __grid_constant__ CUte
     __syncthreads();
     if (ctl->flag) {
         __threadfence();
-        const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
-        const int mt_clear = aborted_run ? p.mt_max : MT;
+        const bool ab = ld_relaxed(&p.hdr->abort) != 0;
+        const int mt_clear = ab ? p.mt_max : P.MT;
         for (int j = threadIdx.x; j < mt_clear * kSplitMax; j += kThreads) p.ev_h[j] = 0;
-        if (aborted_run)
-            for (int j = threadIdx.x; j < p.mt_max * HT; j += kThreads) p.ev_y[j] = 0;
+        if (ab)
+            for (int j = threadIdx.x; j < p.mt_max * P.HT; j += kThreads) p.ev_y[j] = 0;
         __syncthreads();
         if (threadIdx.x == 0) {
             p.hdr->ev_norm = 0;
@@ -222,6 +278,9 @@ mlp_chain_kernel(const __grid_constant__ MlpArgs p, const __grid_constant__ CUte
         }
     }
 }
+
+int mlp_smem_bytes() { return smem_bytes_for(stages_for(kWideNMax, 0), kWideNMax, 0); }
+int mlp_stages() { return stages_for(kWideNMax, 0); }
 
 cudaError_t launch_mlp(const MlpArgs& a, const CUtensorMap* maps, int grid, int smem,
                        cudaStream_t stream) {
@@ -235,8 +294,8 @@ cudaError_t launch_mlp(const MlpArgs& a, const CUtensorMap* maps, int grid, int 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mlp_chain_kernel, a, maps[0], maps[1], maps[2], maps[3],
-                              maps[4]);
+    return cudaLaunchKernelEx(&cfg, mlp_chain_kernel, maps[0], maps[1], maps[2], maps[3], maps[4],
+                              a);
 }
 
 cudaError_t prepare_mlp(int smem) {

@@ -1,9 +1,11 @@
 // moe_kernel.cu -- the MoE layer as one persistent megakernel whose tiled
 // tasks are ordered by device-resident event counters, not kernel boundaries.
 //
-// Task graph (one dynamic queue, popped with an atomic head; index order is
-// a topological order, so every wait is on a task that a live CTA already
-// popped -- the grid is cooperative, all CTAs are resident):
+// Task graph (one dynamic queue, popped with an atomic head by each CTA's
+// producer thread and handed to its MMA thread and worker warps through a
+// small shared-memory ring; index order is a topological order and every
+// role of a CTA walks its tasks in that order, so every wait is on a task
+// that a resident CTA already holds -- the launch is cooperative):
 //   [0, R)      ROUTER r   fixed-order fp32 logits, top-k, gate weights and
 //                          a per-tile expert histogram;       releases ev_router
 //   R           SCAN       waits ev_router >= R (target computed from the
@@ -56,6 +58,10 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
+__device__ __forceinline__ int wtid_() { return static_cast<int>(threadIdx.x) - kEpiWarp0 * 32; }
+
+constexpr int kMoeScratch = 18432;  // SIMT scratch: router logits [16][256] f32 + histogram
+
 // ------------------------------------------------------------------ ROUTER
 
 // Logits of up to 16 tokens against all E experts.  Lane l of a warp owns
@@ -63,16 +69,16 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 // ascending order with fp32 fma (exact bf16 products, so fma == mul+add);
 // the halving shuffle tree (16, 8, 4, 2, 1) then adds p[l] + p[l+off].  This
 // is the fixed order that makes routing bit-reproducible.
-__device__ __noinline__ void router_task(const MoeArgs& p, int T, int r, uint8_t* smem) {
+__device__ __forceinline__ void router_task(const MoeArgs& p, int T, int r, uint8_t* smem) {
     const int E = p.E, H = p.H, k = p.k;
     float* lg = reinterpret_cast<float*>(smem);                                // [16][E]
     int* hs = reinterpret_cast<int*>(smem + kRouterTile * 256 * sizeof(float));  // [E]
     const int t0 = r * kRouterTile, nt = min(kRouterTile, T - t0);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int e = threadIdx.x; e < E; e += kThreads) hs[e] = 0;
+    const int warp = wtid_() >> 5, lane = wtid_() & 31;
+    for (int e = wtid_(); e < E; e += kWorkers) hs[e] = 0;
     const int neb = ceil_div(E, 8), ntb = ceil_div(nt, 8);
     const bool vec = (E % 8) == 0;
-    for (int job = warp; job < neb * ntb; job += kThreads / 32) {
+    for (int job = warp; job < neb * ntb; job += kWorkers / 32) {
         const int tb = job / neb, eb = job % neb;
         const int tbase = t0 + tb * 8, ebase = eb * 8;
         const int tn = min(8, t0 + nt - tbase), en = min(8, E - ebase);
@@ -116,9 +122,9 @@ __device__ __noinline__ void router_task(const MoeArgs& p, int T, int r, uint8_t
                 }
         }
     }
-    __syncthreads();
+    worker_sync();
     // top-k per token (warp per token): order (logit desc, index asc)
-    for (int tt = warp; tt < nt; tt += kThreads / 32) {
+    for (int tt = warp; tt < nt; tt += kWorkers / 32) {
         const float* L = lg + tt * E;
         float v[8];
 #pragma unroll
@@ -176,10 +182,10 @@ __device__ __noinline__ void router_task(const MoeArgs& p, int T, int r, uint8_t
             }
         }
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kThreads) p.hist[static_cast<size_t>(r) * E + e] = hs[e];
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    worker_sync();
+    for (int e = wtid_(); e < E; e += kWorkers) p.hist[static_cast<size_t>(r) * E + e] = hs[e];
+    worker_sync();
+    if (wtid_() == 0) {
         __threadfence();
         red_release_add(&p.hdr->ev_router, 1);
     }
@@ -191,17 +197,17 @@ __device__ __noinline__ void router_task(const MoeArgs& p, int T, int r, uint8_t
 // targets the later waits use (R permute tiles; F-tiles per chunk; the total
 // number of output tiles) are all derived here, on the device, from the
 // routing of this very call.
-__device__ __noinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem, Ctl* ctl,
+__device__ __forceinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem, Ctl* ctl,
                                        const WaitCtx& wc) {
     const int E = p.E, k = p.k, R = ceil_div(T, kRouterTile);
-    if (threadIdx.x == 0) ctl->flag = ev_wait_geq(wc, &p.hdr->ev_router, R, kWhereRouter) ? 1 : 0;
-    __syncthreads();
+    if (wtid_() == 0) ctl->flag = ev_wait_geq(wc, &p.hdr->ev_router, R, kWhereRouter) ? 1 : 0;
+    worker_sync();
     if (!ctl->flag) return false;
     int* cnt_s = reinterpret_cast<int*>(smem);  // [256]
     int* off_s = cnt_s + 256;                   // [257]
     int* n_s = off_s + 264;                     // [256]
     int* mtb_s = n_s + 256;                     // [257]
-    for (int e = threadIdx.x; e < E; e += kThreads) {
+    for (int e = wtid_(); e < E; e += kWorkers) {
         int run = 0;
         for (int r = 0; r < R; ++r) {
             const int c = __ldcg(p.hist + static_cast<size_t>(r) * E + e);
@@ -210,9 +216,9 @@ __device__ __noinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem, C
         }
         cnt_s[e] = run;
     }
-    __syncthreads();
+    worker_sync();
     const int FT = p.F / kTileM, HT = p.H / kTileM;
-    if (threadIdx.x == 0) {
+    if (wtid_() == 0) {
         off_s[0] = 0;
         mtb_s[0] = 0;
         for (int e = 0; e < E; ++e) {
@@ -237,9 +243,9 @@ __device__ __noinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem, C
         ctl->scratch[0] = total_mt;
         ctl->scratch[1] = S;
     }
-    __syncthreads();
+    worker_sync();
     const int total_mt = ctl->scratch[0], S = ctl->scratch[1];
-    for (int e = threadIdx.x; e < E; e += kThreads) {
+    for (int e = wtid_(); e < E; e += kWorkers) {
         p.cnt[e] = cnt_s[e];
         p.off[e] = off_s[e];
         if (e == E - 1) p.off[E] = off_s[E];
@@ -256,10 +262,10 @@ __device__ __noinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem, C
               n_cb = ceil_div(T, kCombineTile);
     const int total = n_perm + n_gu + n_dn + n_cb;
     if (total > p.q_max) {  // cannot happen for a valid workspace; fail loudly
-        if (threadIdx.x == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereQueue);
+        if (wtid_() == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereQueue);
         return false;
     }
-    for (int q = threadIdx.x; q < total; q += kThreads) {
+    for (int q = wtid_(); q < total; q += kWorkers) {
         int4 d;
         if (q < n_perm) {
             d = make_int4(kTaskPermute, q, 0, 0);
@@ -275,8 +281,8 @@ __device__ __noinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem, C
         }
         p.queue[q] = d;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    worker_sync();
+    if (wtid_() == 0) {
         p.hdr->total_mt = total_mt;
         p.hdr->split = S;
         p.hdr->q_total = total;
@@ -290,15 +296,15 @@ __device__ __noinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem, C
 
 // Stable dispatch of router tile r: row (t, j) goes to off[e] + (rank of t
 // among this call's tokens routed to e), and its x row is copied there.
-__device__ __noinline__ void permute_task(const MoeArgs& p, int T, int r, uint8_t* smem) {
+__device__ __forceinline__ void permute_task(const MoeArgs& p, int T, int r, uint8_t* smem) {
     const int k = p.k, E = p.E, H = p.H;
     const int t0 = r * kRouterTile, nt = min(kRouterTile, T - t0), nent = nt * k;
     int* ie = reinterpret_cast<int*>(smem);  // [128]
     int* slot = ie + 128;                    // [128]
-    for (int i = threadIdx.x; i < nent; i += kThreads)
+    for (int i = wtid_(); i < nent; i += kWorkers)
         ie[i] = __ldcg(p.idx + static_cast<size_t>(t0) * k + i);
-    __syncthreads();
-    for (int i = threadIdx.x; i < nent; i += kThreads) {
+    worker_sync();
+    for (int i = wtid_(); i < nent; i += kWorkers) {
         const int e = ie[i], tl = i / k;
         int rank = 0;
         for (int i2 = 0; i2 < tl * k; ++i2) rank += (ie[i2] == e);
@@ -307,17 +313,17 @@ __device__ __noinline__ void permute_task(const MoeArgs& p, int T, int r, uint8_
         p.pos[static_cast<size_t>(t0) * k + i] = pp;
         slot[i] = pp;
     }
-    __syncthreads();
+    worker_sync();
     const int vpr = H / 8;
-    for (int v = threadIdx.x; v < nent * vpr; v += kThreads) {
+    for (int v = wtid_(); v < nent * vpr; v += kWorkers) {
         const int i = v / vpr, c = v % vpr;
         const int t = t0 + i / k;
         const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H) + c);
         reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(slot[i]) * H)[c] = val;
     }
     fence_proxy_async_global();
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    worker_sync();
+    if (wtid_() == 0) {
         __threadfence();
         red_release_add(&p.hdr->ev_perm, 1);
     }
@@ -325,17 +331,17 @@ __device__ __noinline__ void permute_task(const MoeArgs& p, int T, int r, uint8_
 
 // ------------------------------------------------------------------ COMBINE
 
-__device__ __noinline__ bool combine_task(const MoeArgs& p, int T, int c, Ctl* ctl,
+__device__ __forceinline__ bool combine_task(const MoeArgs& p, int T, int c, Ctl* ctl,
                                           const WaitCtx& wc) {
     const int H = p.H, k = p.k;
-    if (threadIdx.x == 0) {
+    if (wtid_() == 0) {
         const int target = ld_relaxed(&p.hdr->total_mt) * (H / kTileM);
         ctl->flag = ev_wait_geq(wc, &p.hdr->ev_ydone, target, kWhereY) ? 1 : 0;
     }
-    __syncthreads();
+    worker_sync();
     if (!ctl->flag) return false;
     const int t0 = c * kCombineTile, nt = min(kCombineTile, T - t0), vpr = H / 8;
-    for (int v = threadIdx.x; v < nt * vpr; v += kThreads) {
+    for (int v = wtid_(); v < nt * vpr; v += kWorkers) {
         const int t = t0 + v / vpr, cc = v % vpr;
         float acc[8];
 #pragma unroll
@@ -351,172 +357,223 @@ __device__ __noinline__ bool combine_task(const MoeArgs& p, int T, int c, Ctl* c
         }
         reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * H)[cc] = pack8(acc);
     }
-    __syncthreads();
+    worker_sync();
     return true;
 }
 
 // ------------------------------------------------------------------ queue pop
 
-__device__ __noinline__ int4 pop_task(const MoeArgs& p, const WaitCtx& wc, int R) {
-    const int4 none = make_int4(kTaskExit, 0, 0, 0);
-    if (aborted(wc)) return none;
+// Producer thread: next task of this CTA (EXIT when the queue is exhausted or
+// the launch aborted).  GEMM tasks carry their expert row-tile parameters,
+// read after the acquire of the published queue.
+__device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc, int R) {
+    TaskMsg m{};
+    m.type = kTaskExit;
+    if (aborted(wc)) return m;
     const int i = atomicAdd(&p.hdr->q_head, 1);
-    if (i < R) return make_int4(kTaskRouter, i, 0, 0);
-    if (i == R) return make_int4(kTaskScan, 0, 0, 0);
+    if (i < R) {
+        m.type = kTaskRouter;
+        m.a = i;
+        return m;
+    }
+    if (i == R) {
+        m.type = kTaskScan;
+        return m;
+    }
     const int j = i - R - 1;
-    if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return none;
-    if (j >= ld_relaxed(&p.hdr->q_total)) return none;
-    return __ldcg(p.queue + j);
+    if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
+    if (j >= ld_relaxed(&p.hdr->q_total)) return m;
+    const int4 d = __ldcg(p.queue + j);
+    m.type = d.x;
+    m.a = d.y;
+    m.b = d.z;
+    m.c = d.w;
+    if (d.x == kTaskGateUp || d.x == kTaskDown) {
+        const int g = d.y;
+        m.e = __ldcg(p.g_expert + g);
+        m.row0 = __ldcg(p.g_row0 + g);
+        m.rows = __ldcg(p.g_rows + g);
+        m.n = __ldcg(p.g_n + g);
+        m.type |= ld_relaxed(&p.hdr->split) << 8;
+    }
+    return m;
 }
 
 // ------------------------------------------------------------------ the kernel
 
 __global__ void __launch_bounds__(kThreads, 1)
-moe_megakernel(const __grid_constant__ MoeArgs p, const __grid_constant__ CUtensorMap tm_wg,
-               const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ CUtensorMap tm_wd,
-               const __grid_constant__ CUtensorMap tm_xp, const __grid_constant__ CUtensorMap tm_h) {
+moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
+               const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xp,
+               const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ MoeArgs p) {
     extern __shared__ uint8_t smem_raw[];
-    Ring ring;
-    Ctl* ctl = cta_setup(smem_raw, p.stages, kMoeNMax, ring);
+    Stages stg;
+    uint8_t* scratch;
+    Ctl* ctl = cta_setup(smem_raw, p.stages, kMoeNMax, kMoeScratch, stg, &scratch);
     const WaitCtx wc{p.hdr, p.timeout_ns};
-    const MoeMaps maps{&tm_wg, &tm_wu, &tm_wd, &tm_xp, &tm_h};
     const uint32_t tmem = ctl->tmem_base;
-    Pipe pipe;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    int T = p.d_T ? *reinterpret_cast<const volatile int32_t*>(p.d_T) : p.T_host;
+    int T = p.T_host;
+    if (p.d_T) T = *reinterpret_cast<const volatile int32_t*>(p.d_T);
     if (T < 0 || T > p.T_max) {
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereBoundsT);
         T = 0;
     }
     const int R = ceil_div(T, kRouterTile);
     const int FT = p.F / kTileM, HT = p.H / kTileM;
-    if (threadIdx.x == 0) {
-        tma_prefetch_map(&tm_wg);
-        tma_prefetch_map(&tm_wu);
-        tma_prefetch_map(&tm_wd);
-        tma_prefetch_map(&tm_xp);
-        tma_prefetch_map(&tm_h);
-    }
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_b = policy_evict_last();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    (void)warp;
-    (void)lane;
 
-    bool ok = true;
-    for (;;) {
-        if (threadIdx.x == 0) {
-            ctl->fail = 0;
-            ctl->task = pop_task(p, wc, R);
+    auto gemm_of = [&](const TaskMsg& m) {
+        const int type = m.type & 0xff, S = m.type >> 8;
+        if (type == kTaskGateUp)
+            return GemmTask{&tm_wg, &tm_wu, &tm_xp, m.e * p.F + m.b * kTileM, m.row0, 0,
+                            p.H / kBlockK, m.n, 1, &p.hdr->ev_perm, R, kWherePerm};
+        const int fchunk = p.F / S;
+        return GemmTask{&tm_wd, nullptr, &tm_h, m.e * p.H + m.c * kTileM, m.row0,
+                        m.b * (fchunk / kBlockK), fchunk / kBlockK, m.n, m.n <= 64 ? 2 : 1,
+                        &p.ev_h[m.a * kSplitMax + m.b], FT / S, kWhereH};
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {  // producer: pop, hand over, load
+            const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
+            uint32_t it = 0;
+            for (int i = 0;; ++i) {
+                const TaskMsg m = pop_task(p, wc, R);
+                const int slot = i % kTaskRing;
+                if (!mbar_wait(wc, &ctl->tq_empty[slot], ((i / kTaskRing) & 1) ^ 1, kWhereQueue))
+                    break;
+                ctl->tq[slot] = m;
+                mbar_arrive(&ctl->tq_full[slot]);
+                const int type = m.type & 0xff;
+                if (type == kTaskExit) break;
+                if (type == kTaskGateUp || type == kTaskDown)
+                    if (!produce_task(gemm_of(m), stg, ctl, it, wc, pol_w, pol_b)) break;
+            }
         }
-        __syncthreads();
-        const int4 tk = ctl->task;
-        if (tk.x == kTaskExit) break;
-
-        if (tk.x == kTaskRouter) {
-            router_task(p, T, tk.y, ring.base);
-        } else if (tk.x == kTaskScan) {
-            if (!scan_task(p, T, ring.base, ctl, wc)) ok = false;
-        } else if (tk.x == kTaskPermute) {
-            permute_task(p, T, tk.y, ring.base);
-        } else if (tk.x == kTaskCombine) {
-            if (!combine_task(p, T, tk.y, ctl, wc)) ok = false;
-        } else if (tk.x == kTaskGateUp) {
-            const int g = tk.y, ft = tk.z;
-            const int e = __ldcg(p.g_expert + g), row0 = __ldcg(p.g_row0 + g);
-            const int rows = __ldcg(p.g_rows + g), n = __ldcg(p.g_n + g);
-            const int S = ld_relaxed(&p.hdr->split);
-            GemmTask t{maps.wg, maps.wu, maps.xp, e * p.F + ft * kTileM, row0, 0, p.H / kBlockK,
-                       n, 1, &p.hdr->ev_perm, R, kWherePerm};
-            const int F = p.F;
-            bf16* hout = p.h;
-            ok = run_gemm_task(t, ctl, ring, pipe, tmem, wc, pol_w, pol_b, [&](int q, int ln) {
-                const int f = ft * kTileM + q * 32 + ln;
-                const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {  // MMA issuer
+            uint32_t it = 0, g = 0;
+            for (int i = 0;; ++i) {
+                const int slot = i % kTaskRing;
+                if (!mbar_wait(wc, &ctl->tq_full[slot], (i / kTaskRing) & 1, kWhereQueue)) break;
+                const TaskMsg m = ctl->tq[slot];
+                mbar_arrive(&ctl->tq_empty[slot]);
+                const int type = m.type & 0xff;
+                if (type == kTaskExit) break;
+                if (type == kTaskGateUp || type == kTaskDown)
+                    if (!mma_task(gemm_of(m), stg, ctl, it, g, 2, kAccBufCols / 2, tmem, wc)) break;
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kEpiWarp0) {  // workers: epilogues and SIMT tasks
+        const int q = warp - kEpiWarp0, wtid = wtid_();
+        const int H = p.H, F = p.F;
+        uint32_t g = 0, wseq = 0;
+        for (int i = 0;; ++i) {
+            const int slot = i % kTaskRing;
+            if (!worker_wait(ctl, &ctl->tq_full[slot], (i / kTaskRing) & 1, wc, kWhereQueue, wseq))
+                break;
+            const TaskMsg m = ctl->tq[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tq_empty[slot]);
+            const int type = m.type & 0xff, S = m.type >> 8;
+            if (type == kTaskExit) break;
+            if (type == kTaskRouter) {
+                router_task(p, T, m.a, scratch);
+                continue;
+            }
+            if (type == kTaskScan) {
+                if (!scan_task(p, T, scratch, ctl, wc)) break;
+                continue;
+            }
+            if (type == kTaskPermute) {
+                permute_task(p, T, m.a, scratch);
+                continue;
+            }
+            if (type == kTaskCombine) {
+                if (!combine_task(p, T, m.a, ctl, wc)) break;
+                continue;
+            }
+            uint32_t acc;
+            if (!epi_acquire(ctl, g, 2, tmem, wc, acc, wseq)) break;
+            const uint32_t lane_base = acc + (static_cast<uint32_t>(q * 32) << 16);
+            const int row0 = m.row0, rows = m.rows, n = m.n;
+            if (type == kTaskGateUp) {
+                const int ft = m.b;
+                const int f = ft * kTileM + q * 32 + lane;
                 for (int c0 = 0; c0 < n; c0 += 16) {
                     float gv[16], uv[16];
                     tmem_ld16(lane_base + c0, gv);
-                    tmem_ld16(lane_base + kAcc1Col + c0, uv);
+                    tmem_ld16(lane_base + kAccBufCols / 2 + c0, uv);
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
                         if (c0 + c < rows)
-                            hout[static_cast<size_t>(row0 + c0 + c) * F + f] =
+                            p.h[static_cast<size_t>(row0 + c0 + c) * F + f] =
                                 __float2bfloat16_rn(silu_mul(gv[c], uv[c]));
                 }
-                fence_proxy_async_global();
-            });
-            if (ok && threadIdx.x == 0) {
-                const bool skip = p.fault_mode == 1 && g * FT + ft == p.fault_arg;
-                __threadfence();
-                if (!skip) red_release_add(&p.ev_h[g * kSplitMax + ft / (FT / S)], 1);
-            }
-        } else if (tk.x == kTaskDown) {
-            const int g = tk.y, s = tk.z, ht = tk.w;
-            const int e = __ldcg(p.g_expert + g), row0 = __ldcg(p.g_row0 + g);
-            const int rows = __ldcg(p.g_rows + g), n = __ldcg(p.g_n + g);
-            const int S = ld_relaxed(&p.hdr->split);
-            const int fchunk = p.F / S;
-            GemmTask t{maps.wd, nullptr, maps.h, e * p.H + ht * kTileM, row0,
-                       s * (fchunk / kBlockK), fchunk / kBlockK, n, n <= 64 ? 2 : 1,
-                       &p.ev_h[g * kSplitMax + s], FT / S, kWhereH};
-            const int H = p.H, cap = p.split_rows_cap;
-            bf16* yout = p.y;
-            float* part = p.partial;
-            ok = run_gemm_task(t, ctl, ring, pipe, tmem, wc, pol_w, pol_b, [&](int q, int ln) {
-                const int hh = ht * kTileM + q * 32 + ln;
-                const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-                for (int c0 = 0; c0 < n; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(lane_base + c0, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        if (c0 + c >= rows) continue;
-                        const size_t row = static_cast<size_t>(row0 + c0 + c);
-                        if (S == 1)
-                            yout[row * H + hh] = __float2bfloat16_rn(v[c]);
-                        else
-                            part[(static_cast<size_t>(s) * cap + row) * H + hh] = v[c];
-                    }
-                }
-            });
-            if (ok) {
-                if (S > 1) {
-                    if (threadIdx.x == 0) {
-                        __threadfence();
-                        const int old = atom_acq_rel_add(&p.ev_y[g * HT + ht], 1);
-                        ctl->flag = (old == S - 1) ? 1 : 0;
-                    }
-                    __syncthreads();
-                    if (ctl->flag) {  // last arriver: sum partials in chunk order
-                        for (int i = threadIdx.x; i < rows * kTileM; i += kThreads) {
-                            const size_t row = static_cast<size_t>(row0 + i / kTileM);
-                            const int hh = ht * kTileM + (i % kTileM);
-                            float sum = 0.0f;
-                            for (int s2 = 0; s2 < S; ++s2)
-                                sum += __ldcg(part + (static_cast<size_t>(s2) * cap + row) * H + hh);
-                            yout[row * H + hh] = __float2bfloat16_rn(sum);
-                        }
-                        __syncthreads();
-                        if (threadIdx.x == 0) {
-                            __threadfence();
-                            red_release_add(&p.hdr->ev_ydone, 1);
-                        }
-                    }
-                } else if (threadIdx.x == 0) {
+                epi_release(ctl, g, 2);
+                ++g;
+                fence_proxy_async_global();  // h is read back by TMA
+                worker_sync();
+                if (wtid == 0) {
+                    const bool skip = p.fault_mode == 1 && m.a * FT + ft == p.fault_arg;
                     __threadfence();
-                    red_release_add(&p.hdr->ev_ydone, 1);
+                    if (!skip) red_release_add(&p.ev_h[m.a * kSplitMax + ft / (FT / S)], 1);
                 }
+                continue;
+            }
+            // DOWN: y (S == 1) or an fp32 partial of F-chunk s
+            const int s = m.b, ht = m.c;
+            const int hh = ht * kTileM + q * 32 + lane;
+            const int cap = p.split_rows_cap;
+            for (int c0 = 0; c0 < n; c0 += 16) {
+                float v[16];
+                tmem_ld16(lane_base + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    if (c0 + c >= rows) continue;
+                    const size_t row = static_cast<size_t>(row0 + c0 + c);
+                    if (S == 1)
+                        p.y[row * H + hh] = __float2bfloat16_rn(v[c]);
+                    else
+                        p.partial[(static_cast<size_t>(s) * cap + row) * H + hh] = v[c];
+                }
+            }
+            epi_release(ctl, g, 2);
+            ++g;
+            worker_sync();  // the tile's stores are done
+            bool done = true;
+            if (S > 1) {
+                if (wtid == 0) {
+                    __threadfence();
+                    ctl->flag = (atom_acq_rel_add(&p.ev_y[m.a * HT + ht], 1) == S - 1) ? 1 : 0;
+                }
+                worker_sync();
+                done = ctl->flag != 0;
+                if (done) {  // last arriver: sum the partials in chunk order
+                    for (int j = wtid; j < rows * kTileM; j += kWorkers) {
+                        const size_t row = static_cast<size_t>(row0 + j / kTileM);
+                        const int c = ht * kTileM + (j % kTileM);
+                        float sum = 0.0f;
+                        for (int s2 = 0; s2 < S; ++s2)
+                            sum += __ldcg(p.partial + (static_cast<size_t>(s2) * cap + row) * H + c);
+                        p.y[row * H + c] = __float2bfloat16_rn(sum);
+                    }
+                    worker_sync();
+                }
+            }
+            if (done && wtid == 0) {
+                __threadfence();
+                red_release_add(&p.hdr->ev_ydone, 1);
             }
         }
-        __syncthreads();
-        if (ctl->fail) ok = false;
-        if (!ok) break;
     }
 
-    if (!ok) drain_after_failure(ctl, ring, pipe);
-    cta_teardown(ctl);
+    const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
+    cta_teardown(ctl, stg, aborted_run);
 
     // Exit protocol: the last CTA out returns every counter to zero.
     __syncthreads();
@@ -549,6 +606,9 @@ moe_megakernel(const __grid_constant__ MoeArgs p, const __grid_constant__ CUtens
     }
 }
 
+int moe_stages() { return stages_for(kMoeNMax, kMoeScratch); }
+int moe_smem_bytes() { return smem_bytes_for(moe_stages(), kMoeNMax, kMoeScratch); }
+
 // Host-side launch (called by the C ABI after validation).
 cudaError_t launch_moe(const MoeArgs& a, const CUtensorMap* maps, int grid, int smem,
                        cudaStream_t stream) {
@@ -562,8 +622,7 @@ cudaError_t launch_moe(const MoeArgs& a, const CUtensorMap* maps, int grid, int 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_megakernel, a, maps[0], maps[1], maps[2], maps[3],
-                              maps[4]);
+    return cudaLaunchKernelEx(&cfg, moe_megakernel, maps[0], maps[1], maps[2], maps[3], maps[4], a);
 }
 
 cudaError_t prepare_moe(int smem) {
