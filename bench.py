@@ -1,0 +1,421 @@
+"""Benchmark of the Event-Tensor MoE megakernel on GB300.
+
+Default workload: the Mixtral-shaped MoE layer (H 4096, 8 experts, top-2,
+SwiGLU FFN 14336, bf16 weights ~N(0, 0.02), synthetic seeded inputs).  One
+step is one pass over the token sweep T = 1, 2, 4, ..., 512 -- every token
+count served by the same compiled kernel, the count read from device memory.
+L2 is flushed (256 MiB write) before every layer call and each call is timed
+with CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload mixtral|fine|splitk|mlp]
+
+Prints ONE JSON line on rank 0.  With N > 1 (torchrun, one process per GPU)
+every rank runs an independent replica of the same sweep ("replicas only":
+the layer has no exchange step on one node here); value = tokens of all
+ranks / the slowest rank's time.  --impl reference times the CPU oracle on
+the host cores (a bounded sample per step) for the same metric.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from moe_task_scheduling_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/s over the token-count sweep (us/layer per T; % of HBM roofline)"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["et_device.cuh", "et_gemm.cuh", "et_layout.h", "moe_kernel.cu",
+                  "splitk_kernel.cu", "mlp_kernel.cu", "etmoe_api.cu"]
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "moe_task_scheduling_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from a committed ncu summary, only if it was taken
+    on the current kernel sources (same source hash)."""
+    path = os.path.join(ROOT, "profiles", f"moe_megakernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != source_hash():
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world, device):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- MoE workload
+
+def moe_algorithmic_bytes(cfg, T, n_touched):
+    """Bytes the layer must move: the expert weights it touches (gate, up, down),
+    the router weight, x in and out.  h, y and split-K partials are the
+    implementation's own traffic and are not counted."""
+    return (n_touched * 3 * cfg.F * cfg.H * 2 + cfg.H * cfg.E * 2 + 2 * T * cfg.H * 2
+            + (cfg.E * 4 if cfg.zipf_s is not None else 0))
+
+
+def moe_algorithmic_flops(cfg, T):
+    return 2 * T * cfg.k * 3 * cfg.H * cfg.F + 2 * T * cfg.H * cfg.E
+
+
+class MoeBench:
+    def __init__(self, cfg, device):
+        from moe_task_scheduling_gb300 import etmoe
+        self.etmoe = etmoe
+        etmoe.load()
+        self.cfg = cfg
+        self.dev = device
+        self.inp = wl.moe_inputs(cfg, device=device)
+        T_max = cfg.T_max
+        self.out = torch.empty((T_max, cfg.H), dtype=torch.bfloat16, device=device)
+        self.cnt = torch.zeros((cfg.E,), dtype=torch.int32, device=device)
+        self.ws = etmoe.alloc_workspace(etmoe.et_moe_workspace_bytes(T_max, cfg.H, cfg.F, cfg.E,
+                                                                     cfg.k), device=device)
+        self.d_T = torch.zeros(1, dtype=torch.int32, device=device)
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.stream = torch.cuda.current_stream(device)
+
+    def call(self, x=None, out=None):
+        i = self.inp
+        self.etmoe.et_moe_layer(x if x is not None else i["x"], i["wr"], i["bias"], i["wg"], i["wu"],
+                                i["wd"], out if out is not None else self.out, k=self.cfg.k, T=0,
+                                d_T=self.d_T, T_max=self.cfg.T_max, expert_counts=self.cnt,
+                                workspace=self.ws, stream=self.stream)
+
+    def step(self, events=None):
+        """One pass over the sweep; returns per-T event pairs if asked."""
+        pairs = []
+        for T in self.cfg.T_sweep:
+            self.flush.zero_()
+            self.d_T.fill_(T)
+            if events:
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(self.stream)
+                self.call()
+                e.record(self.stream)
+                pairs.append((T, s, e))
+            else:
+                self.call()
+        return pairs
+
+    def touched(self):
+        out = {}
+        for T in self.cfg.T_sweep:
+            self.d_T.fill_(T)
+            self.call()
+            torch.cuda.synchronize()
+            out[T] = int((self.cnt > 0).sum().item())
+        return out
+
+    def e2e(self, steps):
+        """Through the public call with host buffers: per T, pinned x -> device,
+        the layer, out -> pinned host; all copies inside the timed region."""
+        cfg = self.cfg
+        xh = {T: self.inp["x"][:T].cpu().pin_memory() for T in cfg.T_sweep}
+        oh = {T: torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory() for T in cfg.T_sweep}
+        xd = torch.empty_like(self.inp["x"])
+        h2d = sum(T * cfg.H * 2 for T in cfg.T_sweep)
+        total = 0.0
+        for _ in range(steps):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(self.stream)
+            for T in cfg.T_sweep:
+                xd[:T].copy_(xh[T], non_blocking=True)
+                self.d_T.fill_(T)
+                self.call(x=xd)
+                oh[T].copy_(self.out[:T], non_blocking=True)
+            e.record(self.stream)
+            e.synchronize()
+            total += s.elapsed_time(e) / 1e3
+        return total, h2d, h2d
+
+
+def run_ours(args, world, rank, local):
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU for --impl ours"
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cfg = {"mixtral": wl.MIXTRAL, "fine": wl.FINE}[args.workload]
+    b = MoeBench(cfg, device)
+    touched = b.touched()
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
+    barrier(world)
+    torch.cuda.synchronize()
+    per_T = {T: [] for T in cfg.T_sweep}
+    wall0 = time.perf_counter()
+    with ClockSampler(gpu_index) as clk:
+        all_pairs = [b.step(events=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - wall0
+        for pairs in all_pairs:
+            for T, s, e in pairs:
+                per_T[T].append(s.elapsed_time(e) / 1e3)
+        e2e_time, h2d, d2h = b.e2e(args.steps)
+    kernel_time = sum(sum(v) for v in per_T.values())  # seconds, summed over steps
+    tokens = args.steps * sum(cfg.T_sweep)
+    t_max = max_over_ranks(kernel_time, world, device)
+    tok_all = sum_over_ranks(tokens, world, device)
+    e2e_max = max_over_ranks(e2e_time, world, device)
+    if rank != 0:
+        return None
+    pk = peaks()
+    sweep = []
+    bytes_total = 0.0
+    for T in cfg.T_sweep:
+        t = statistics.median(per_T[T])
+        by = moe_algorithmic_bytes(cfg, T, touched[T])
+        bytes_total += by * len(per_T[T])
+        sweep.append({"T": T, "us_per_layer": round(t * 1e6, 2), "us_min": round(min(per_T[T]) * 1e6, 2),
+                      "tokens_per_s": round(T / t, 1), "experts_touched": touched[T],
+                      "hbm_frac": round(by / t / 1e9 / pk["hbm_gbs"], 4),
+                      "tensor_frac": round(moe_algorithmic_flops(cfg, T) / t / 1e12 / pk["bf16_tflops"], 4)})
+    achieved = bytes_total / kernel_time / 1e9
+    traffic = profiled_traffic(args.workload)
+    n_launch = args.steps * len(cfg.T_sweep)
+    line = {
+        "metric": METRIC,
+        "value": round(tok_all / t_max, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) bf16 weights and activations)",
+        "config": {"workload": f"{cfg.name} MoE layer, T sweep {list(cfg.T_sweep)}",
+                   "H": cfg.H, "F": cfg.F, "E": cfg.E, "k": cfg.k,
+                   "l2": "flushed (256 MiB write) before every layer call",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "symbolic_T": "one compiled kernel, T read from device memory"},
+        "sweep": sweep,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "traffic": traffic, "peak_source": pk["source"] + " (hbm copy, burst)",
+                     "kernel": "moe_megakernel"},
+        "e2e": {"value": round(tok_all / e2e_max, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": n_launch,
+        "wall_s_timed": round(wall, 3),
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(b, cfg, args)
+    return line
+
+
+def cpu_baseline(b, cfg, args):
+    """The oracle, as it stands, on the host cores over a bounded sample of the
+    same workload (the first `n` tokens of the sweep's largest batch)."""
+    import oracle
+    n = args.cpu_tokens
+    hb = {k: (wl.bits(v) if v is not None and v.dtype == torch.bfloat16 else
+              (None if v is None else v.detach().cpu().numpy())) for k, v in b.inp.items()}
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.moe_layer(hb["x"][:n], hb["wr"], hb["bias"], hb["wg"], hb["wu"], hb["wd"], k=cfg.k,
+                     nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} tokens of the {cfg.name} layer (all routing + outputs), one call, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, timed on the host cores, one bounded
+    sample (args.ref_tokens tokens of the same layer) per step."""
+    if rank != 0:
+        return None
+    import oracle
+    cfg = {"mixtral": wl.MIXTRAL, "fine": wl.FINE}[args.workload]
+    inp = wl.moe_inputs(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+    hb = {k: (wl.bits(v) if v is not None and v.dtype == torch.bfloat16 else
+              (None if v is None else v.detach().cpu().numpy())) for k, v in inp.items()}
+    del inp
+    n = args.ref_tokens
+    threads = oracle.default_threads()
+
+    def one():
+        oracle.moe_layer(hb["x"][:n], hb["wr"], hb["bias"], hb["wg"], hb["wu"], hb["wd"],
+                         k=cfg.k, nthreads=threads)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    v = round(args.steps * n / dt, 3)
+    return {
+        "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,0.02) bf16 weights and activations)", "impl": "reference",
+        "config": {"workload": f"{cfg.name} MoE layer, T sweep {list(cfg.T_sweep)}",
+                   "H": cfg.H, "F": cfg.F, "E": cfg.E, "k": cfg.k,
+                   "sample_per_step": f"{n} tokens"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} tokens of the {cfg.name} layer per step"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["mixtral", "fine"], default="mixtral")
+    ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--ref-tokens", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
