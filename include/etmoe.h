@@ -117,6 +117,36 @@ int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t*
                    const et_opts* opts, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Split-K GEMM that allocates nothing (the source paper has no counterpart;
+ * this entry point exists for callers that cannot allocate).
+ *
+ * Same result as et_splitk_gemm with d_M = NULL and M_max = M, but without a
+ * caller workspace: the scratch (status word, tile counters, fp32 partial
+ * sums) lives in one device array of ET_SPLITK_NOALLOC_SCRATCH_BYTES inside
+ * the library, held by every GPU that loads the library until the process
+ * exits.  Meant for callers that cannot call cudaMalloc -- e.g. a plugin or
+ * custom-op interface that only passes input and output buffers, or a code
+ * path where allocating could synchronise the device or break a fixed
+ * memory plan.  The caller still passes X, Wt and Y.
+ *  - No cudaMalloc, cudaFree or other allocating call is made.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Each call first clears the status word and tile counters of the array
+ *    on `stream` (cudaMemsetAsync), then runs the split-K kernel.
+ *  - Every call shares the one array: calls that overlap on the GPU (other
+ *    streams, other host threads) race on it and must be serialised.
+ *  - Shapes whose scratch (et_splitk_workspace_bytes(M, N, K, split)) exceeds
+ *    the array are rejected with ET_ERR_WORKSPACE before anything is
+ *    launched; other argument rules are those of et_splitk_gemm.
+ *  - Device-side errors are not observable through et_status here.
+ * ---------------------------------------------------------------------- */
+#define ET_SPLITK_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+int et_splitk_gemm_noalloc(const void* X, const void* Wt, void* Y, int M, int N, int K, int split,
+                           void* stream);
+
+/* ------------------------------------------------------------------------
  * Dense dependent MLP chain, statically scheduled (tasks bound to CTAs):
  *   xhat = bf16( x / sqrt(mean(x^2) + eps) * gamma )
  *   out  = bf16( bf16( silu(xhat Wg^T) * (xhat Wu^T) ) Wd^T )

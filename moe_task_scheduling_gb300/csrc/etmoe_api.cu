@@ -466,3 +466,68 @@ int et_reset_status(void* workspace, void* stream) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Split-K GEMM without any allocation.
+//
+// Some callers cannot hand this library a workspace: a plugin or custom-op
+// interface that passes only input and output buffers, or a code path that
+// must not call cudaMalloc because allocating may synchronise the device or
+// break a fixed memory plan.  For them, et_splitk_gemm_noalloc runs the same
+// split-K kernel with its scratch (status word, tile counters, fp32 partial
+// sums) in the file-scope device array below, which every GPU that loads the
+// library keeps until the process exits.
+// ----------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_splitk_noalloc_scratch[ET_SPLITK_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the real address is looked up
+// once per device, with that device current.
+int noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_splitk_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr)
+            return fail_cuda(e, "cudaGetSymbolAddress(split-K scratch)");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return ET_OK;
+}
+
+}  // namespace
+
+extern "C" int et_splitk_gemm_noalloc(const void* X, const void* Wt, void* Y, int M, int N, int K,
+                                      int split, void* stream) {
+    g_last_error.clear();
+    if (!X || !Wt || !Y) return fail(ET_ERR_INVALID, "X, Wt and Y must be non-NULL");
+    if (M < 0 || M > (1 << 20)) return fail(ET_ERR_INVALID, "M must be in [0, 2^20]");
+    const size_t need = et_splitk_workspace_bytes(M > 0 ? M : 1, N, K, split);
+    if (need == 0)
+        return fail(ET_ERR_UNSUPPORTED,
+                    "N must be a positive multiple of 128, split in [1, 16], K a multiple of 64*split");
+    if (need > ET_SPLITK_NOALLOC_SCRATCH_BYTES)
+        return fail(ET_ERR_WORKSPACE,
+                    "et_splitk_gemm_noalloc: this shape needs " + std::to_string(need) +
+                        " bytes of scratch but the built-in area holds " +
+                        std::to_string(static_cast<size_t>(ET_SPLITK_NOALLOC_SCRATCH_BYTES)) +
+                        " (use et_splitk_gemm with a workspace for larger shapes)");
+    if (M == 0) return ET_OK;
+    DeviceState* st = nullptr;
+    int dev = 0;
+    int rc = device_state(&st, &dev);
+    if (rc) return rc;
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch(dev, &scratch))) return rc;
+    // The array keeps the previous call's contents: zero the status word and
+    // the tile counters (everything before the partial sums) for this call.
+    const SplitKLayout L = splitk_layout(M, N, K, split);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, L.partial, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(split-K scratch counters)");
+    return et_splitk_gemm(X, Wt, Y, M, nullptr, M, N, K, split, scratch, need, nullptr, stream);
+}
