@@ -256,6 +256,82 @@ class MoeBench:
         return total, h2d, h2d
 
 
+class DenseBench:
+    """Split-K GEMM (config 2) or the MLP chain (config 3) over their M / B sweeps."""
+
+    def __init__(self, kind, device):
+        from moe_task_scheduling_gb300 import etmoe
+        self.etmoe = etmoe
+        etmoe.load()
+        self.kind = kind
+        self.dev = device
+        self.stream = torch.cuda.current_stream(device)
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.d_n = torch.zeros(1, dtype=torch.int32, device=device)
+        if kind == "splitk":
+            c = self.cfg = wl.SPLITK
+            self.inp = wl.splitk_inputs(c, device=device)
+            self.sweep = c.M_sweep
+            self.out = torch.empty((c.M_max, c.N), dtype=torch.bfloat16, device=device)
+            self.ws = etmoe.alloc_workspace(etmoe.et_splitk_workspace_bytes(c.M_max, c.N, c.K,
+                                                                            c.split), device=device)
+        else:
+            c = self.cfg = wl.MLP
+            self.inp = wl.mlp_inputs(c, device=device)
+            self.sweep = c.B_sweep
+            self.out = torch.empty((c.B_max, c.H), dtype=torch.bfloat16, device=device)
+            self.ws = etmoe.alloc_workspace(etmoe.et_mlp_workspace_bytes(c.B_max, c.H, c.F),
+                                            device=device)
+
+    def call(self):
+        c, i = self.cfg, self.inp
+        if self.kind == "splitk":
+            self.etmoe.et_splitk_gemm(i["X"], i["Wt"], self.out, split=c.split, M=0, d_M=self.d_n,
+                                      M_max=c.M_max, workspace=self.ws, stream=self.stream)
+        else:
+            self.etmoe.et_mlp_chain(i["x"], i["gamma"], c.eps, i["wg"], i["wu"], i["wd"], self.out,
+                                    B=0, d_B=self.d_n, B_max=c.B_max, workspace=self.ws,
+                                    stream=self.stream)
+
+    def bytes_flops(self, n):
+        c = self.cfg
+        if self.kind == "splitk":
+            return c.N * c.K * 2 + n * c.K * 2 + n * c.N * 2, 2 * n * c.N * c.K
+        return 3 * c.H * c.F * 2 + 2 * n * c.H * 2 + c.H * 2, 6 * n * c.H * c.F
+
+    def measure(self, steps, warmup):
+        res = []
+        for n in self.sweep:
+            self.d_n.fill_(n)
+            for _ in range(warmup):
+                self.flush.zero_()
+                self.call()
+            ts = []
+            for _ in range(steps):
+                self.flush.zero_()
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(self.stream)
+                self.call()
+                e.record(self.stream)
+                ts.append((s, e))
+            torch.cuda.synchronize()
+            t = statistics.median(s.elapsed_time(e) / 1e3 for s, e in ts)
+            by, fl = self.bytes_flops(n)
+            pk = peaks()
+            res.append({"n": n, "us": round(t * 1e6, 2), "hbm_frac": round(by / t / 1e9 / pk["hbm_gbs"], 4),
+                        "tensor_frac": round(fl / t / 1e12 / pk["bf16_tflops"], 4)})
+        return res
+
+
+def run_dense(args, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    b = DenseBench(args.workload, device)
+    res = b.measure(args.steps, args.warmup)
+    return {"workload": args.workload, "sweep": res,
+            "note": "per-call CUDA-event median, L2 flushed before each call; not the headline line"}
+
+
 def run_ours(args, world, rank, local):
     assert torch.cuda.is_available(), "bench.py needs a CUDA GPU for --impl ours"
     device = torch.device("cuda", local)
@@ -398,7 +474,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["mixtral", "fine"], default="mixtral")
+    ap.add_argument("--workload", choices=["mixtral", "fine", "splitk", "mlp"], default="mixtral")
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -408,6 +484,8 @@ def main(argv=None):
     world, rank, local = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, world, rank)
+    elif args.workload in ("splitk", "mlp"):
+        line = run_dense(args, local) if rank == 0 else None
     else:
         line = run_ours(args, world, rank, local)
     if line is not None:

@@ -68,11 +68,16 @@ enum et_status_code {
 /* Optional knobs; pass NULL for the defaults. */
 typedef struct et_opts {
     uint32_t timeout_us; /* bound on every device-side wait; 0 = 200000 us */
-    uint32_t reserved;
+    uint32_t trace_cap;  /* records the trace buffer holds (0 = no trace) */
     int32_t fault_mode;  /* test hook, 0 = off; 1 = the producer task chosen by
                             fault_arg skips its event release, so that its
                             consumers must time out cleanly */
     int32_t fault_arg;
+    void* trace;         /* optional DEVICE buffer of 32 + 32*trace_cap bytes,
+                            zeroed by the caller: et_moe_layer appends one
+                            record per task and role -- {int32 type | role<<8,
+                            a, b, cta; uint64 t_begin, t_end} (%globaltimer ns)
+                            after a uint64 record count.  NULL = no trace. */
 } et_opts;
 
 /* ------------------------------------------------------------------------

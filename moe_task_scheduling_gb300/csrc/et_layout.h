@@ -28,8 +28,8 @@ constexpr int kSplitMax = 8;         // largest split of the MoE / MLP down proj
 
 // MoE
 constexpr int kMoeNMax = 128;        // token rows per expert tile (UMMA N)
-constexpr int kRouterTile = 16;      // tokens per router / permute task
-constexpr int kCombineTile = 16;     // tokens per combine task
+constexpr int kRouterTile = 16;      // tokens per router tile (router and permute tasks)
+constexpr int kCombineTile = 16;     // most tokens per combine task
 constexpr int kMoeSplitRowsCap = 512;  // split the down projection only up to T*k rows
 
 // split-K GEMM and MLP chain: up to 256 token rows per tile
@@ -94,6 +94,8 @@ struct MoeArgs {
     EtHeader* hdr;
     int32_t* ev_h;        // [mt_max * kSplitMax]
     int32_t* ev_y;        // [mt_max * (H/128)]
+    int32_t* ev_tile;     // [r_max]: router expert chunks done per tile (self-resetting)
+    float* logits;        // [T_max, E]: router logits when the experts are split in chunks
     int32_t* hist;        // [r_max * E]: per router tile expert histogram
     int32_t* base;        // [r_max * E]: first permuted row of each (tile, expert)
     int32_t* off;         // [E + 1]
@@ -109,6 +111,8 @@ struct MoeArgs {
     float* partial;       // [kSplitMax, split_rows_cap, H]
     int mt_max, q_max, split_rows_cap, r_max;
     int stages, num_ctas;
+    uint64_t* trace;      // optional per-task trace (see et_opts)
+    int trace_cap;
     uint64_t timeout_ns;
     int fault_mode, fault_arg;
 };

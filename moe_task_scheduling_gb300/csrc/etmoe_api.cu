@@ -130,8 +130,8 @@ struct Carve {
 
 struct MoeLayout {
     int Tk, r_max, mt_max, q_max, split_cap;
-    size_t ev_h, ev_y, hist, base, idx, gw, cnt, off, pos, perm, g_expert, g_row0, g_rows, g_n,
-        queue, xp, h, y, partial, total;
+    size_t ev_h, ev_y, ev_tile, logits, hist, base, idx, gw, cnt, off, pos, perm, g_expert, g_row0,
+        g_rows, g_n, queue, xp, h, y, partial, total;
 };
 
 MoeLayout moe_layout(int T_max, int H, int F, int E, int k) {
@@ -140,11 +140,13 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k) {
     L.r_max = ceil_div(T_max, kRouterTile);
     L.mt_max = ceil_div(L.Tk, kMoeNMax) + E;
     const int FT = F / kTileM, HT = H / kTileM;
-    L.q_max = L.r_max + L.mt_max * FT + L.mt_max * kSplitMax * HT + ceil_div(T_max, kCombineTile);
+    L.q_max = L.r_max * kRouterTile * k + L.mt_max * FT + L.mt_max * kSplitMax * HT + T_max;
     L.split_cap = L.Tk < kMoeSplitRowsCap ? L.Tk : kMoeSplitRowsCap;
     Carve c;
     L.ev_h = c.take(sizeof(int) * L.mt_max * kSplitMax);
     L.ev_y = c.take(sizeof(int) * L.mt_max * HT);
+    L.ev_tile = c.take(sizeof(int) * L.r_max);
+    L.logits = c.take(sizeof(float) * static_cast<size_t>(T_max) * E);
     L.hist = c.take(sizeof(int) * L.r_max * E);
     L.base = c.take(sizeof(int) * L.r_max * E);
     L.idx = c.take(sizeof(int) * L.Tk);
@@ -285,6 +287,8 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
     a.hdr = reinterpret_cast<EtHeader*>(ws);
     a.ev_h = reinterpret_cast<int32_t*>(ws + L.ev_h);
     a.ev_y = reinterpret_cast<int32_t*>(ws + L.ev_y);
+    a.ev_tile = reinterpret_cast<int32_t*>(ws + L.ev_tile);
+    a.logits = reinterpret_cast<float*>(ws + L.logits);
     a.hist = reinterpret_cast<int32_t*>(ws + L.hist);
     a.base = reinterpret_cast<int32_t*>(ws + L.base);
     a.off = reinterpret_cast<int32_t*>(ws + L.off);
@@ -307,6 +311,8 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
     a.timeout_ns = timeout_ns_of(opts);
     a.fault_mode = opts ? opts->fault_mode : 0;
     a.fault_arg = opts ? opts->fault_arg : 0;
+    a.trace = (opts && opts->trace && opts->trace_cap) ? static_cast<uint64_t*>(opts->trace) : nullptr;
+    a.trace_cap = opts ? static_cast<int>(opts->trace_cap) : 0;
 
     CUtensorMap maps[5];
     const uint64_t EF = static_cast<uint64_t>(E) * F, EH = static_cast<uint64_t>(E) * H;

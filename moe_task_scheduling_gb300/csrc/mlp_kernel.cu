@@ -120,10 +120,11 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     P.HT = p.H / kTileM;
     P.NR = ceil_div(P.B, kNormRows);
     P.MT = ceil_div(P.B, kWideNMax);
-    // split of the down projection: the smallest divisor of FT (<= 8) that
-    // gives at least one down task per CTA, else the largest such divisor
+    // split of the down projection: none when the down tiles already cover
+    // every CTA, else the smallest divisor of FT (<= 8) that does, else the
+    // largest such divisor
     P.S = 1;
-    if (P.MT > 0) {
+    if (P.MT > 0 && P.MT * P.HT < static_cast<int>(gridDim.x)) {
         for (int d = 2; d <= kSplitMax; ++d) {
             if (P.FT % d) continue;
             P.S = d;

@@ -64,46 +64,61 @@ constexpr int kMoeScratch = 18432;  // SIMT scratch: router logits [16][256] f32
 
 // ------------------------------------------------------------------ ROUTER
 
-// Logits of up to 16 tokens against all E experts.  Lane l of a warp owns
-// partial sum l of 8 tokens x 8 experts and accumulates h = l, l+32, ... in
-// ascending order with fp32 fma (exact bf16 products, so fma == mul+add);
-// the halving shuffle tree (16, 8, 4, 2, 1) then adds p[l] + p[l+off].  This
-// is the fixed order that makes routing bit-reproducible.
-__device__ __forceinline__ void router_task(const MoeArgs& p, int T, int r, uint8_t* smem) {
-    const int E = p.E, H = p.H, k = p.k;
-    float* lg = reinterpret_cast<float*>(smem);                                // [16][E]
-    int* hs = reinterpret_cast<int*>(smem + kRouterTile * 256 * sizeof(float));  // [E]
-    const int t0 = r * kRouterTile, nt = min(kRouterTile, T - t0);
+template <int EBW>
+__device__ __forceinline__ void load_w(const bf16* wrow, float (&w)[EBW]) {
+    if constexpr (EBW == 8) {
+        unpack8(*reinterpret_cast<const uint4*>(wrow), w);
+    } else if constexpr (EBW == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(wrow);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
+        w[0] = f0.x; w[1] = f0.y; w[2] = f1.x; w[3] = f1.y;
+    } else if constexpr (EBW == 2) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(wrow));
+        w[0] = f.x; w[1] = f.y;
+    } else {
+        w[0] = bf2f(*wrow);
+    }
+}
+
+// Fixed-order logits of nt (<= 16) tokens x `ec` experts (global experts
+// e0 .. e0+ec).  A job is 8 tokens x EBW experts; lane l of the job's warp
+// owns partial sum l and accumulates h = l, l+32, ... in ascending order with
+// fp32 fma (exact bf16 products, so fma == mul+add); the halving shuffle tree
+// (16, 8, 4, 2, 1) then adds p[l] + p[l+off].  xb: token rows (stride H);
+// wb: weight rows (stride ws) whose column 0 is expert e0.  Logit (t, e0+j)
+// goes to out[t * out_stride + out_e0 + j].
+template <int EBW>
+__device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, const bf16* wb,
+                                              int ws, int nt, int e0, int ec, float* out,
+                                              int out_stride, int out_e0) {
+    const int H = p.H;
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
-    for (int e = wtid_(); e < E; e += kWorkers) hs[e] = 0;
-    const int neb = ceil_div(E, 8), ntb = ceil_div(nt, 8);
-    const bool vec = (E % 8) == 0;
+    const int neb = ec / EBW, ntb = ceil_div(nt, 8);
+    constexpr int U = 4;  // h-steps whose weights are loaded ahead of their fmas
     for (int job = warp; job < neb * ntb; job += kWorkers / 32) {
-        const int tb = job / neb, eb = job % neb;
-        const int tbase = t0 + tb * 8, ebase = eb * 8;
-        const int tn = min(8, t0 + nt - tbase), en = min(8, E - ebase);
-        float acc[8][8];
+        const int tb = job / neb, eb = (job % neb) * EBW;
+        const int tn = min(8, nt - tb * 8);
+        float acc[8][EBW];
 #pragma unroll
         for (int a = 0; a < 8; ++a)
 #pragma unroll
-            for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
-        const bf16* xrow = p.x + static_cast<size_t>(tbase) * H;
-        for (int h = lane; h < H; h += 32) {
-            float wv[8];
-            if (vec) {
-                const uint4 raw =
-                    __ldg(reinterpret_cast<const uint4*>(p.wr + static_cast<size_t>(h) * E + ebase));
-                unpack8(raw, wv);
-            } else {
+            for (int b = 0; b < EBW; ++b) acc[a][b] = 0.0f;
+        const bf16* xr = xb + static_cast<size_t>(tb * 8) * H;
+        for (int h0 = 0; h0 < H; h0 += 32 * U) {  // H is a multiple of 128
+            float wv[U][EBW];
 #pragma unroll
-                for (int b = 0; b < 8; ++b)
-                    wv[b] = b < en ? bf2f(p.wr[static_cast<size_t>(h) * E + ebase + b]) : 0.0f;
-            }
+            for (int u = 0; u < U; ++u)
+                load_w<EBW>(wb + static_cast<size_t>(h0 + 32 * u + lane) * ws + eb, wv[u]);
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                const float xv = a < tn ? bf2f(xrow[static_cast<size_t>(a) * H + h]) : 0.0f;
+            for (int u = 0; u < U; ++u) {
+                const int h = h0 + 32 * u + lane;
 #pragma unroll
-                for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xv, wv[b], acc[a][b]);
+                for (int a = 0; a < 8; ++a) {
+                    const float xv = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
+#pragma unroll
+                    for (int b = 0; b < EBW; ++b) acc[a][b] = fmaf(xv, wv[u][b], acc[a][b]);
+                }
             }
         }
 #pragma unroll
@@ -111,17 +126,150 @@ __device__ __forceinline__ void router_task(const MoeArgs& p, int T, int r, uint
 #pragma unroll
             for (int a = 0; a < 8; ++a)
 #pragma unroll
-                for (int b = 0; b < 8; ++b)
+                for (int b = 0; b < EBW; ++b)
                     acc[a][b] = acc[a][b] + __shfl_down_sync(0xffffffffu, acc[a][b], off);
         if (lane == 0) {
             for (int a = 0; a < tn; ++a)
-                for (int b = 0; b < en; ++b) {
+#pragma unroll
+                for (int b = 0; b < EBW; ++b) {
                     float L = acc[a][b];
-                    if (p.bias) L = L + p.bias[ebase + b];
-                    lg[(tb * 8 + a) * E + ebase + b] = L;
+                    if (p.bias) L = L + p.bias[e0 + eb + b];
+                    out[(tb * 8 + a) * out_stride + out_e0 + eb + b] = L;
                 }
         }
     }
+}
+
+// Flat copy of `bytes` (multiple of 16, 16-byte aligned ends) by the worker
+// group into shared memory, several 16-byte loads in flight per thread.
+__device__ __forceinline__ void worker_copy_flat(uint8_t* dst, const uint8_t* src, size_t bytes) {
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    const int n = static_cast<int>(bytes / 16);
+    constexpr int U = 8;
+    for (int i = wtid_(); i < n; i += kWorkers * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i + u * kWorkers < n) v[u] = __ldcg(s + i + u * kWorkers);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i + u * kWorkers < n) d[i + u * kWorkers] = v[u];
+    }
+}
+
+// Columns [e0, e0 + ec) of the router weight [H, E] into contiguous
+// shared memory [H][ec], with the widest element the alignment allows.
+template <class V>
+__device__ __forceinline__ void copy_cols_t(uint8_t* dst, const bf16* wr, int H, int E, int e0,
+                                            int ec) {
+    const int per_row = ec * 2 / static_cast<int>(sizeof(V));
+    const int n = H * per_row;
+    constexpr int U = 4;
+    for (int i = wtid_(); i < n; i += kWorkers * U) {
+        V v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = i + u * kWorkers;
+            if (j < n) {
+                const int h = j / per_row, q = j - h * per_row;
+                v[u] = *(reinterpret_cast<const V*>(wr + static_cast<size_t>(h) * E + e0) + q);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = i + u * kWorkers;
+            if (j < n) reinterpret_cast<V*>(dst)[j] = v[u];
+        }
+    }
+}
+
+__device__ __forceinline__ void copy_cols(uint8_t* dst, const bf16* wr, int H, int E, int e0, int ec) {
+    const int bytes = ec * 2, off = e0 * 2, stride = E * 2;
+    if ((bytes | off | stride) % 16 == 0)
+        copy_cols_t<uint4>(dst, wr, H, E, e0, ec);
+    else if ((bytes | off | stride) % 4 == 0)
+        copy_cols_t<uint32_t>(dst, wr, H, E, e0, ec);
+    else
+        copy_cols_t<unsigned short>(dst, wr, H, E, e0, ec);
+}
+
+// The per-call plan: a pure function of the device token count, E, k and the
+// grid, so every CTA and every role derives the same task numbering.
+struct MoePlan {
+    int T, R;      // tokens; router tiles of kRouterTile tokens
+    int C, EC;     // router expert chunks per tile, experts per chunk
+    int Q;         // permute parts per router tile
+    int CT, NC;    // tokens per combine task; combine tasks
+};
+
+__device__ __forceinline__ MoePlan moe_plan(int T, int E, int k, int G) {
+    MoePlan P;
+    P.T = T;
+    P.R = ceil_div(T, kRouterTile);
+    // Split the router's experts into chunks when there are few router tiles,
+    // so a small batch still spreads over many CTAs (each chunk >= 2 experts).
+    const int want = P.R > 0 ? max(1, G / P.R) : 1;
+    P.C = 1;
+    for (int d = 2; d <= E / 2; ++d)
+        if (E % d == 0 && d <= want) P.C = d;
+    P.EC = E / P.C;
+    P.Q = P.R > 0 ? min(max(1, G / P.R), kRouterTile * k) : 1;
+    P.CT = min(kCombineTile, max(1, ceil_div(T, G)));
+    P.NC = ceil_div(T, P.CT);
+    return P;
+}
+
+// Logits of router tile r for expert chunk c.  The token rows and the chunk's
+// router-weight columns are staged into the stage ring first (no GEMM task is
+// published before the scan, which waits for every router tile, so the ring
+// is idle while any router task runs).  With several chunks the logits go to
+// a global buffer and the chunk that brings the tile's counter to C does the
+// top-k for the whole tile -- the same event-counter reduction as split-K.
+__device__ __forceinline__ void router_task(const MoeArgs& p, const MoePlan& P, int r, int c,
+                                            uint8_t* smem, uint8_t* ring, size_t ring_bytes,
+                                            Ctl* ctl) {
+    const int E = p.E, H = p.H, k = p.k;
+    float* lg = reinterpret_cast<float*>(smem);                                // [16][E]
+    int* hs = reinterpret_cast<int*>(smem + kRouterTile * 256 * sizeof(float));  // [E]
+    const int t0 = r * kRouterTile, nt = min(kRouterTile, P.T - t0);
+    const int warp = wtid_() >> 5, lane = wtid_() & 31;
+    const int e0 = c * P.EC, ec = P.EC;
+    const size_t xbytes = static_cast<size_t>(nt) * H * 2;
+    const size_t wbytes = static_cast<size_t>(H) * ec * 2;
+    const bool x_in = xbytes <= ring_bytes;
+    const bool w_in = x_in && xbytes + wbytes <= ring_bytes;
+    if (x_in)
+        worker_copy_flat(ring, reinterpret_cast<const uint8_t*>(p.x + static_cast<size_t>(t0) * H),
+                         xbytes);
+    if (w_in) copy_cols(ring + xbytes, p.wr, H, E, e0, ec);
+    worker_sync();
+    const bf16* xb = x_in ? reinterpret_cast<const bf16*>(ring) : p.x + static_cast<size_t>(t0) * H;
+    const bf16* wb = w_in ? reinterpret_cast<const bf16*>(ring + xbytes) : p.wr + e0;
+    const int ws = w_in ? ec : E;
+    float* out = P.C == 1 ? lg : p.logits + static_cast<size_t>(t0) * E;
+    // widest expert block (at most 4: registers) that still gives every worker warp a job
+    const int ntb = ceil_div(nt, 8), warps = kWorkers / 32;
+    if (ec % 4 == 0 && ntb * (ec / 4) >= warps)
+        router_logits<4>(p, xb, wb, ws, nt, e0, ec, out, E, e0);
+    else if (ec % 2 == 0)
+        router_logits<2>(p, xb, wb, ws, nt, e0, ec, out, E, e0);
+    else
+        router_logits<1>(p, xb, wb, ws, nt, e0, ec, out, E, e0);
+    worker_sync();
+    if (P.C > 1) {  // tile reduction through the tile's event counter
+        if (wtid_() == 0) {
+            __threadfence();
+            ctl->flag = (atom_acq_rel_add(p.ev_tile + r, 1) == P.C - 1) ? 1 : 0;
+        }
+        worker_sync();
+        if (!ctl->flag) return;  // another chunk of this tile finishes it
+        if (wtid_() == 0) p.ev_tile[r] = 0;  // every chunk arrived: reset for the next call
+        for (int i = wtid_(); i < nt * E; i += kWorkers)
+            lg[i] = __ldcg(p.logits + static_cast<size_t>(t0) * E + i);
+        worker_sync();
+    }
+    for (int e = wtid_(); e < E; e += kWorkers) hs[e] = 0;
     worker_sync();
     // top-k per token (warp per token): order (logit desc, index asc)
     for (int tt = warp; tt < nt; tt += kWorkers / 32) {
@@ -197,9 +345,9 @@ __device__ __forceinline__ void router_task(const MoeArgs& p, int T, int r, uint
 // targets the later waits use (R permute tiles; F-tiles per chunk; the total
 // number of output tiles) are all derived here, on the device, from the
 // routing of this very call.
-__device__ __forceinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem, Ctl* ctl,
+__device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, uint8_t* smem, Ctl* ctl,
                                        const WaitCtx& wc) {
-    const int E = p.E, k = p.k, R = ceil_div(T, kRouterTile);
+    const int E = p.E, k = p.k, R = P.R, T = P.T;
     if (wtid_() == 0) ctl->flag = ev_wait_geq(wc, &p.hdr->ev_router, R, kWhereRouter) ? 1 : 0;
     worker_sync();
     if (!ctl->flag) return false;
@@ -230,7 +378,7 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem
         }
         const int total_mt = mtb_s[E];
         int S = 1;
-        if (T * k <= p.split_rows_cap && total_mt > 0) {
+        if (T * k <= p.split_rows_cap && total_mt > 0 && total_mt * HT < p.num_ctas) {
             const int down = total_mt * HT;
             int best = 1;
             for (int d = 2; d <= kSplitMax; ++d) {
@@ -258,8 +406,7 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem
             p.g_n[g] = n;
         }
     }
-    const int n_perm = R, n_gu = total_mt * FT, n_dn = total_mt * S * HT,
-              n_cb = ceil_div(T, kCombineTile);
+    const int n_perm = R * P.Q, n_gu = total_mt * FT, n_dn = total_mt * S * HT, n_cb = P.NC;
     const int total = n_perm + n_gu + n_dn + n_cb;
     if (total > p.q_max) {  // cannot happen for a valid workspace; fail loudly
         if (wtid_() == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereQueue);
@@ -268,7 +415,7 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem
     for (int q = wtid_(); q < total; q += kWorkers) {
         int4 d;
         if (q < n_perm) {
-            d = make_int4(kTaskPermute, q, 0, 0);
+            d = make_int4(kTaskPermute, q / P.Q, q % P.Q, 0);
         } else if (q < n_perm + n_gu) {
             const int i = q - n_perm;
             d = make_int4(kTaskGateUp, i / FT, i % FT, 0);
@@ -296,17 +443,19 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, int T, uint8_t* smem
 
 // Stable dispatch of router tile r: row (t, j) goes to off[e] + (rank of t
 // among this call's tokens routed to e), and its x row is copied there.
-__device__ __forceinline__ void permute_task(const MoeArgs& p, int T, int r, uint8_t* smem) {
+__device__ __forceinline__ void permute_task(const MoeArgs& p, const MoePlan& P, int r, int part,
+                                             uint8_t* smem) {
     const int k = p.k, E = p.E, H = p.H;
-    const int t0 = r * kRouterTile, nt = min(kRouterTile, T - t0), nent = nt * k;
+    const int t0 = r * kRouterTile, nt = min(kRouterTile, P.T - t0), nent = nt * k;
+    const int i0 = part * nent / P.Q, i1 = (part + 1) * nent / P.Q;  // this part's entries
     int* ie = reinterpret_cast<int*>(smem);  // [128]
     int* slot = ie + 128;                    // [128]
     for (int i = wtid_(); i < nent; i += kWorkers)
         ie[i] = __ldcg(p.idx + static_cast<size_t>(t0) * k + i);
     worker_sync();
-    for (int i = wtid_(); i < nent; i += kWorkers) {
+    for (int i = i0 + wtid_(); i < i1; i += kWorkers) {
         const int e = ie[i], tl = i / k;
-        int rank = 0;
+        int rank = 0;  // tokens before t in this tile routed to e (each at most once)
         for (int i2 = 0; i2 < tl * k; ++i2) rank += (ie[i2] == e);
         const int pp = __ldcg(p.base + static_cast<size_t>(r) * E + e) + rank;
         p.perm[pp] = t0 * k + i;
@@ -314,12 +463,26 @@ __device__ __forceinline__ void permute_task(const MoeArgs& p, int T, int r, uin
         slot[i] = pp;
     }
     worker_sync();
-    const int vpr = H / 8;
-    for (int v = wtid_(); v < nent * vpr; v += kWorkers) {
-        const int i = v / vpr, c = v % vpr;
-        const int t = t0 + i / k;
-        const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H) + c);
-        reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(slot[i]) * H)[c] = val;
+    const int vpr = H / 8, nvec = (i1 - i0) * vpr;
+    constexpr int U = 8;  // 16-byte row segments in flight per thread
+    for (int v0 = wtid_(); v0 < nvec; v0 += kWorkers * U) {
+        uint4 val[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * kWorkers;
+            if (v < nvec) {
+                const int i = i0 + v / vpr, c = v % vpr;
+                val[u] = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t0 + i / k) * H) + c);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * kWorkers;
+            if (v < nvec) {
+                const int i = i0 + v / vpr, c = v % vpr;
+                reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(slot[i]) * H)[c] = val[u];
+            }
+        }
     }
     fence_proxy_async_global();
     worker_sync();
@@ -331,7 +494,7 @@ __device__ __forceinline__ void permute_task(const MoeArgs& p, int T, int r, uin
 
 // ------------------------------------------------------------------ COMBINE
 
-__device__ __forceinline__ bool combine_task(const MoeArgs& p, int T, int c, Ctl* ctl,
+__device__ __forceinline__ bool combine_task(const MoeArgs& p, const MoePlan& P, int c, uint8_t* smem, Ctl* ctl,
                                           const WaitCtx& wc) {
     const int H = p.H, k = p.k;
     if (wtid_() == 0) {
@@ -340,47 +503,106 @@ __device__ __forceinline__ bool combine_task(const MoeArgs& p, int T, int c, Ctl
     }
     worker_sync();
     if (!ctl->flag) return false;
-    const int t0 = c * kCombineTile, nt = min(kCombineTile, T - t0), vpr = H / 8;
-    for (int v = wtid_(); v < nt * vpr; v += kWorkers) {
-        const int t = t0 + v / vpr, cc = v % vpr;
-        float acc[8];
+    const int t0 = c * P.CT, nt = min(P.CT, P.T - t0), vpr = H / 8;
+    float* w_s = reinterpret_cast<float*>(smem);           // [16 * k]
+    int* pos_s = reinterpret_cast<int*>(smem) + kCombineTile * 8;  // [16 * k]
+    for (int i = wtid_(); i < nt * k; i += kWorkers) {
+        w_s[i] = __ldcg(p.gw + static_cast<size_t>(t0) * k + i);
+        pos_s[i] = __ldcg(p.pos + static_cast<size_t>(t0) * k + i);
+    }
+    worker_sync();
+    constexpr int U = 4;  // output segments per thread and pass (U loads in flight per j)
+    const int nvec = nt * vpr;
+    for (int v0 = wtid_(); v0 < nvec; v0 += kWorkers * U) {
+        float acc[U][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const float wj = __ldcg(p.gw + static_cast<size_t>(t) * k + j);
-            const int row = __ldcg(p.pos + static_cast<size_t>(t) * k + j);
-            const uint4 raw = __ldcg(reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(row) * H) + cc);
-            float yv[8];
-            unpack8(raw, yv);
+        for (int u = 0; u < U; ++u)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, yv[i], acc[i]);
+            for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+        for (int j = 0; j < k; ++j) {  // fp32 sum in slot order j = 0 .. k-1
+            uint4 ys[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * kWorkers;
+                if (v < nvec) {
+                    const int tt = v / vpr, cc = v % vpr;
+                    ys[u] = __ldcg(reinterpret_cast<const uint4*>(
+                                       p.y + static_cast<size_t>(pos_s[tt * k + j]) * H) + cc);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * kWorkers;
+                if (v < nvec) {
+                    const float wj = w_s[(v / vpr) * k + j];
+                    float yv[8];
+                    unpack8(ys[u], yv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(wj, yv[i], acc[u][i]);
+                }
+            }
         }
-        reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * H)[cc] = pack8(acc);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * kWorkers;
+            if (v < nvec)
+                reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t0 + v / vpr) * H)[v % vpr] =
+                    pack8(acc[u]);
+        }
     }
     worker_sync();
     return true;
 }
+
+// ------------------------------------------------------------------ trace
+
+// Optional per-task record (see et_opts.trace): {type | role << 8, a, b, cta,
+// t_begin, t_end}.  role 0 = producer (pop .. loads issued), 1 = workers
+// (task received .. done), 2 = CTA (start .. set-up done), 3 = CTA exit.
+__device__ __forceinline__ void trace_rec(const MoeArgs& p, int type, int role, int a, int b,
+                                          uint64_t t0, uint64_t t1) {
+    if (!p.trace) return;
+    const unsigned long long i = atomicAdd(reinterpret_cast<unsigned long long*>(p.trace), 1ull);
+    if (i >= static_cast<unsigned long long>(p.trace_cap)) return;
+    int4* r = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(p.trace) + 32 + i * 32);
+    r[0] = make_int4(type | (role << 8), a, b, static_cast<int>(blockIdx.x));
+    uint64_t* t = reinterpret_cast<uint64_t*>(r + 1);
+    t[0] = t0;
+    t[1] = t1;
+}
+
+struct TraceScope {  // records the workers' task on scope exit (worker thread 0)
+    const MoeArgs& p;
+    int type, a, b;
+    uint64_t t0;
+    bool on;
+    __device__ __forceinline__ ~TraceScope() {
+        if (on) trace_rec(p, type, 1, a, b, t0, globaltimer_ns());
+    }
+};
 
 // ------------------------------------------------------------------ queue pop
 
 // Producer thread: next task of this CTA (EXIT when the queue is exhausted or
 // the launch aborted).  GEMM tasks carry their expert row-tile parameters,
 // read after the acquire of the published queue.
-__device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc, int R) {
+__device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc, const MoePlan& P) {
     TaskMsg m{};
     m.type = kTaskExit;
     if (aborted(wc)) return m;
     const int i = atomicAdd(&p.hdr->q_head, 1);
-    if (i < R) {
+    const int nr = P.R * P.C;
+    if (i < nr) {
         m.type = kTaskRouter;
-        m.a = i;
+        m.a = i / P.C;
+        m.b = i % P.C;
         return m;
     }
-    if (i == R) {
+    if (i == nr) {
         m.type = kTaskScan;
         return m;
     }
-    const int j = i - R - 1;
+    const int j = i - nr - 1;
     if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
     if (j >= ld_relaxed(&p.hdr->q_total)) return m;
     const int4 d = __ldcg(p.queue + j);
@@ -406,12 +628,14 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xp,
                const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ MoeArgs p) {
     extern __shared__ uint8_t smem_raw[];
+    const uint64_t t_start = globaltimer_ns();
     Stages stg;
     uint8_t* scratch;
     Ctl* ctl = cta_setup(smem_raw, p.stages, kMoeNMax, kMoeScratch, stg, &scratch);
     const WaitCtx wc{p.hdr, p.timeout_ns};
     const uint32_t tmem = ctl->tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) trace_rec(p, 0, 2, 0, 0, t_start, globaltimer_ns());
 
     int T = p.T_host;
     if (p.d_T) T = *reinterpret_cast<const volatile int32_t*>(p.d_T);
@@ -419,14 +643,14 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereBoundsT);
         T = 0;
     }
-    const int R = ceil_div(T, kRouterTile);
+    const MoePlan P = moe_plan(T, p.E, p.k, static_cast<int>(gridDim.x));
     const int FT = p.F / kTileM, HT = p.H / kTileM;
 
     auto gemm_of = [&](const TaskMsg& m) {
         const int type = m.type & 0xff, S = m.type >> 8;
         if (type == kTaskGateUp)
             return GemmTask{&tm_wg, &tm_wu, &tm_xp, m.e * p.F + m.b * kTileM, m.row0, 0,
-                            p.H / kBlockK, m.n, 1, &p.hdr->ev_perm, R, kWherePerm};
+                            p.H / kBlockK, m.n, 1, &p.hdr->ev_perm, P.R * P.Q, kWherePerm};
         const int fchunk = p.F / S;
         return GemmTask{&tm_wd, nullptr, &tm_h, m.e * p.H + m.c * kTileM, m.row0,
                         m.b * (fchunk / kBlockK), fchunk / kBlockK, m.n, m.n <= 64 ? 2 : 1,
@@ -438,7 +662,8 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
             uint32_t it = 0;
             for (int i = 0;; ++i) {
-                const TaskMsg m = pop_task(p, wc, R);
+                const uint64_t tp = globaltimer_ns();
+                const TaskMsg m = pop_task(p, wc, P);
                 const int slot = i % kTaskRing;
                 if (!mbar_wait(wc, &ctl->tq_empty[slot], ((i / kTaskRing) & 1) ^ 1, kWhereQueue))
                     break;
@@ -448,6 +673,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 if (type == kTaskExit) break;
                 if (type == kTaskGateUp || type == kTaskDown)
                     if (!produce_task(gemm_of(m), stg, ctl, it, wc, pol_w, pol_b)) break;
+                trace_rec(p, type, 0, m.a, m.b, tp, globaltimer_ns());
             }
         }
         __syncwarp();
@@ -479,20 +705,22 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             if (lane == 0) mbar_arrive(&ctl->tq_empty[slot]);
             const int type = m.type & 0xff, S = m.type >> 8;
             if (type == kTaskExit) break;
+            TraceScope trace_scope{p, type, m.a, m.b, p.trace ? globaltimer_ns() : 0ull,
+                                   p.trace != nullptr && wtid == 0};
             if (type == kTaskRouter) {
-                router_task(p, T, m.a, scratch);
+                router_task(p, P, m.a, m.b, scratch, stg.base, static_cast<size_t>(stg.n) * stg.bytes, ctl);
                 continue;
             }
             if (type == kTaskScan) {
-                if (!scan_task(p, T, scratch, ctl, wc)) break;
+                if (!scan_task(p, P, scratch, ctl, wc)) break;
                 continue;
             }
             if (type == kTaskPermute) {
-                permute_task(p, T, m.a, scratch);
+                permute_task(p, P, m.a, m.b, scratch);
                 continue;
             }
             if (type == kTaskCombine) {
-                if (!combine_task(p, T, m.a, ctl, wc)) break;
+                if (!combine_task(p, P, m.a, scratch, ctl, wc)) break;
                 continue;
             }
             uint32_t acc;
@@ -572,8 +800,10 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         }
     }
 
+    const uint64_t t_exit = globaltimer_ns();
     const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
     cta_teardown(ctl, stg, aborted_run);
+    if (threadIdx.x == 0) trace_rec(p, 0, 3, 0, 0, t_exit, globaltimer_ns());
 
     // Exit protocol: the last CTA out returns every counter to zero.
     __syncthreads();

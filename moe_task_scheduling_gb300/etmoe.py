@@ -22,8 +22,9 @@ STATUS_NAMES = {0: "ET_OK", 1: "ET_ERR_INVALID", 2: "ET_ERR_WORKSPACE", 3: "ET_E
 
 
 class et_opts(ctypes.Structure):
-    _fields_ = [("timeout_us", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
-                ("fault_mode", ctypes.c_int32), ("fault_arg", ctypes.c_int32)]
+    _fields_ = [("timeout_us", ctypes.c_uint32), ("trace_cap", ctypes.c_uint32),
+                ("fault_mode", ctypes.c_int32), ("fault_arg", ctypes.c_int32),
+                ("trace", ctypes.c_void_p)]
 
 
 class EtError(RuntimeError):
@@ -92,10 +93,30 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream
 
 
-def _opts(timeout_us=0, fault_mode=0, fault_arg=0):
-    if not (timeout_us or fault_mode):
+def _opts(timeout_us=0, fault_mode=0, fault_arg=0, trace=None):
+    if not (timeout_us or fault_mode or trace is not None):
         return None
-    return ctypes.byref(et_opts(timeout_us, 0, fault_mode, fault_arg))
+    cap = 0 if trace is None else (trace.numel() * trace.element_size() - 32) // 32
+    return ctypes.byref(et_opts(timeout_us, cap, fault_mode, fault_arg, _ptr(trace)))
+
+
+def alloc_trace(records: int, device="cuda"):
+    """A zeroed device buffer for `records` trace records (see et_opts.trace)."""
+    import torch
+    return torch.zeros(32 + 32 * records, dtype=torch.uint8, device=device)
+
+
+def read_trace(buf):
+    """Decode a trace buffer: list of (type, role, a, b, cta, t_begin_ns, t_end_ns)."""
+    import numpy as np
+    raw = buf.cpu().numpy()
+    n = int(raw[:8].view(np.uint64)[0])
+    cap = (raw.size - 32) // 32
+    rec = raw[32:32 + 32 * min(n, cap)].reshape(-1, 32)
+    ints = rec[:, :16].copy().view(np.int32).reshape(-1, 4)
+    ts = rec[:, 16:].copy().view(np.uint64).reshape(-1, 2)
+    return [(int(i[0]) & 0xff, int(i[0]) >> 8, int(i[1]), int(i[2]), int(i[3]), int(t[0]), int(t[1]))
+            for i, t in zip(ints, ts)]
 
 
 def _check(rc):
@@ -133,7 +154,8 @@ def alloc_workspace(nbytes: int, device="cuda"):
 
 def et_moe_layer(x, w_router, router_bias, w_gate, w_up, w_down, out, *, k, T=None, d_T=None,
                  T_max=None, topk_idx=None, topk_w=None, expert_counts=None, perm=None,
-                 workspace, stream=None, timeout_us=0, fault_mode=0, fault_arg=0, check=True):
+                 workspace, stream=None, timeout_us=0, fault_mode=0, fault_arg=0, trace=None,
+                 check=True):
     H = x.shape[1]
     E = w_router.shape[1]
     F = w_gate.shape[1]
@@ -143,7 +165,7 @@ def et_moe_layer(x, w_router, router_bias, w_gate, w_up, w_down, out, *, k, T=No
         _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
         _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts), _ptr(perm), T, _ptr(d_T),
         T_max, H, F, E, k, _ptr(workspace), workspace.numel() if hasattr(workspace, "numel") else 0,
-        _opts(timeout_us, fault_mode, fault_arg), _stream(stream))
+        _opts(timeout_us, fault_mode, fault_arg, trace), _stream(stream))
     if check:
         _check(rc)
     return rc
