@@ -1,33 +1,44 @@
 // et_gemm.cuh -- persistent, warp-specialised tile-GEMM pipeline:
 //   D[128 weight rows, n token rows] = sum_k W[a_row.., k] * Act[b_row.., k]
 // with the weight tile on the UMMA M side ("swap-AB": decode-sized token
-// counts sit on N, which may be as small as 16).
+// counts sit on N, which may be as small as 16 and as large as 256).
 //
 // Each role runs its own loop over the CTA's task sequence and meets the
 // others only through mbarriers -- there is no CTA-wide barrier inside a loop:
-//   warp 0 lane 0   TMA producer: waits for a free stage, posts its byte
-//                   count, loads the weight tile(s) and the activation rows;
-//                   a task with a dependency loads its first weight tiles
-//                   *before* it waits on the event, so the weight stream is
-//                   already in flight when the dependency resolves;
-//   warp 1 lane 0   MMA issuer: per task, waits for a free TMEM accumulator
-//                   buffer, issues tcgen05.mma per full stage, frees each
-//                   stage with tcgen05.commit, commits the accumulator;
+//   warp 0 lane 0   TMA producer: reserves ring space for one k-block fill,
+//                   posts its byte count, loads the weight tile(s) and the
+//                   activation rows; a task with a dependency loads the
+//                   weight tiles of the fills that fit *before* it waits on
+//                   the event, so the weight stream is already in flight
+//                   when the dependency resolves;
+//   warp 1 lane 0   MMA issuer: per task, waits for free TMEM accumulator
+//                   slots, issues tcgen05.mma per full fill, frees each fill
+//                   with tcgen05.commit, commits the accumulator slots;
 //   warps 4..7      workers: the epilogue (tcgen05.ld from TMEM, stores,
 //                   event releases) and every non-GEMM task; they sync among
 //                   themselves with named barrier 1.
-// Two TMEM accumulator buffers of 256 columns let the MMA of task i+1 run
-// while the workers drain task i.
+//
+// The stage ring is byte-granular: a fill takes exactly the bytes of its
+// k-block (weights 16 or 32 KB, plus n * 128 bytes of activation rows), so a
+// decode-sized task keeps many more weight bytes in flight than a wide one.
+// Producer and MMA issuer place fills with the same deterministic rule; only
+// the producer waits for space, releasing older fills in order.
+//
+// TMEM holds two accumulator slots of 256 columns.  A task takes one slot
+// (gate and up side by side when n <= 128) or both (gate/up with n > 128), so
+// the MMA of the next task overlaps the epilogue of the last one whenever the
+// accumulators fit.
 #pragma once
 
 #include "et_device.cuh"
 
 namespace et {
 
-constexpr int kTaskRing = 4;      // dynamic-queue tasks handed from producer to consumers
-constexpr int kWorkers = 128;     // warps 4..7
-constexpr int kWorkerBar = 1;     // named barrier id of the worker group
-constexpr int kAccBufCols = 256;  // TMEM columns per accumulator buffer
+constexpr int kTaskRing = 4;       // dynamic-queue tasks handed from producer to consumers
+constexpr int kWorkers = 128;      // warps 4..7
+constexpr int kWorkerBar = 1;      // named barrier id of the worker group
+constexpr int kSlots = 16;         // ring fills in flight at most (one barrier pair each)
+constexpr int kAccSlotCols = 256;  // TMEM columns per accumulator slot
 
 // One task as handed through the smem ring (dynamic schedules).
 struct TaskMsg {
@@ -37,28 +48,29 @@ struct TaskMsg {
 
 // Per-CTA control block, after the stage ring and the SIMT scratch in smem.
 struct Ctl {
-    uint64_t full[kMaxStages];
-    uint64_t empty[kMaxStages];
+    uint64_t full[kSlots];
+    uint64_t empty[kSlots];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t tq_full[kTaskRing];
     uint64_t tq_empty[kTaskRing];
     uint64_t drain;
+    uint64_t sbar;                // worker staging copies (bulk async)
     TaskMsg tq[kTaskRing];
+    uint32_t unit_end[kSlots];    // producer: ring end position of each fill in flight
     uint32_t tmem_base;
-    int32_t issued;    // stage fills posted by the producer (for the unwind)
-    int32_t consumed;  // stage fills consumed by the MMA issuer
+    int32_t issued;    // fills posted by the producer (for the unwind)
+    int32_t consumed;  // fills consumed by the MMA issuer
     int32_t flag;      // worker broadcast
     int32_t wflag[2];  // worker_wait decisions, double buffered
+    int32_t ring_ret;  // ring leases the workers have returned
     int32_t scratch[16];
 };
 
-// Stage ring geometry: stage = [A0 16K][A1 16K][B nmax*128].
-struct Stages {
+// The byte ring of stage fills.
+struct Ring {
     uint8_t* base;
-    int n;
-    int bytes;
-    int b_off;
+    uint32_t bytes;
 };
 
 struct GemmTask {
@@ -68,126 +80,215 @@ struct GemmTask {
     int a_row;              // first weight row
     int b_row;              // first activation row
     int kb0, nkb;           // k-blocks [kb0, kb0 + nkb), 64 elements each
-    int n;                  // UMMA N: multiple of 16
-    int kpack;              // k-blocks per stage when a1 == nullptr (1 or 2)
+    int n;                  // UMMA N: multiple of 16, <= 256
     const int* dep;         // wait *dep >= dep_target before activation loads
     int dep_target;
     int dep_where;
 };
 
-__device__ __forceinline__ int kpack_of(const GemmTask& t) { return t.a1 ? 1 : t.kpack; }
+// One k-block: [A0 16K][A1 16K if gate/up][B n*128].  A fill packs two
+// consecutive k-blocks when one is small (a narrow down-projection tile), so
+// the weight rows are requested 256 contiguous bytes at a time.
+__device__ __forceinline__ uint32_t kblock_bytes(const GemmTask& t) {
+    return (t.a1 ? 2u : 1u) * kABytes + static_cast<uint32_t>(t.n) * 128u;
+}
+__device__ __forceinline__ int kpack_of(const GemmTask& t) {
+    return kblock_bytes(t) <= 24576u ? 2 : 1;
+}
+__device__ __forceinline__ int fills_of(const GemmTask& t) { return ceil_div(t.nkb, kpack_of(t)); }
+// Fill layout: [A0 x kp][A1 x kp][B x kp] (every tile 1024-byte aligned); a
+// ragged last fill is placed with the full size.
+__device__ __forceinline__ uint32_t unit_bytes(const GemmTask& t) {
+    return static_cast<uint32_t>(kpack_of(t)) * kblock_bytes(t);
+}
+
+// TMEM accumulator slots a task takes: gate/up needs 2n columns.
+__host__ __device__ __forceinline__ uint32_t acc_slots(bool two, int n) {
+    return (two ? 2 * n : n) > kAccSlotCols ? 2u : 1u;
+}
+
+// Ring placement shared by producer and MMA issuer: a fill that would run
+// past the end starts again at offset 0.  Positions are monotonic; the
+// address is base + position % bytes.
+__device__ __forceinline__ uint32_t ring_place(uint32_t& head, uint32_t sb, uint32_t rb) {
+    const uint32_t off = head % rb;
+    if (off + sb > rb) head += rb - off;
+    const uint32_t start = head;
+    head += sb;
+    return start;
+}
 
 // ------------------------------------------------------------------ producer
 
-// Issues every load of one GEMM task.  `it` counts stage fills over the
-// whole launch (stage = it % n, phase = (it / n) & 1).  With a dependency,
-// the weight tiles of the first min(units, stages) fills are posted first,
-// then the event is awaited, then their activation rows follow.
-__device__ __forceinline__ void load_acts(const GemmTask& t, const Stages& s, Ctl* ctl, uint32_t f,
-                                          int u, uint64_t pol_b) {
-    const int kp = kpack_of(t);
-    const int st = static_cast<int>(f % s.n);
-    const int nk = min(kp, t.nkb - u * kp);
-    const uint32_t bbytes = static_cast<uint32_t>(t.n) * 128u;
-    uint8_t* bb = s.base + st * s.bytes + s.b_off;
-    for (int j = 0; j < nk; ++j)
-        for (int i = 0; i < t.n / kBBoxRows; ++i)
-            tma_load_2d(bb + j * bbytes + i * (kBBoxRows * 128), t.b, &ctl->full[st],
-                        (t.kb0 + u * kp + j) * kBlockK, t.b_row + i * kBBoxRows, pol_b);
+struct ProdState {
+    uint32_t it = 0;    // fills posted
+    uint32_t head = 0;  // ring position after the last placed fill
+    uint32_t rel = 0;   // fills known to be released
+    uint32_t tail = 0;  // ring end position of the newest released fill
+    uint32_t leases = 0;  // SIMT tasks handed to the workers (each leases the ring)
+};
+
+// A SIMT task may use the ring as staging space: the producer hands it over
+// (a lease) and posts no fill until the workers have returned every lease.
+// Every earlier fill is already consumed when the workers start that task
+// (they take tasks in order, after the epilogue of the last GEMM).
+__device__ __forceinline__ bool ring_lease_wait(Ctl* ctl, const ProdState& ps, const WaitCtx& wc) {
+    const volatile int32_t* ret = &ctl->ring_ret;
+    if (*ret < static_cast<int32_t>(ps.leases)) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1; *ret < static_cast<int32_t>(ps.leases); ++it) {
+            if ((it & 15u) == 0) {
+                if (aborted(wc)) return false;
+                if (globaltimer_ns() - t0 > wc.timeout_ns) {
+                    raise_error(wc, ET_ERR_TIMEOUT, kWhereStage);
+                    return false;
+                }
+            }
+        }
+    }
+    fence_proxy_async_smem();  // the workers' use of the ring precedes the next TMA writes
+    return true;
 }
 
-__device__ __forceinline__ bool post_weights(const GemmTask& t, const Stages& s, Ctl* ctl,
-                                             uint32_t f, int u, const WaitCtx& wc,
-                                             uint64_t pol_w) {
-    const int kp = kpack_of(t);
-    const int st = static_cast<int>(f % s.n);
-    if (!mbar_wait(wc, &ctl->empty[st], ((f / s.n) & 1u) ^ 1u, kWhereEmpty)) return false;
-    const int nk = min(kp, t.nkb - u * kp);
-    const uint32_t bytes = (t.a1 ? 2u : static_cast<uint32_t>(nk)) * kABytes +
-                           static_cast<uint32_t>(nk) * static_cast<uint32_t>(t.n) * 128u;
-    mbar_arrive_expect_tx(&ctl->full[st], bytes);
-    uint8_t* sb = s.base + st * s.bytes;
-    const int kb = t.kb0 + u * kp;
-    if (t.a1) {
-        tma_load_2d(sb, t.a0, &ctl->full[st], kb * kBlockK, t.a_row, pol_w);
-        tma_load_2d(sb + kABytes, t.a1, &ctl->full[st], kb * kBlockK, t.a_row, pol_w);
-    } else {
-        for (int j = 0; j < nk; ++j)
-            tma_load_2d(sb + j * kABytes, t.a0, &ctl->full[st], (kb + j) * kBlockK, t.a_row, pol_w);
+// Wait, oldest first, for released fills until a fill of `sb` bytes at
+// `start` has both a barrier slot and its bytes free.
+__device__ __forceinline__ bool ring_reserve(Ctl* ctl, ProdState& ps, uint32_t start, uint32_t sb,
+                                             uint32_t rb, const WaitCtx& wc) {
+    while (ps.rel < ps.it && (ps.it - ps.rel >= static_cast<uint32_t>(kSlots) ||
+                              start + sb > ps.tail + rb)) {
+        const uint32_t slot = ps.rel % kSlots;
+        if (!mbar_wait(wc, &ctl->empty[slot], (ps.rel / kSlots) & 1u, kWhereEmpty)) return false;
+        ps.tail = ctl->unit_end[slot];
+        ++ps.rel;
     }
     return true;
 }
 
-__device__ __forceinline__ bool produce_task(const GemmTask& t, const Stages& s, Ctl* ctl,
-                                             uint32_t& it, const WaitCtx& wc, uint64_t pol_w,
+// Reserve and post fill `u` of task t (its byte count, its weight tiles).
+__device__ __forceinline__ bool post_weights(const GemmTask& t, const Ring& R, Ctl* ctl,
+                                             ProdState& ps, int u, const WaitCtx& wc,
+                                             uint64_t pol_w) {
+    const uint32_t sb = unit_bytes(t);
+    const uint32_t start = ring_place(ps.head, sb, R.bytes);
+    if (!ring_reserve(ctl, ps, start, sb, R.bytes, wc)) return false;
+    const uint32_t slot = ps.it % kSlots;
+    ctl->unit_end[slot] = start + sb;
+    const int kp = kpack_of(t), nk = min(kp, t.nkb - u * kp);
+    mbar_arrive_expect_tx(&ctl->full[slot], static_cast<uint32_t>(nk) * kblock_bytes(t));
+    uint8_t* dst = R.base + start % R.bytes;
+    for (int j = 0; j < nk; ++j) {
+        const int kx = (t.kb0 + u * kp + j) * kBlockK;
+        tma_load_2d(dst + j * kABytes, t.a0, &ctl->full[slot], kx, t.a_row, pol_w);
+        if (t.a1)
+            tma_load_2d(dst + (kp + j) * kABytes, t.a1, &ctl->full[slot], kx, t.a_row, pol_w);
+    }
+    ++ps.it;
+    return true;
+}
+
+// Activation rows of fill number `f` (already posted) = fill u of task t.
+__device__ __forceinline__ void load_acts(const GemmTask& t, const Ring& R, Ctl* ctl, uint32_t f,
+                                          int u, uint64_t pol_b) {
+    const uint32_t slot = f % kSlots;
+    const uint32_t start = ctl->unit_end[slot] - unit_bytes(t);
+    const int kp = kpack_of(t), nk = min(kp, t.nkb - u * kp);
+    const uint32_t bbytes = static_cast<uint32_t>(t.n) * 128u;
+    uint8_t* bb = R.base + start % R.bytes + static_cast<uint32_t>(kp) * (t.a1 ? 2u : 1u) * kABytes;
+    for (int j = 0; j < nk; ++j) {
+        const int kx = (t.kb0 + u * kp + j) * kBlockK;
+        for (int i = 0; i < t.n / kBBoxRows; ++i)
+            tma_load_2d(bb + j * bbytes + i * (kBBoxRows * 128), t.b, &ctl->full[slot], kx,
+                        t.b_row + i * kBBoxRows, pol_b);
+    }
+}
+
+__device__ __forceinline__ bool produce_task(const GemmTask& t, const Ring& R, Ctl* ctl,
+                                             ProdState& ps, const WaitCtx& wc, uint64_t pol_w,
                                              uint64_t pol_b) {
-    const int units = ceil_div(t.nkb, kpack_of(t));
-    const int pre = t.dep ? min(units, s.n) : 0;
+    if (!ring_lease_wait(ctl, ps, wc)) return false;
+    const uint32_t sb = unit_bytes(t);
+    const int nfill = fills_of(t);
+    int pre = 0;
+    if (t.dep) {  // fills whose space frees up without any fill of this task
+        uint32_t h = ps.head;
+        const uint32_t limit = ps.head + R.bytes;
+        while (pre < nfill && pre < kSlots) {
+            const uint32_t st = ring_place(h, sb, R.bytes);
+            if (st + sb > limit) break;
+            ++pre;
+        }
+    }
+    const uint32_t f0 = ps.it;
     bool ok = true;
     int posted = 0;
     for (int u = 0; u < pre && ok; ++u) {  // weights first, ahead of the dependency
-        ok = post_weights(t, s, ctl, it + u, u, wc, pol_w);
+        ok = post_weights(t, R, ctl, ps, u, wc, pol_w);
         if (ok) posted = u + 1;
     }
     if (ok && t.dep) {
         ok = ev_wait_geq(wc, t.dep, t.dep_target, t.dep_where);
         if (ok) {
             fence_proxy_async_global();  // rows written by other CTAs' generic stores
-            for (int u = 0; u < pre; ++u) load_acts(t, s, ctl, it + u, u, pol_b);
+            for (int u = 0; u < posted; ++u) load_acts(t, R, ctl, f0 + u, u, pol_b);
         }
     }
-    for (int u = pre; u < units && ok; ++u) {
-        ok = post_weights(t, s, ctl, it + u, u, wc, pol_w);
-        if (ok) {
-            posted = u + 1;
-            load_acts(t, s, ctl, it + u, u, pol_b);
-        }
+    for (int u = pre; u < nfill && ok; ++u) {
+        ok = post_weights(t, R, ctl, ps, u, wc, pol_w);
+        if (ok) load_acts(t, R, ctl, ps.it - 1, u, pol_b);
     }
-    it += posted;
-    ctl->issued = static_cast<int32_t>(it);
+    ctl->issued = static_cast<int32_t>(ps.it);
     return ok;
 }
 
 // ------------------------------------------------------------------ MMA issuer
 
-// `it` counts consumed stage fills; `g` counts GEMM tasks (accumulator
-// buffer = g % nbuf).  u_off is the column offset of the second accumulator.
-__device__ __forceinline__ bool mma_task(const GemmTask& t, const Stages& s, Ctl* ctl, uint32_t& it,
-                                         uint32_t& g, int nbuf, uint32_t u_off, uint32_t tmem,
-                                         const WaitCtx& wc) {
-    const uint32_t buf = g % nbuf, use = g / nbuf;
-    if (!mbar_wait(wc, &ctl->acc_empty[buf], (use & 1u) ^ 1u, kWhereAcc)) return false;
+struct MmaState {
+    uint32_t it = 0;    // fills consumed
+    uint32_t head = 0;  // ring position (same placement as the producer)
+    uint32_t acc = 0;   // accumulator slots taken
+};
+
+__device__ __forceinline__ bool mma_task(const GemmTask& t, const Ring& R, Ctl* ctl, MmaState& ms,
+                                         uint32_t tmem, const WaitCtx& wc) {
+    const uint32_t w = acc_slots(t.a1 != nullptr, t.n);
+    for (uint32_t i = 0; i < w; ++i) {
+        const uint32_t s = ms.acc + i;
+        if (!mbar_wait(wc, &ctl->acc_empty[s & 1u], ((s >> 1) & 1u) ^ 1u, kWhereAcc)) return false;
+    }
     tc_fence_after();
-    const int kp = kpack_of(t);
-    const int units = ceil_div(t.nkb, kp);
-    const uint32_t idesc = idesc_bf16_m128(t.n);
+    const uint32_t acc0 = tmem + (ms.acc & 1u) * kAccSlotCols;
+    const uint32_t acc1 =
+        w == 2 ? tmem + ((ms.acc + 1) & 1u) * kAccSlotCols : acc0 + kAccSlotCols / 2;
+    const uint32_t sb = unit_bytes(t);
+    const int kp = kpack_of(t), nfill = fills_of(t);
     const uint32_t bbytes = static_cast<uint32_t>(t.n) * 128u;
-    const uint32_t acc0 = tmem + buf * kAccBufCols;
-    const uint32_t acc1 = acc0 + u_off;
-    for (int u = 0; u < units; ++u) {
-        const int st = static_cast<int>(it % s.n);
-        if (!mbar_wait(wc, &ctl->full[st], (it / s.n) & 1u, kWhereFull)) return false;
-        it += 1;
-        ctl->consumed = static_cast<int32_t>(it);
+    const uint32_t b_off = static_cast<uint32_t>(kp) * (t.a1 ? 2u : 1u) * kABytes;
+    const uint32_t idesc = idesc_bf16_m128(t.n);
+    for (int u = 0; u < nfill; ++u) {
+        const uint32_t start = ring_place(ms.head, sb, R.bytes);
+        const uint32_t slot = ms.it % kSlots;
+        if (!mbar_wait(wc, &ctl->full[slot], (ms.it / kSlots) & 1u, kWhereFull)) return false;
+        ms.it += 1;
+        ctl->consumed = static_cast<int32_t>(ms.it);
         tc_fence_after();
-        const uint32_t sb = smem_u32(s.base + st * s.bytes);
+        const uint32_t base = smem_u32(R.base + start % R.bytes);
         const int nk = min(kp, t.nkb - u * kp);
         for (int j = 0; j < nk; ++j) {
-            const uint32_t a_s = sb + (t.a1 ? 0u : static_cast<uint32_t>(j) * kABytes);
-            const uint32_t b_s = sb + s.b_off + static_cast<uint32_t>(j) * bbytes;
+            const uint32_t a_s = base + j * kABytes;
+            const uint32_t a1_s = base + (kp + j) * kABytes;
+            const uint32_t b_s = base + b_off + j * bbytes;
 #pragma unroll
             for (int kk = 0; kk < kBlockK / 16; ++kk) {
                 const uint32_t accumulate = (u > 0 || j > 0 || kk > 0) ? 1u : 0u;
                 const uint64_t bd = sdesc_sw128(b_s + kk * 32);
                 tc_mma_bf16(acc0, sdesc_sw128(a_s + kk * 32), bd, idesc, accumulate);
-                if (t.a1)
-                    tc_mma_bf16(acc1, sdesc_sw128(sb + kABytes + kk * 32), bd, idesc, accumulate);
+                if (t.a1) tc_mma_bf16(acc1, sdesc_sw128(a1_s + kk * 32), bd, idesc, accumulate);
             }
         }
-        tc_commit(&ctl->empty[st]);
+        tc_commit(&ctl->empty[slot]);
     }
-    tc_commit(&ctl->acc_full[buf]);
-    g += 1;
+    for (uint32_t i = 0; i < w; ++i) tc_commit(&ctl->acc_full[(ms.acc + i) & 1u]);
+    ms.acc += w;
     return true;
 }
 
@@ -208,44 +309,85 @@ __device__ __forceinline__ bool worker_wait(Ctl* ctl, uint64_t* bar, uint32_t pa
     return ctl->wflag[slot] != 0;
 }
 
-// Wait for the accumulator of the workers' next GEMM task; returns its TMEM
-// base (lane 0, first column of the buffer) through `acc`.
-__device__ __forceinline__ bool epi_acquire(Ctl* ctl, uint32_t g, int nbuf, uint32_t tmem,
-                                            const WaitCtx& wc, uint32_t& acc, uint32_t& seq) {
-    const uint32_t buf = g % nbuf, use = g / nbuf;
-    if (!worker_wait(ctl, &ctl->acc_full[buf], use & 1u, wc, kWhereAcc, seq)) return false;
+// The workers' view of the accumulator slots.
+struct EpiState {
+    uint32_t acc = 0;   // accumulator slots consumed
+    uint32_t seq = 0;   // worker_wait calls
+};
+
+// Wait for the accumulator slot(s) of the workers' next GEMM task; returns
+// the TMEM address (lane 0) of the first and the second accumulator.
+__device__ __forceinline__ bool epi_acquire(Ctl* ctl, EpiState& es, bool two, int n, uint32_t tmem,
+                                            const WaitCtx& wc, uint32_t& acc0, uint32_t& acc1) {
+    const uint32_t w = acc_slots(two, n);
+    for (uint32_t i = 0; i < w; ++i) {
+        const uint32_t s = es.acc + i;
+        if (!worker_wait(ctl, &ctl->acc_full[s & 1u], (s >> 1) & 1u, wc, kWhereAcc, es.seq))
+            return false;
+    }
     tc_fence_after();
-    acc = tmem + buf * kAccBufCols;
+    acc0 = tmem + (es.acc & 1u) * kAccSlotCols;
+    acc1 = w == 2 ? tmem + ((es.acc + 1) & 1u) * kAccSlotCols : acc0 + kAccSlotCols / 2;
     return true;
 }
 
-// The worker warp is done reading the accumulator buffer of task g.
-__device__ __forceinline__ void epi_release(Ctl* ctl, uint32_t g, int nbuf) {
+// The worker warp is done reading the accumulator slot(s) of its task.
+__device__ __forceinline__ void epi_release(Ctl* ctl, EpiState& es, bool two, int n) {
+    const uint32_t w = acc_slots(two, n);
     tc_fence_before();
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->acc_empty[g % nbuf]);
+    if ((threadIdx.x & 31) == 0)
+        for (uint32_t i = 0; i < w; ++i) mbar_arrive(&ctl->acc_empty[(es.acc + i) & 1u]);
+    es.acc += w;
+}
+
+// Bulk (async-proxy) staging by the workers: worker thread 0 posts `bytes`
+// on the staging barrier and issues the copies; all workers then wait.
+// `sphase` is the workers' running count of staging rounds.
+__device__ __forceinline__ bool staging_wait(Ctl* ctl, uint32_t& sphase, const WaitCtx& wc,
+                                             uint32_t& seq) {
+    const uint32_t parity = sphase & 1u;
+    const bool ok = worker_wait(ctl, &ctl->sbar, parity, wc, kWhereStage, seq);
+    ++sphase;
+    // the phase has completed: every worker observes it itself, which makes
+    // the async-proxy writes visible to its own reads
+    if (ok) (void)mbar_try_wait(&ctl->sbar, parity);
+    return ok;
+}
+
+// The workers are done with the ring after a SIMT task: return the lease.
+__device__ __forceinline__ void ring_return(Ctl* ctl) {
+    worker_sync();
+    if (threadIdx.x == kEpiWarp0 * 32) {
+        fence_proxy_async_smem();
+        __threadfence_block();
+        *reinterpret_cast<volatile int32_t*>(&ctl->ring_ret) = ctl->ring_ret + 1;
+    }
 }
 
 // ------------------------------------------------------------------ set-up / unwind
 
-// Dynamic smem layout: [align 1024][stages x stage_bytes][scratch][Ctl].
-__host__ __device__ constexpr int smem_bytes_for(int stages, int nmax, int scratch) {
-    return 1024 + stages * stage_bytes(nmax) + scratch + static_cast<int>(sizeof(Ctl));
+// Stage ring bytes that fit next to `scratch` bytes of SIMT scratch.
+__host__ __device__ constexpr int ring_bytes_for(int scratch) {
+    return (kSmemLimit - 1024 - scratch - static_cast<int>(sizeof(Ctl))) / 1024 * 1024;
 }
 
-__device__ __forceinline__ Ctl* cta_setup(uint8_t* smem_raw, int stages, int nmax, int scratch,
-                                          Stages& s, uint8_t** scratch_out) {
+// Dynamic smem layout: [align 1024][ring][scratch][Ctl].
+__host__ __device__ constexpr int smem_bytes_for(int scratch) {
+    return 1024 + ring_bytes_for(scratch) + scratch + static_cast<int>(sizeof(Ctl));
+}
+
+__device__ __forceinline__ Ctl* cta_setup(uint8_t* smem_raw, int scratch, Ring& R,
+                                          uint8_t** scratch_out) {
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    s.base = base;
-    s.n = stages;
-    s.bytes = stage_bytes(nmax);
-    s.b_off = 2 * kABytes;
-    *scratch_out = base + stages * s.bytes;
-    Ctl* ctl = reinterpret_cast<Ctl*>(base + stages * s.bytes + scratch);
+    R.base = base;
+    R.bytes = static_cast<uint32_t>(ring_bytes_for(scratch));
+    *scratch_out = base + R.bytes;
+    Ctl* ctl = reinterpret_cast<Ctl*>(base + R.bytes + scratch);
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kMaxStages; ++i) {
+        for (int i = 0; i < kSlots; ++i) {
             mbar_init(&ctl->full[i], 1);
             mbar_init(&ctl->empty[i], 1);
         }
@@ -258,8 +400,10 @@ __device__ __forceinline__ Ctl* cta_setup(uint8_t* smem_raw, int stages, int nma
             mbar_init(&ctl->tq_empty[i], 1 + kWorkers / 32);  // MMA thread + worker warps
         }
         mbar_init(&ctl->drain, 1);
+        mbar_init(&ctl->sbar, 1);
         ctl->issued = 0;
         ctl->consumed = 0;
+        ctl->ring_ret = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -275,13 +419,13 @@ __device__ __forceinline__ Ctl* cta_setup(uint8_t* smem_raw, int stages, int nma
 // After every role has left its loop (call with the whole CTA): if the launch
 // aborted, let this CTA's own TMA copies and MMAs land (bounded, without
 // raising), then release TMEM.
-__device__ __forceinline__ void cta_teardown(Ctl* ctl, const Stages& s, bool aborted_run) {
+__device__ __forceinline__ void cta_teardown(Ctl* ctl, bool aborted_run) {
     __syncthreads();
     if (aborted_run && threadIdx.x == 32) {
         const uint64_t budget = 2000000ull;  // 2 ms per wait
         for (uint32_t c = static_cast<uint32_t>(ctl->consumed);
              c < static_cast<uint32_t>(ctl->issued); ++c)
-            mbar_drain(&ctl->full[c % s.n], (c / s.n) & 1u, budget);
+            mbar_drain(&ctl->full[c % kSlots], (c / kSlots) & 1u, budget);
         tc_commit(&ctl->drain);
         mbar_drain(&ctl->drain, 0, budget);
     }
@@ -289,14 +433,6 @@ __device__ __forceinline__ void cta_teardown(Ctl* ctl, const Stages& s, bool abo
     __syncthreads();
     tc_fence_after();
     if ((threadIdx.x >> 5) == 1) tmem_dealloc(ctl->tmem_base, kTmemCols);
-}
-
-// Stages that fit next to `scratch` bytes of SIMT scratch.
-__host__ __device__ constexpr int stages_for(int nmax, int scratch) {
-    return (kSmemLimit - 1024 - scratch - static_cast<int>(sizeof(Ctl))) / stage_bytes(nmax) >
-                   kMaxStages
-               ? kMaxStages
-               : (kSmemLimit - 1024 - scratch - static_cast<int>(sizeof(Ctl))) / stage_bytes(nmax);
 }
 
 }  // namespace et

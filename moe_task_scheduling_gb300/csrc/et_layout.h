@@ -20,14 +20,13 @@ constexpr int kTileM = 128;          // weight rows per tile (UMMA M)
 constexpr int kBlockK = 64;          // bf16 elements per k-block = one 128-byte swizzle row
 constexpr int kABytes = kTileM * kBlockK * 2;   // 16 KB weight tile
 constexpr int kBBoxRows = 16;        // activation rows per TMA box
-constexpr int kMaxStages = 8;
 constexpr int kTmemCols = 512;       // accumulator 0 at column 0, accumulator 1 at 256
 constexpr int kAcc1Col = 256;
 constexpr int kSmemLimit = 232448;   // 227 KB of opt-in dynamic shared memory per CTA
 constexpr int kSplitMax = 8;         // largest split of the MoE / MLP down projection
 
 // MoE
-constexpr int kMoeNMax = 128;        // token rows per expert tile (UMMA N)
+constexpr int kMoeNMax = 256;        // token rows per expert tile (UMMA N)
 constexpr int kRouterTile = 16;      // tokens per router tile (router and permute tasks)
 constexpr int kCombineTile = 16;     // most tokens per combine task
 constexpr int kMoeSplitRowsCap = 512;  // split the down projection only up to T*k rows
@@ -70,7 +69,8 @@ enum WaitWhere {
     kWhereH = 7,
     kWhereY = 8,
     kWhereNorm = 9,
-    kWhereBoundsT = 10
+    kWhereBoundsT = 10,
+    kWhereStage = 11
 };
 
 // Task descriptor of the dynamic queue: {type, a, b, c}
@@ -110,7 +110,8 @@ struct MoeArgs {
     bf16* y;              // [T_max*k, H]
     float* partial;       // [kSplitMax, split_rows_cap, H]
     int mt_max, q_max, split_rows_cap, r_max;
-    int stages, num_ctas;
+    int wr_box;           // router-weight TMA box height (0: the weight is read in place)
+    int num_ctas;
     uint64_t* trace;      // optional per-task trace (see et_opts)
     int trace_cap;
     uint64_t timeout_ns;
@@ -124,7 +125,7 @@ struct SplitKArgs {
     EtHeader* hdr;
     int32_t* ev;          // [ceil(M_max/256) * N/128], self-resetting
     float* partial;       // [split, M_max, N]
-    int stages, num_ctas;
+    int num_ctas;
     uint64_t timeout_ns;
     int fault_mode, fault_arg;
 };
@@ -143,12 +144,9 @@ struct MlpArgs {
     int32_t* ev_y;        // [mt_max * H/128], self-resetting
     float* partial;       // [kSplitMax, B_max, H]
     int mt_max;
-    int stages, num_ctas;
+    int num_ctas;
     uint64_t timeout_ns;
     int fault_mode, fault_arg;
 };
-
-// Shared-memory geometry of one pipeline stage: [A0 16K][A1 16K][B nmax*128].
-__host__ __device__ constexpr int stage_bytes(int nmax) { return 2 * kABytes + nmax * 128; }
 
 }  // namespace et

@@ -12,15 +12,13 @@
 namespace et {
 cudaError_t launch_moe(const MoeArgs&, const CUtensorMap*, int, int, cudaStream_t);
 cudaError_t prepare_moe(int);
-int moe_stages();
 int moe_smem_bytes();
+int moe_ring_bytes();
 cudaError_t launch_splitk(const SplitKArgs&, const CUtensorMap*, int, int, cudaStream_t);
 cudaError_t prepare_splitk(int);
-int splitk_stages();
 int splitk_smem_bytes();
 cudaError_t launch_mlp(const MlpArgs&, const CUtensorMap*, int, int, cudaStream_t);
 cudaError_t prepare_mlp(int);
-int mlp_stages();
 int mlp_smem_bytes();
 }  // namespace et
 
@@ -111,6 +109,24 @@ int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uin
     return ET_OK;
 }
 
+// Row-major bf16 [rows, cols] without swizzle, box {box_cols, box_rows}
+// (box_cols * 2 a multiple of 16 bytes, cols * 2 too).
+int make_map_plain(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_cols, uint32_t box_rows, const char* what) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(ET_ERR_CUDA, std::string("cuTensorMapEncodeTiled failed for ") + what +
+                                     " (code " + std::to_string(static_cast<int>(r)) + ")");
+    return ET_OK;
+}
+
 uint64_t timeout_ns_of(const et_opts* o) {
     const uint32_t us = (o && o->timeout_us) ? o->timeout_us : 200000u;
     return static_cast<uint64_t>(us) * 1000ull;
@@ -176,6 +192,10 @@ bool moe_shape_ok(int T_max, int H, int F, int E, int k, std::string* why) {
     if (k < 1 || k > 8 || k > E) { *why = "k must be in [1, min(E, 8)]"; return false; }
     if (static_cast<long long>(E) * F >= (1ll << 31) || static_cast<long long>(E) * H >= (1ll << 31)) {
         *why = "E*F and E*H must fit in int32"; return false;
+    }
+    if (static_cast<long long>(k) * H * 2 > moe_ring_bytes()) {  // one token's k rows are staged at once
+        *why = "k*H*2 bytes must fit in the stage ring (" + std::to_string(moe_ring_bytes()) + ")";
+        return false;
     }
     return true;
 }
@@ -260,7 +280,6 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
 
     DeviceState* st = nullptr;
     if ((rc = device_state(&st, nullptr))) return rc;
-    const int stages = moe_stages();
     const int smem = moe_smem_bytes();
     if (!st->moe) {
         cudaError_t e = prepare_moe(smem);
@@ -306,7 +325,7 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
     a.q_max = L.q_max;
     a.split_rows_cap = L.split_cap;
     a.r_max = L.r_max;
-    a.stages = stages;
+    a.wr_box = E % 8 == 0 ? (H % 256 == 0 ? 256 : 128) : 0;
     a.num_ctas = st->sms;
     a.timeout_ns = timeout_ns_of(opts);
     a.fault_mode = opts ? opts->fault_mode : 0;
@@ -314,13 +333,18 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
     a.trace = (opts && opts->trace && opts->trace_cap) ? static_cast<uint64_t*>(opts->trace) : nullptr;
     a.trace_cap = opts ? static_cast<int>(opts->trace_cap) : 0;
 
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     const uint64_t EF = static_cast<uint64_t>(E) * F, EH = static_cast<uint64_t>(E) * H;
     if ((rc = make_map(&maps[0], w_gate, EF, H, kTileM, "w_gate"))) return rc;
     if ((rc = make_map(&maps[1], w_up, EF, H, kTileM, "w_up"))) return rc;
     if ((rc = make_map(&maps[2], w_down, EH, F, kTileM, "w_down"))) return rc;
     if ((rc = make_map(&maps[3], a.xp, L.Tk, H, kBBoxRows, "permuted x"))) return rc;
     if ((rc = make_map(&maps[4], a.h, L.Tk, F, kBBoxRows, "h"))) return rc;
+    if (a.wr_box) {
+        if ((rc = make_map_plain(&maps[5], w_router, H, E, 8, a.wr_box, "w_router"))) return rc;
+    } else {
+        maps[5] = maps[0];  // unused: the router weight is read in place
+    }
     cudaError_t e = launch_moe(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "launch of the MoE megakernel");
     return ET_OK;
@@ -352,7 +376,6 @@ int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t*
     if (!d_M && M == 0) return ET_OK;
     DeviceState* st = nullptr;
     if ((rc = device_state(&st, nullptr))) return rc;
-    const int stages = splitk_stages();
     const int smem = splitk_smem_bytes();
     if (!st->splitk) {
         cudaError_t e = prepare_splitk(smem);
@@ -371,7 +394,6 @@ int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t*
     a.hdr = reinterpret_cast<EtHeader*>(ws);
     a.ev = reinterpret_cast<int32_t*>(ws + L.ev);
     a.partial = reinterpret_cast<float*>(ws + L.partial);
-    a.stages = stages;
     a.num_ctas = st->sms;
     a.timeout_ns = timeout_ns_of(opts);
     a.fault_mode = opts ? opts->fault_mode : 0;
@@ -409,7 +431,6 @@ int et_mlp_chain(const void* x, const void* gamma, float eps, const void* w_gate
     if (!d_B && B == 0) return ET_OK;
     DeviceState* st = nullptr;
     if ((rc = device_state(&st, nullptr))) return rc;
-    const int stages = mlp_stages();
     const int smem = mlp_smem_bytes();
     if (!st->mlp) {
         cudaError_t e = prepare_mlp(smem);
@@ -434,7 +455,6 @@ int et_mlp_chain(const void* x, const void* gamma, float eps, const void* w_gate
     a.ev_y = reinterpret_cast<int32_t*>(ws + L.ev_y);
     a.partial = reinterpret_cast<float*>(ws + L.partial);
     a.mt_max = L.mt_max;
-    a.stages = stages;
     a.num_ctas = st->sms;
     a.timeout_ns = timeout_ns_of(opts);
     a.fault_mode = opts ? opts->fault_mode : 0;

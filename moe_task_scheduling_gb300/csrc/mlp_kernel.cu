@@ -23,8 +23,7 @@ namespace et {
 constexpr int kNormRows = 8;  // two rows per worker warp
 
 struct MlpPlan {
-    int B, NR, MT, FT, HT, S, n_gu, n_dn, total, nbuf;
-    uint32_t u_off;
+    int B, NR, MT, FT, HT, S, n_gu, n_dn, total;
 };
 
 struct MlpTile {
@@ -102,9 +101,9 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                  const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xhat,
                  const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ MlpArgs p) {
     extern __shared__ uint8_t smem_raw[];
-    Stages stg;
+    Ring ring;
     uint8_t* scratch;
-    Ctl* ctl = cta_setup(smem_raw, p.stages, kWideNMax, 0, stg, &scratch);
+    Ctl* ctl = cta_setup(smem_raw, 0, ring, &scratch);
     const WaitCtx wc{p.hdr, p.timeout_ns};
     const uint32_t tmem = ctl->tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -134,46 +133,42 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     P.n_gu = P.MT * P.FT;
     P.n_dn = P.MT * P.S * P.HT;
     P.total = P.NR + P.n_gu + P.n_dn;
-    // two accumulator buffers when both gate/up accumulators fit in 256 columns
-    P.nbuf = P.B <= kWideNMax / 2 ? 2 : 1;
-    P.u_off = P.nbuf == 2 ? kAccBufCols / 2 : kAccBufCols;
 
     auto gemm_of = [&](const MlpTile& t) {
         if (t.kind == 1)
             return GemmTask{&tm_wg, &tm_wu, &tm_xhat, t.ft * kTileM, t.mt * kWideNMax, 0,
-                            p.H / kBlockK, t.n, 1, &p.hdr->ev_norm, P.NR, kWhereNorm};
+                            p.H / kBlockK, t.n, &p.hdr->ev_norm, P.NR, kWhereNorm};
         const int fchunk = p.F / P.S;
         return GemmTask{&tm_wd, nullptr, &tm_h, t.ht * kTileM, t.mt * kWideNMax,
                         t.s * (fchunk / kBlockK), fchunk / kBlockK, t.n,
-                        t.n <= kWideNMax / 2 ? 2 : 1, &p.ev_h[t.mt * kSplitMax + t.s], P.FT / P.S,
-                        kWhereH};
+                        &p.ev_h[t.mt * kSplitMax + t.s], P.FT / P.S, kWhereH};
     };
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
-            uint32_t it = 0;
+            ProdState ps;
             for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
                 const MlpTile t = mlp_tile(P, task);
                 if (t.kind == 0) continue;
-                if (!produce_task(gemm_of(t), stg, ctl, it, wc, pol_w, pol_b)) break;
+                if (!produce_task(gemm_of(t), ring, ctl, ps, wc, pol_w, pol_b)) break;
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            uint32_t it = 0, g = 0;
+            MmaState ms;
             for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
                 const MlpTile t = mlp_tile(P, task);
                 if (t.kind == 0) continue;
-                if (!mma_task(gemm_of(t), stg, ctl, it, g, P.nbuf, P.u_off, tmem, wc)) break;
+                if (!mma_task(gemm_of(t), ring, ctl, ms, tmem, wc)) break;
             }
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
         const int q = warp - kEpiWarp0, wtid = threadIdx.x - kEpiWarp0 * 32;
         const int H = p.H, F = p.F;
-        uint32_t g = 0, wseq = 0;
+        EpiState es;
         for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
             const MlpTile t = mlp_tile(P, task);
             if (t.kind == 0) {
@@ -186,16 +181,18 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 }
                 continue;
             }
-            uint32_t acc;
-            if (!epi_acquire(ctl, g, P.nbuf, tmem, wc, acc, wseq)) break;
-            const uint32_t lane_base = acc + (static_cast<uint32_t>(q * 32) << 16);
+            const bool two = t.kind == 1;
+            uint32_t acc, acc1;
+            if (!epi_acquire(ctl, es, two, t.n, tmem, wc, acc, acc1)) break;
+            const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+            const uint32_t lane_base = acc + lane_off;
             const size_t m0 = static_cast<size_t>(t.mt) * kWideNMax;
             if (t.kind == 1) {
                 const int f = t.ft * kTileM + q * 32 + lane;
                 for (int c0 = 0; c0 < t.n; c0 += 16) {
                     float gv[16], uv[16];
                     tmem_ld16(lane_base + c0, gv);
-                    tmem_ld16(lane_base + P.u_off + c0, uv);
+                    tmem_ld16(acc1 + lane_off + c0, uv);
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
@@ -203,8 +200,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                             p.h[(m0 + c0 + c) * F + f] =
                                 __float2bfloat16_rn(gv[c] / (1.0f + __expf(-gv[c])) * uv[c]);
                 }
-                epi_release(ctl, g, P.nbuf);
-                ++g;
+                epi_release(ctl, es, true, t.n);
                 fence_proxy_async_global();  // h is read back by TMA
                 worker_sync();
                 if (wtid == 0) {
@@ -230,8 +226,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                         p.partial[(static_cast<size_t>(t.s) * p.B_max + m) * H + hh] = v[c];
                 }
             }
-            epi_release(ctl, g, P.nbuf);
-            ++g;
+            epi_release(ctl, es, false, t.n);
             if (P.S > 1) {
                 int* ev = p.ev_y + t.mt * P.HT + t.ht;
                 worker_sync();
@@ -256,7 +251,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     }
 
     const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
-    cta_teardown(ctl, stg, aborted_run);
+    cta_teardown(ctl, aborted_run);
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -280,8 +275,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     }
 }
 
-int mlp_smem_bytes() { return smem_bytes_for(stages_for(kWideNMax, 0), kWideNMax, 0); }
-int mlp_stages() { return stages_for(kWideNMax, 0); }
+int mlp_smem_bytes() { return smem_bytes_for(0); }
 
 cudaError_t launch_mlp(const MlpArgs& a, const CUtensorMap* maps, int grid, int smem,
                        cudaStream_t stream) {

@@ -82,39 +82,45 @@ __device__ __forceinline__ void load_w(const bf16* wrow, float (&w)[EBW]) {
 }
 
 // Fixed-order logits of nt (<= 16) tokens x `ec` experts (global experts
-// e0 .. e0+ec).  A job is 8 tokens x EBW experts; lane l of the job's warp
-// owns partial sum l and accumulates h = l, l+32, ... in ascending order with
-// fp32 fma (exact bf16 products, so fma == mul+add); the halving shuffle tree
-// (16, 8, 4, 2, 1) then adds p[l] + p[l+off].  xb: token rows (stride H);
-// wb: weight rows (stride ws) whose column 0 is expert e0.  Logit (t, e0+j)
-// goes to out[t * out_stride + out_e0 + j].
+// e0 .. e0+ec).  A job is 4 tokens x EBW experts on one warp: lane l owns
+// partial sum l and accumulates h = l, l+32, ... in ascending order with fp32
+// fma (a bf16 x bf16 product is exact in fp32, so fma == mul + add); the
+// halving shuffle tree (16, 8, 4, 2, 1) then adds p[l] + p[l + off].
+// Token rows: xb + t * H.  Weight element (h, j) of chunk column j sits at
+//   wb + ((o + j) >> 3) * blk + h * rs + ((o + j) & 7)
+// which covers the [H, E] layout in global memory (o = 0, blk = 8, rs = E)
+// and the staged one (blocks of 8 experts, 16 bytes a row).  EBW divides
+// both ec and 8, so a job's EBW columns never straddle a block.  Logit
+// (t, e0 + j) goes to out[t * E + e0 + j].
 template <int EBW>
 __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, const bf16* wb,
-                                              int ws, int nt, int e0, int ec, float* out,
-                                              int out_stride, int out_e0) {
-    const int H = p.H;
+                                              int o, int rs, int blk, int nt, int e0, int ec,
+                                              float* out) {
+    const int H = p.H, E = p.E;
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
-    const int neb = ec / EBW, ntb = ceil_div(nt, 8);
-    constexpr int U = 4;  // h-steps whose weights are loaded ahead of their fmas
+    constexpr int TB = 4;  // tokens per job
+    constexpr int U = 4;   // h-steps whose weights are loaded ahead of their fmas
+    const int neb = ec / EBW, ntb = ceil_div(nt, TB);
     for (int job = warp; job < neb * ntb; job += kWorkers / 32) {
-        const int tb = job / neb, eb = (job % neb) * EBW;
-        const int tn = min(8, nt - tb * 8);
-        float acc[8][EBW];
+        const int tb = job / neb, j0 = (job % neb) * EBW;
+        const int tn = min(TB, nt - tb * TB);
+        float acc[TB][EBW];
 #pragma unroll
-        for (int a = 0; a < 8; ++a)
+        for (int a = 0; a < TB; ++a)
 #pragma unroll
             for (int b = 0; b < EBW; ++b) acc[a][b] = 0.0f;
-        const bf16* xr = xb + static_cast<size_t>(tb * 8) * H;
+        const bf16* xr = xb + static_cast<size_t>(tb * TB) * H;
+        const bf16* wj = wb + static_cast<size_t>((o + j0) >> 3) * blk + ((o + j0) & 7);
         for (int h0 = 0; h0 < H; h0 += 32 * U) {  // H is a multiple of 128
             float wv[U][EBW];
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                load_w<EBW>(wb + static_cast<size_t>(h0 + 32 * u + lane) * ws + eb, wv[u]);
+                load_w<EBW>(wj + static_cast<size_t>(h0 + 32 * u + lane) * rs, wv[u]);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int h = h0 + 32 * u + lane;
 #pragma unroll
-                for (int a = 0; a < 8; ++a) {
+                for (int a = 0; a < TB; ++a) {
                     const float xv = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
 #pragma unroll
                     for (int b = 0; b < EBW; ++b) acc[a][b] = fmaf(xv, wv[u][b], acc[a][b]);
@@ -124,7 +130,7 @@ __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, 
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1)
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
+            for (int a = 0; a < TB; ++a)
 #pragma unroll
                 for (int b = 0; b < EBW; ++b)
                     acc[a][b] = acc[a][b] + __shfl_down_sync(0xffffffffu, acc[a][b], off);
@@ -133,77 +139,34 @@ __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, 
 #pragma unroll
                 for (int b = 0; b < EBW; ++b) {
                     float L = acc[a][b];
-                    if (p.bias) L = L + p.bias[e0 + eb + b];
-                    out[(tb * 8 + a) * out_stride + out_e0 + eb + b] = L;
+                    if (p.bias) L = L + p.bias[e0 + j0 + b];
+                    out[(tb * TB + a) * E + e0 + j0 + b] = L;
                 }
         }
     }
 }
 
-// Flat copy of `bytes` (multiple of 16, 16-byte aligned ends) by the worker
-// group into shared memory, several 16-byte loads in flight per thread.
-__device__ __forceinline__ void worker_copy_flat(uint8_t* dst, const uint8_t* src, size_t bytes) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-    uint4* d = reinterpret_cast<uint4*>(dst);
-    const int n = static_cast<int>(bytes / 16);
-    constexpr int U = 8;
-    for (int i = wtid_(); i < n; i += kWorkers * U) {
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (i + u * kWorkers < n) v[u] = __ldcg(s + i + u * kWorkers);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (i + u * kWorkers < n) d[i + u * kWorkers] = v[u];
-    }
+// Router-weight staging geometry: 8-expert column blocks, rows padded to the
+// TMA box height.
+__device__ __forceinline__ int wr_rows_pad(int H, int box) { return (H + box - 1) / box * box; }
+
+// 8-expert blocks a chunk of ec experts spans (0: the chunk cannot be staged).
+__device__ __forceinline__ int wr_blocks(int ec) {
+    return ec % 8 == 0 ? ec / 8 : (8 % ec == 0 ? 1 : 0);
 }
 
-// Columns [e0, e0 + ec) of the router weight [H, E] into contiguous
-// shared memory [H][ec], with the widest element the alignment allows.
-template <class V>
-__device__ __forceinline__ void copy_cols_t(uint8_t* dst, const bf16* wr, int H, int E, int e0,
-                                            int ec) {
-    const int per_row = ec * 2 / static_cast<int>(sizeof(V));
-    const int n = H * per_row;
-    constexpr int U = 4;
-    for (int i = wtid_(); i < n; i += kWorkers * U) {
-        V v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = i + u * kWorkers;
-            if (j < n) {
-                const int h = j / per_row, q = j - h * per_row;
-                v[u] = *(reinterpret_cast<const V*>(wr + static_cast<size_t>(h) * E + e0) + q);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = i + u * kWorkers;
-            if (j < n) reinterpret_cast<V*>(dst)[j] = v[u];
-        }
-    }
-}
-
-__device__ __forceinline__ void copy_cols(uint8_t* dst, const bf16* wr, int H, int E, int e0, int ec) {
-    const int bytes = ec * 2, off = e0 * 2, stride = E * 2;
-    if ((bytes | off | stride) % 16 == 0)
-        copy_cols_t<uint4>(dst, wr, H, E, e0, ec);
-    else if ((bytes | off | stride) % 4 == 0)
-        copy_cols_t<uint32_t>(dst, wr, H, E, e0, ec);
-    else
-        copy_cols_t<unsigned short>(dst, wr, H, E, e0, ec);
-}
-
-// The per-call plan: a pure function of the device token count, E, k and the
-// grid, so every CTA and every role derives the same task numbering.
+// The per-call plan: a pure function of the device token count, the shapes
+// and the grid, so every CTA and every role derives the same task numbering.
 struct MoePlan {
     int T, R;      // tokens; router tiles of kRouterTile tokens
     int C, EC;     // router expert chunks per tile, experts per chunk
     int Q;         // permute parts per router tile
     int CT, NC;    // tokens per combine task; combine tasks
+    bool stage;    // router tiles stage x and their weight chunk in the ring
 };
 
-__device__ __forceinline__ MoePlan moe_plan(int T, int E, int k, int G) {
+__device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint32_t ring_bytes) {
+    const int E = p.E, k = p.k, H = p.H;
     MoePlan P;
     P.T = T;
     P.R = ceil_div(T, kRouterTile);
@@ -213,6 +176,21 @@ __device__ __forceinline__ MoePlan moe_plan(int T, int E, int k, int G) {
     P.C = 1;
     for (int d = 2; d <= E / 2; ++d)
         if (E % d == 0 && d <= want) P.C = d;
+    // Staging: the smallest chunking (at least the one above) whose weight
+    // blocks fit in the ring next to a full token tile.
+    P.stage = false;
+    if (p.wr_box > 0) {
+        const uint32_t xpad = (static_cast<uint32_t>(min(T, kRouterTile) * H * 2) + 1023u) & ~1023u;
+        const uint32_t hp = static_cast<uint32_t>(wr_rows_pad(H, p.wr_box));
+        for (int d = P.C; d <= E && !P.stage; ++d) {
+            if (E % d) continue;
+            const int nb = wr_blocks(E / d);
+            if (nb > 0 && xpad + static_cast<uint32_t>(nb) * hp * 16u <= ring_bytes) {
+                P.C = d;
+                P.stage = true;
+            }
+        }
+    }
     P.EC = E / P.C;
     P.Q = P.R > 0 ? min(max(1, G / P.R), kRouterTile * k) : 1;
     P.CT = min(kCombineTile, max(1, ceil_div(T, G)));
@@ -220,42 +198,59 @@ __device__ __forceinline__ MoePlan moe_plan(int T, int E, int k, int G) {
     return P;
 }
 
-// Logits of router tile r for expert chunk c.  The token rows and the chunk's
-// router-weight columns are staged into the stage ring first (no GEMM task is
-// published before the scan, which waits for every router tile, so the ring
-// is idle while any router task runs).  With several chunks the logits go to
-// a global buffer and the chunk that brings the tile's counter to C does the
-// top-k for the whole tile -- the same event-counter reduction as split-K.
-__device__ __forceinline__ void router_task(const MoeArgs& p, const MoePlan& P, int r, int c,
-                                            uint8_t* smem, uint8_t* ring, size_t ring_bytes,
-                                            Ctl* ctl) {
+// Logits of router tile r for expert chunk c.  With staging, the token rows
+// (one bulk copy) and the chunk's 8-expert weight blocks (TMA boxes) are
+// copied into the ring, which the workers hold on lease for the task.  With
+// several chunks the logits go to a global buffer and the chunk that brings
+// the tile's counter to C does the top-k for the whole tile -- the same
+// event-counter reduction as split-K.
+__device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, int r, int c,
+                                            uint8_t* smem, const Ring& ring, Ctl* ctl,
+                                            const CUtensorMap* tm_wr, const WaitCtx& wc,
+                                            uint32_t& sphase, uint32_t& seq) {
     const int E = p.E, H = p.H, k = p.k;
-    float* lg = reinterpret_cast<float*>(smem);                                // [16][E]
+    float* lg = reinterpret_cast<float*>(smem);                                  // [16][E]
     int* hs = reinterpret_cast<int*>(smem + kRouterTile * 256 * sizeof(float));  // [E]
     const int t0 = r * kRouterTile, nt = min(kRouterTile, P.T - t0);
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
     const int e0 = c * P.EC, ec = P.EC;
-    const size_t xbytes = static_cast<size_t>(nt) * H * 2;
-    const size_t wbytes = static_cast<size_t>(H) * ec * 2;
-    const bool x_in = xbytes <= ring_bytes;
-    const bool w_in = x_in && xbytes + wbytes <= ring_bytes;
-    if (x_in)
-        worker_copy_flat(ring, reinterpret_cast<const uint8_t*>(p.x + static_cast<size_t>(t0) * H),
-                         xbytes);
-    if (w_in) copy_cols(ring + xbytes, p.wr, H, E, e0, ec);
-    worker_sync();
-    const bf16* xb = x_in ? reinterpret_cast<const bf16*>(ring) : p.x + static_cast<size_t>(t0) * H;
-    const bf16* wb = w_in ? reinterpret_cast<const bf16*>(ring + xbytes) : p.wr + e0;
-    const int ws = w_in ? ec : E;
+    const bf16* xb = p.x + static_cast<size_t>(t0) * H;
+    const bf16* wb = p.wr + e0;
+    int o = 0, rs = E, blk = 8;
+    if (P.stage) {
+        const uint32_t xbytes = static_cast<uint32_t>(nt * H * 2);
+        const uint32_t xpad = (xbytes + 1023u) & ~1023u;
+        const int box = p.wr_box, hp = wr_rows_pad(H, box);
+        const int eb0 = e0 >> 3, nb = ((e0 + ec + 7) >> 3) - eb0;
+        uint8_t* wdst = ring.base + xpad;
+        if (wtid_() == 0) {
+            mbar_arrive_expect_tx(&ctl->sbar, xbytes + static_cast<uint32_t>(nb * hp * 16));
+            bulk_g2s(ring.base, xb, xbytes, &ctl->sbar);
+            const uint64_t pol = policy_evict_last();
+            for (int b = 0; b < nb; ++b)
+                for (int h0 = 0; h0 < hp; h0 += box)
+                    tma_load_2d(wdst + static_cast<size_t>(b * hp + h0) * 16, tm_wr, &ctl->sbar,
+                                (eb0 + b) * 8, h0, pol);
+        }
+        if (!staging_wait(ctl, sphase, wc, seq)) return false;
+        xb = reinterpret_cast<const bf16*>(ring.base);
+        wb = reinterpret_cast<const bf16*>(wdst);
+        o = e0 & 7;
+        rs = 8;
+        blk = hp * 8;
+    }
     float* out = P.C == 1 ? lg : p.logits + static_cast<size_t>(t0) * E;
-    // widest expert block (at most 4: registers) that still gives every worker warp a job
-    const int ntb = ceil_div(nt, 8), warps = kWorkers / 32;
-    if (ec % 4 == 0 && ntb * (ec / 4) >= warps)
-        router_logits<4>(p, xb, wb, ws, nt, e0, ec, out, E, e0);
-    else if (ec % 2 == 0)
-        router_logits<2>(p, xb, wb, ws, nt, e0, ec, out, E, e0);
+    // the widest expert block (<= 8) that divides the chunk (and E when the
+    // weight is read in place, for aligned vector loads)
+    const int ew = P.stage ? ec : (ec | E);
+    if (ew % 8 == 0)
+        router_logits<8>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    else if (ew % 4 == 0)
+        router_logits<4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    else if (ew % 2 == 0)
+        router_logits<2>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
     else
-        router_logits<1>(p, xb, wb, ws, nt, e0, ec, out, E, e0);
+        router_logits<1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
     worker_sync();
     if (P.C > 1) {  // tile reduction through the tile's event counter
         if (wtid_() == 0) {
@@ -263,7 +258,7 @@ __device__ __forceinline__ void router_task(const MoeArgs& p, const MoePlan& P, 
             ctl->flag = (atom_acq_rel_add(p.ev_tile + r, 1) == P.C - 1) ? 1 : 0;
         }
         worker_sync();
-        if (!ctl->flag) return;  // another chunk of this tile finishes it
+        if (!ctl->flag) return true;  // another chunk of this tile finishes it
         if (wtid_() == 0) p.ev_tile[r] = 0;  // every chunk arrived: reset for the next call
         for (int i = wtid_(); i < nt * E; i += kWorkers)
             lg[i] = __ldcg(p.logits + static_cast<size_t>(t0) * E + i);
@@ -337,6 +332,7 @@ __device__ __forceinline__ void router_task(const MoeArgs& p, const MoePlan& P, 
         __threadfence();
         red_release_add(&p.hdr->ev_router, 1);
     }
+    return true;
 }
 
 // ------------------------------------------------------------------ SCAN
@@ -344,9 +340,10 @@ __device__ __forceinline__ void router_task(const MoeArgs& p, const MoePlan& P, 
 // Counts, offsets, expert row tiles, split choice, and the task queue.  The
 // targets the later waits use (R permute tiles; F-tiles per chunk; the total
 // number of output tiles) are all derived here, on the device, from the
-// routing of this very call.
-__device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, uint8_t* smem, Ctl* ctl,
-                                       const WaitCtx& wc) {
+// routing of this very call.  The per-tile histograms are staged in the ring
+// (many loads in flight) and scanned per expert there.
+__device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, uint8_t* smem,
+                                          const Ring& ring, Ctl* ctl, const WaitCtx& wc) {
     const int E = p.E, k = p.k, R = P.R, T = P.T;
     if (wtid_() == 0) ctl->flag = ev_wait_geq(wc, &p.hdr->ev_router, R, kWhereRouter) ? 1 : 0;
     worker_sync();
@@ -355,14 +352,44 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     int* off_s = cnt_s + 256;                   // [257]
     int* n_s = off_s + 264;                     // [256]
     int* mtb_s = n_s + 256;                     // [257]
-    for (int e = wtid_(); e < E; e += kWorkers) {
-        int run = 0;
-        for (int r = 0; r < R; ++r) {
-            const int c = __ldcg(p.hist + static_cast<size_t>(r) * E + e);
-            p.base[static_cast<size_t>(r) * E + e] = run;
-            run += c;
+    const int RE = R * E;
+    const bool staged = static_cast<size_t>(RE) * 4 <= ring.bytes;
+    int* hs = reinterpret_cast<int*>(ring.base);
+    if (staged) {
+        const int n4 = RE / 4;
+        const int4* src = reinterpret_cast<const int4*>(p.hist);
+        int4* dst = reinterpret_cast<int4*>(hs);
+        constexpr int U = 8;
+        for (int i = wtid_(); i < n4; i += kWorkers * U) {
+            int4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (i + u * kWorkers < n4) v[u] = __ldcg(src + i + u * kWorkers);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (i + u * kWorkers < n4) dst[i + u * kWorkers] = v[u];
         }
-        cnt_s[e] = run;
+        for (int i = n4 * 4 + wtid_(); i < RE; i += kWorkers) hs[i] = __ldcg(p.hist + i);
+        worker_sync();
+        for (int e = wtid_(); e < E; e += kWorkers) {
+            int run = 0;
+            for (int r = 0; r < R; ++r) {
+                const int c = hs[r * E + e];
+                hs[r * E + e] = run;
+                run += c;
+            }
+            cnt_s[e] = run;
+        }
+    } else {
+        for (int e = wtid_(); e < E; e += kWorkers) {
+            int run = 0;
+            for (int r = 0; r < R; ++r) {
+                const int c = __ldcg(p.hist + static_cast<size_t>(r) * E + e);
+                p.base[static_cast<size_t>(r) * E + e] = run;
+                run += c;
+            }
+            cnt_s[e] = run;
+        }
     }
     worker_sync();
     const int FT = p.F / kTileM, HT = p.H / kTileM;
@@ -397,7 +424,6 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         p.cnt[e] = cnt_s[e];
         p.off[e] = off_s[e];
         if (e == E - 1) p.off[E] = off_s[E];
-        for (int r = 0; r < R; ++r) p.base[static_cast<size_t>(r) * E + e] += off_s[e];
         const int n = n_s[e];
         for (int g = mtb_s[e], mt = 0; g < mtb_s[e + 1]; ++g, ++mt) {
             p.g_expert[g] = e;
@@ -405,6 +431,11 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
             p.g_rows[g] = min(n, cnt_s[e] - mt * n);
             p.g_n[g] = n;
         }
+    }
+    if (staged) {
+        for (int i = wtid_(); i < RE; i += kWorkers) p.base[i] = hs[i] + off_s[i % E];
+    } else {
+        for (int i = wtid_(); i < RE; i += kWorkers) p.base[i] += off_s[i % E];
     }
     const int n_perm = R * P.Q, n_gu = total_mt * FT, n_dn = total_mt * S * HT, n_cb = P.NC;
     const int total = n_perm + n_gu + n_dn + n_cb;
@@ -442,14 +473,27 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
 // ------------------------------------------------------------------ PERMUTE
 
 // Stable dispatch of router tile r: row (t, j) goes to off[e] + (rank of t
-// among this call's tokens routed to e), and its x row is copied there.
-__device__ __forceinline__ void permute_task(const MoeArgs& p, const MoePlan& P, int r, int part,
-                                             uint8_t* smem) {
+// among this call's tokens routed to e), and its x row is copied there.  The
+// part's token rows come into the ring by bulk copy (the first batch is
+// issued before the ranks are computed, so it flies meanwhile); each routed
+// row then leaves with one bulk shared -> global copy.
+__device__ __forceinline__ bool permute_task(const MoeArgs& p, const MoePlan& P, int r, int part,
+                                             uint8_t* smem, const Ring& ring, Ctl* ctl,
+                                             const WaitCtx& wc, uint32_t& sphase, uint32_t& seq) {
     const int k = p.k, E = p.E, H = p.H;
     const int t0 = r * kRouterTile, nt = min(kRouterTile, P.T - t0), nent = nt * k;
     const int i0 = part * nent / P.Q, i1 = (part + 1) * nent / P.Q;  // this part's entries
     int* ie = reinterpret_cast<int*>(smem);  // [128]
     int* slot = ie + 128;                    // [128]
+    const int tl0 = i0 / k, ntok = i1 > i0 ? (i1 - 1) / k - tl0 + 1 : 0;
+    const uint32_t rowb = static_cast<uint32_t>(H) * 2u;
+    const int per = static_cast<int>(ring.bytes / rowb);  // token rows per batch (>= k)
+    auto issue = [&](int c0) {  // worker thread 0: token rows tl0 + c0 .. of the part
+        const int nc = min(per, ntok - c0);
+        mbar_arrive_expect_tx(&ctl->sbar, nc * rowb);
+        bulk_g2s(ring.base, p.x + static_cast<size_t>(t0 + tl0 + c0) * H, nc * rowb, &ctl->sbar);
+    };
+    if (ntok > 0 && wtid_() == 0) issue(0);
     for (int i = wtid_(); i < nent; i += kWorkers)
         ie[i] = __ldcg(p.idx + static_cast<size_t>(t0) * k + i);
     worker_sync();
@@ -462,40 +506,33 @@ __device__ __forceinline__ void permute_task(const MoeArgs& p, const MoePlan& P,
         p.pos[static_cast<size_t>(t0) * k + i] = pp;
         slot[i] = pp;
     }
-    worker_sync();
-    const int vpr = H / 8, nvec = (i1 - i0) * vpr;
-    constexpr int U = 8;  // 16-byte row segments in flight per thread
-    for (int v0 = wtid_(); v0 < nvec; v0 += kWorkers * U) {
-        uint4 val[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int v = v0 + u * kWorkers;
-            if (v < nvec) {
-                const int i = i0 + v / vpr, c = v % vpr;
-                val[u] = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t0 + i / k) * H) + c);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int v = v0 + u * kWorkers;
-            if (v < nvec) {
-                const int i = i0 + v / vpr, c = v % vpr;
-                reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(slot[i]) * H)[c] = val[u];
-            }
-        }
+    for (int c0 = 0; c0 < ntok; c0 += per) {
+        if (c0 > 0 && wtid_() == 0) issue(c0);
+        if (!staging_wait(ctl, sphase, wc, seq)) return false;
+        const int ia = max(i0, (tl0 + c0) * k), ib = min(i1, (tl0 + c0 + per) * k);
+        for (int i = ia + wtid_(); i < ib; i += kWorkers)
+            bulk_s2g(p.xp + static_cast<size_t>(slot[i]) * H, ring.base + (i / k - tl0 - c0) * rowb,
+                     rowb);
+        bulk_commit_wait_all();  // rows written (and the batch read) before the next one
+        worker_sync();
     }
-    fence_proxy_async_global();
+    if (ntok > 0) fence_proxy_async_global();  // the rows are read back by TMA
     worker_sync();
     if (wtid_() == 0) {
         __threadfence();
         red_release_add(&p.hdr->ev_perm, 1);
     }
+    return true;
 }
 
 // ------------------------------------------------------------------ COMBINE
 
-__device__ __forceinline__ bool combine_task(const MoeArgs& p, const MoePlan& P, int c, uint8_t* smem, Ctl* ctl,
-                                          const WaitCtx& wc) {
+// out[t] = bf16(sum_j w[t, j] * y[pos(t, j)]) in slot order.  The k expert
+// output rows of a batch of tokens are gathered into the ring with bulk
+// copies (as many tokens as fit), then summed from shared memory.
+__device__ __forceinline__ bool combine_task(const MoeArgs& p, const MoePlan& P, int c,
+                                             uint8_t* smem, const Ring& ring, Ctl* ctl,
+                                             const WaitCtx& wc, uint32_t& sphase, uint32_t& seq) {
     const int H = p.H, k = p.k;
     if (wtid_() == 0) {
         const int target = ld_relaxed(&p.hdr->total_mt) * (H / kTileM);
@@ -503,54 +540,43 @@ __device__ __forceinline__ bool combine_task(const MoeArgs& p, const MoePlan& P,
     }
     worker_sync();
     if (!ctl->flag) return false;
+    fence_proxy_async_global();  // y rows written by other CTAs' generic stores
     const int t0 = c * P.CT, nt = min(P.CT, P.T - t0), vpr = H / 8;
-    float* w_s = reinterpret_cast<float*>(smem);           // [16 * k]
+    const uint32_t rowb = static_cast<uint32_t>(H) * 2u;
+    float* w_s = reinterpret_cast<float*>(smem);                   // [16 * k]
     int* pos_s = reinterpret_cast<int*>(smem) + kCombineTile * 8;  // [16 * k]
     for (int i = wtid_(); i < nt * k; i += kWorkers) {
         w_s[i] = __ldcg(p.gw + static_cast<size_t>(t0) * k + i);
         pos_s[i] = __ldcg(p.pos + static_cast<size_t>(t0) * k + i);
     }
+    const int per = static_cast<int>(ring.bytes / (static_cast<uint32_t>(k) * rowb));
+    if (wtid_() == 0 && nt > 0) mbar_arrive_expect_tx(&ctl->sbar, min(per, nt) * k * rowb);
     worker_sync();
-    constexpr int U = 4;  // output segments per thread and pass (U loads in flight per j)
-    const int nvec = nt * vpr;
-    for (int v0 = wtid_(); v0 < nvec; v0 += kWorkers * U) {
-        float acc[U][8];
+    for (int b0 = 0; b0 < nt; b0 += per) {
+        const int nb = min(per, nt - b0);
+        for (int q = wtid_(); q < nb * k; q += kWorkers)
+            bulk_g2s(ring.base + q * rowb, p.y + static_cast<size_t>(pos_s[b0 * k + q]) * H, rowb,
+                     &ctl->sbar);
+        if (!staging_wait(ctl, sphase, wc, seq)) return false;
+        for (int v = wtid_(); v < nb * vpr; v += kWorkers) {
+            const int tt = v / vpr, cc = v % vpr;
+            float acc[8];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            for (int j = 0; j < k; ++j) {  // fp32 sum in slot order j = 0 .. k-1
+                const float wj = w_s[(b0 + tt) * k + j];
+                float yv[8];
+                unpack8(reinterpret_cast<const uint4*>(ring.base + (tt * k + j) * rowb)[cc], yv);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-        for (int j = 0; j < k; ++j) {  // fp32 sum in slot order j = 0 .. k-1
-            uint4 ys[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * kWorkers;
-                if (v < nvec) {
-                    const int tt = v / vpr, cc = v % vpr;
-                    ys[u] = __ldcg(reinterpret_cast<const uint4*>(
-                                       p.y + static_cast<size_t>(pos_s[tt * k + j]) * H) + cc);
-                }
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, yv[i], acc[i]);
             }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * kWorkers;
-                if (v < nvec) {
-                    const float wj = w_s[(v / vpr) * k + j];
-                    float yv[8];
-                    unpack8(ys[u], yv);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(wj, yv[i], acc[u][i]);
-                }
-            }
+            reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t0 + b0 + tt) * H)[cc] = pack8(acc);
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int v = v0 + u * kWorkers;
-            if (v < nvec)
-                reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t0 + v / vpr) * H)[v % vpr] =
-                    pack8(acc[u]);
-        }
+        worker_sync();  // the batch is consumed before the ring is refilled
+        if (wtid_() == 0 && b0 + per < nt)
+            mbar_arrive_expect_tx(&ctl->sbar, min(per, nt - b0 - per) * k * rowb);
+        worker_sync();
     }
-    worker_sync();
     return true;
 }
 
@@ -626,12 +652,13 @@ __device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc,
 __global__ void __launch_bounds__(kThreads, 1)
 moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xp,
-               const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ MoeArgs p) {
+               const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wr,
+               const __grid_constant__ MoeArgs p) {
     extern __shared__ uint8_t smem_raw[];
     const uint64_t t_start = globaltimer_ns();
-    Stages stg;
+    Ring ring;
     uint8_t* scratch;
-    Ctl* ctl = cta_setup(smem_raw, p.stages, kMoeNMax, kMoeScratch, stg, &scratch);
+    Ctl* ctl = cta_setup(smem_raw, kMoeScratch, ring, &scratch);
     const WaitCtx wc{p.hdr, p.timeout_ns};
     const uint32_t tmem = ctl->tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -643,24 +670,24 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereBoundsT);
         T = 0;
     }
-    const MoePlan P = moe_plan(T, p.E, p.k, static_cast<int>(gridDim.x));
+    const MoePlan P = moe_plan(p, T, static_cast<int>(gridDim.x), ring.bytes);
     const int FT = p.F / kTileM, HT = p.H / kTileM;
 
     auto gemm_of = [&](const TaskMsg& m) {
         const int type = m.type & 0xff, S = m.type >> 8;
         if (type == kTaskGateUp)
             return GemmTask{&tm_wg, &tm_wu, &tm_xp, m.e * p.F + m.b * kTileM, m.row0, 0,
-                            p.H / kBlockK, m.n, 1, &p.hdr->ev_perm, P.R * P.Q, kWherePerm};
+                            p.H / kBlockK, m.n, &p.hdr->ev_perm, P.R * P.Q, kWherePerm};
         const int fchunk = p.F / S;
         return GemmTask{&tm_wd, nullptr, &tm_h, m.e * p.H + m.c * kTileM, m.row0,
-                        m.b * (fchunk / kBlockK), fchunk / kBlockK, m.n, m.n <= 64 ? 2 : 1,
+                        m.b * (fchunk / kBlockK), fchunk / kBlockK, m.n,
                         &p.ev_h[m.a * kSplitMax + m.b], FT / S, kWhereH};
     };
 
     if (warp == 0) {
         if (lane == 0) {  // producer: pop, hand over, load
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
-            uint32_t it = 0;
+            ProdState ps;
             for (int i = 0;; ++i) {
                 const uint64_t tp = globaltimer_ns();
                 const TaskMsg m = pop_task(p, wc, P);
@@ -671,15 +698,18 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 mbar_arrive(&ctl->tq_full[slot]);
                 const int type = m.type & 0xff;
                 if (type == kTaskExit) break;
-                if (type == kTaskGateUp || type == kTaskDown)
-                    if (!produce_task(gemm_of(m), stg, ctl, it, wc, pol_w, pol_b)) break;
+                if (type == kTaskGateUp || type == kTaskDown) {
+                    if (!produce_task(gemm_of(m), ring, ctl, ps, wc, pol_w, pol_b)) break;
+                } else {
+                    ++ps.leases;  // a SIMT task holds the ring until the workers return it
+                }
                 trace_rec(p, type, 0, m.a, m.b, tp, globaltimer_ns());
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {  // MMA issuer
-            uint32_t it = 0, g = 0;
+            MmaState ms;
             for (int i = 0;; ++i) {
                 const int slot = i % kTaskRing;
                 if (!mbar_wait(wc, &ctl->tq_full[slot], (i / kTaskRing) & 1, kWhereQueue)) break;
@@ -688,17 +718,18 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 const int type = m.type & 0xff;
                 if (type == kTaskExit) break;
                 if (type == kTaskGateUp || type == kTaskDown)
-                    if (!mma_task(gemm_of(m), stg, ctl, it, g, 2, kAccBufCols / 2, tmem, wc)) break;
+                    if (!mma_task(gemm_of(m), ring, ctl, ms, tmem, wc)) break;
             }
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {  // workers: epilogues and SIMT tasks
         const int q = warp - kEpiWarp0, wtid = wtid_();
         const int H = p.H, F = p.F;
-        uint32_t g = 0, wseq = 0;
+        EpiState es;
+        uint32_t sphase = 0;
         for (int i = 0;; ++i) {
             const int slot = i % kTaskRing;
-            if (!worker_wait(ctl, &ctl->tq_full[slot], (i / kTaskRing) & 1, wc, kWhereQueue, wseq))
+            if (!worker_wait(ctl, &ctl->tq_full[slot], (i / kTaskRing) & 1, wc, kWhereQueue, es.seq))
                 break;
             const TaskMsg m = ctl->tq[slot];
             __syncwarp();
@@ -707,25 +738,25 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             if (type == kTaskExit) break;
             TraceScope trace_scope{p, type, m.a, m.b, p.trace ? globaltimer_ns() : 0ull,
                                    p.trace != nullptr && wtid == 0};
-            if (type == kTaskRouter) {
-                router_task(p, P, m.a, m.b, scratch, stg.base, static_cast<size_t>(stg.n) * stg.bytes, ctl);
+            if (type != kTaskGateUp && type != kTaskDown) {  // SIMT task on the leased ring
+                bool ok;
+                if (type == kTaskRouter)
+                    ok = router_task(p, P, m.a, m.b, scratch, ring, ctl, &tm_wr, wc, sphase, es.seq);
+                else if (type == kTaskScan)
+                    ok = scan_task(p, P, scratch, ring, ctl, wc);
+                else if (type == kTaskPermute)
+                    ok = permute_task(p, P, m.a, m.b, scratch, ring, ctl, wc, sphase, es.seq);
+                else
+                    ok = combine_task(p, P, m.a, scratch, ring, ctl, wc, sphase, es.seq);
+                if (!ok) break;
+                ring_return(ctl);
                 continue;
             }
-            if (type == kTaskScan) {
-                if (!scan_task(p, P, scratch, ctl, wc)) break;
-                continue;
-            }
-            if (type == kTaskPermute) {
-                permute_task(p, P, m.a, m.b, scratch);
-                continue;
-            }
-            if (type == kTaskCombine) {
-                if (!combine_task(p, P, m.a, scratch, ctl, wc)) break;
-                continue;
-            }
-            uint32_t acc;
-            if (!epi_acquire(ctl, g, 2, tmem, wc, acc, wseq)) break;
-            const uint32_t lane_base = acc + (static_cast<uint32_t>(q * 32) << 16);
+            const bool two = type == kTaskGateUp;
+            uint32_t acc, acc1;
+            if (!epi_acquire(ctl, es, two, m.n, tmem, wc, acc, acc1)) break;
+            const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+            const uint32_t lane_base = acc + lane_off;
             const int row0 = m.row0, rows = m.rows, n = m.n;
             if (type == kTaskGateUp) {
                 const int ft = m.b;
@@ -733,7 +764,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 for (int c0 = 0; c0 < n; c0 += 16) {
                     float gv[16], uv[16];
                     tmem_ld16(lane_base + c0, gv);
-                    tmem_ld16(lane_base + kAccBufCols / 2 + c0, uv);
+                    tmem_ld16(acc1 + lane_off + c0, uv);
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
@@ -741,8 +772,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                             p.h[static_cast<size_t>(row0 + c0 + c) * F + f] =
                                 __float2bfloat16_rn(silu_mul(gv[c], uv[c]));
                 }
-                epi_release(ctl, g, 2);
-                ++g;
+                epi_release(ctl, es, true, n);
                 fence_proxy_async_global();  // h is read back by TMA
                 worker_sync();
                 if (wtid == 0) {
@@ -770,8 +800,8 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                         p.partial[(static_cast<size_t>(s) * cap + row) * H + hh] = v[c];
                 }
             }
-            epi_release(ctl, g, 2);
-            ++g;
+            epi_release(ctl, es, false, n);
+            fence_proxy_async_global();  // y is gathered by bulk copies in the combine
             worker_sync();  // the tile's stores are done
             bool done = true;
             if (S > 1) {
@@ -790,6 +820,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                             sum += __ldcg(p.partial + (static_cast<size_t>(s2) * cap + row) * H + c);
                         p.y[row * H + c] = __float2bfloat16_rn(sum);
                     }
+                    fence_proxy_async_global();
                     worker_sync();
                 }
             }
@@ -802,7 +833,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
 
     const uint64_t t_exit = globaltimer_ns();
     const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
-    cta_teardown(ctl, stg, aborted_run);
+    cta_teardown(ctl, aborted_run);
     if (threadIdx.x == 0) trace_rec(p, 0, 3, 0, 0, t_exit, globaltimer_ns());
 
     // Exit protocol: the last CTA out returns every counter to zero.
@@ -836,8 +867,8 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
     }
 }
 
-int moe_stages() { return stages_for(kMoeNMax, kMoeScratch); }
-int moe_smem_bytes() { return smem_bytes_for(moe_stages(), kMoeNMax, kMoeScratch); }
+int moe_smem_bytes() { return smem_bytes_for(kMoeScratch); }
+int moe_ring_bytes() { return ring_bytes_for(kMoeScratch); }
 
 // Host-side launch (called by the C ABI after validation).
 cudaError_t launch_moe(const MoeArgs& a, const CUtensorMap* maps, int grid, int smem,
@@ -852,7 +883,8 @@ cudaError_t launch_moe(const MoeArgs& a, const CUtensorMap* maps, int grid, int 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_megakernel, maps[0], maps[1], maps[2], maps[3], maps[4], a);
+    return cudaLaunchKernelEx(&cfg, moe_megakernel, maps[0], maps[1], maps[2], maps[3], maps[4],
+                              maps[5], a);
 }
 
 cudaError_t prepare_moe(int smem) {

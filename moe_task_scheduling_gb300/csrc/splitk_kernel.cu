@@ -37,9 +37,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ SplitKArgs p) {
     extern __shared__ uint8_t smem_raw[];
-    Stages stg;
+    Ring ring;
     uint8_t* scratch;
-    Ctl* ctl = cta_setup(smem_raw, p.stages, kWideNMax, 0, stg, &scratch);
+    Ctl* ctl = cta_setup(smem_raw, 0, ring, &scratch);
     const WaitCtx wc{p.hdr, p.timeout_ns};
     const uint32_t tmem = ctl->tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -57,35 +57,34 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 
     auto gemm_of = [&](const SplitKTile& t) {
         return GemmTask{&tm_w, nullptr, &tm_x, t.nt * kTileM, t.mt * kWideNMax, t.s * kbs, kbs,
-                        t.n, t.n <= kWideNMax / 2 ? 2 : 1, nullptr, 0, 0};
+                        t.n, nullptr, 0, 0};
     };
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
-            uint32_t it = 0;
+            ProdState ps;
             for (int task = blockIdx.x; task < total; task += gridDim.x)
-                if (!produce_task(gemm_of(splitk_tile(task, split, NT, M)), stg, ctl, it, wc, pol_w,
+                if (!produce_task(gemm_of(splitk_tile(task, split, NT, M)), ring, ctl, ps, wc, pol_w,
                                   pol_b))
                     break;
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            uint32_t it = 0, g = 0;
+            MmaState ms;
             for (int task = blockIdx.x; task < total; task += gridDim.x)
-                if (!mma_task(gemm_of(splitk_tile(task, split, NT, M)), stg, ctl, it, g, 2, 0, tmem,
-                              wc))
+                if (!mma_task(gemm_of(splitk_tile(task, split, NT, M)), ring, ctl, ms, tmem, wc))
                     break;
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
         const int q = warp - kEpiWarp0, wtid = threadIdx.x - kEpiWarp0 * 32;
-        uint32_t g = 0, wseq = 0;
-        for (int task = blockIdx.x; task < total; task += gridDim.x, ++g) {
+        EpiState es;
+        for (int task = blockIdx.x; task < total; task += gridDim.x) {
             const SplitKTile t = splitk_tile(task, split, NT, M);
-            uint32_t acc;
-            if (!epi_acquire(ctl, g, 2, tmem, wc, acc, wseq)) break;
+            uint32_t acc, acc1;
+            if (!epi_acquire(ctl, es, false, t.n, tmem, wc, acc, acc1)) break;
             const int col = t.nt * kTileM + q * 32 + lane;
             const uint32_t lane_base = acc + (static_cast<uint32_t>(q * 32) << 16);
             const size_t m0 = static_cast<size_t>(t.mt) * kWideNMax;
@@ -103,7 +102,7 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                         p.partial[(static_cast<size_t>(t.s) * p.M_max + m) * N + col] = v[c];
                 }
             }
-            epi_release(ctl, g, 2);
+            epi_release(ctl, es, false, t.n);
             if (split > 1) {
                 int* ev = p.ev + t.mt * NT + t.nt;
                 worker_sync();  // every partial of this CTA is stored
@@ -128,7 +127,7 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     }
 
     const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
-    cta_teardown(ctl, stg, aborted_run);
+    cta_teardown(ctl, aborted_run);
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -145,8 +144,7 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     }
 }
 
-int splitk_smem_bytes() { return smem_bytes_for(stages_for(kWideNMax, 0), kWideNMax, 0); }
-int splitk_stages() { return stages_for(kWideNMax, 0); }
+int splitk_smem_bytes() { return smem_bytes_for(0); }
 
 cudaError_t launch_splitk(const SplitKArgs& a, const CUtensorMap* maps, int grid, int smem,
                           cudaStream_t stream) {
