@@ -412,6 +412,23 @@ def run_ours(args, world, rank, local):
     return line
 
 
+def run_single(args, local):
+    """One layer call at token count T after `warmup` identical calls (L2
+    flushed before each): the launch an ncu capture selects with -s/-c."""
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cfg = {"mixtral": wl.MIXTRAL, "fine": wl.FINE}[args.workload]
+    b = MoeBench(cfg, device)
+    b.d_T.fill_(args.single)
+    for _ in range(args.warmup + 1):
+        b.flush.zero_()
+        b.call()
+    torch.cuda.synchronize()
+    code, detail = b.etmoe.et_status(b.ws)
+    return {"single": args.single, "workload": args.workload, "launches": args.warmup + 1,
+            "status": [code, detail]}
+
+
 def cpu_baseline(b, cfg, args):
     """The oracle, as it stands, on the host cores over a bounded sample of the
     same workload (the first `n` tokens of the sweep's largest batch)."""
@@ -478,11 +495,18 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single", type=int, default=None,
+                    help="MoE workloads: run warmup+1 calls at this token count and exit "
+                         "(for profiler captures; prints no bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
-    if args.impl == "reference":
+    if args.single is not None:
+        if args.workload not in ("mixtral", "fine"):
+            ap.error("--single applies to the MoE workloads")
+        line = run_single(args, local) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, world, rank)
     elif args.workload in ("splitk", "mlp"):
         line = run_dense(args, local) if rank == 0 else None

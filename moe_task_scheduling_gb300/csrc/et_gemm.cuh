@@ -14,9 +14,11 @@
 //   warp 1 lane 0   MMA issuer: per task, waits for free TMEM accumulator
 //                   slots, issues tcgen05.mma per full fill, frees each fill
 //                   with tcgen05.commit, commits the accumulator slots;
-//   warps 4..7      workers: the epilogue (tcgen05.ld from TMEM, stores,
+//   warps 4..11     workers: the epilogue (tcgen05.ld from TMEM, stores,
 //                   event releases) and every non-GEMM task; they sync among
-//                   themselves with named barrier 1.
+//                   themselves with named barrier 1.  Warp w reads TMEM lanes
+//                   32*(w%4) ..; warps 4..7 take the even 16-column chunks of
+//                   an accumulator, warps 8..11 the odd ones.
 //
 // The stage ring is byte-granular: a fill takes exactly the bytes of its
 // k-block (weights 16 or 32 KB, plus n * 128 bytes of activation rows), so a
@@ -35,7 +37,7 @@
 namespace et {
 
 constexpr int kTaskRing = 4;       // dynamic-queue tasks handed from producer to consumers
-constexpr int kWorkers = 128;      // warps 4..7
+constexpr int kWorkers = 256;      // warps 4..11
 constexpr int kWorkerBar = 1;      // named barrier id of the worker group
 constexpr int kSlots = 16;         // ring fills in flight at most (one barrier pair each)
 constexpr int kAccSlotCols = 256;  // TMEM columns per accumulator slot
@@ -74,14 +76,16 @@ struct Ring {
 };
 
 struct GemmTask {
-    const CUtensorMap* a0;  // weight map, box 64 x 128
-    const CUtensorMap* a1;  // second weight map (gate/up) or nullptr
-    const CUtensorMap* b;   // activation map, box 64 x 16
-    int a_row;              // first weight row
-    int b_row;              // first activation row
-    int kb0, nkb;           // k-blocks [kb0, kb0 + nkb), 64 elements each
-    int n;                  // UMMA N: multiple of 16, <= 256
-    const int* dep;         // wait *dep >= dep_target before activation loads
+    const CUtensorMap* a0;   // weight map, box 64 x 128
+    const CUtensorMap* a1;   // second weight map (gate/up) or nullptr
+    const CUtensorMap* b;    // activation map, box 64 x 16
+    const CUtensorMap* b64;  // the same activations, box 64 x 64
+    int a_row;               // first weight row
+    int b_row;               // first activation row
+    int kb0, nkb;            // k-blocks [kb0, kb0 + nkb), 64 elements each
+    int n;                   // UMMA N: multiple of 16, <= 256
+    int rot;                 // the k loop starts at fill rot % fills (see fill_kb)
+    const int* dep;          // wait *dep >= dep_target before activation loads
     int dep_target;
     int dep_where;
 };
@@ -96,6 +100,17 @@ __device__ __forceinline__ int kpack_of(const GemmTask& t) {
     return kblock_bytes(t) <= 24576u ? 2 : 1;
 }
 __device__ __forceinline__ int fills_of(const GemmTask& t) { return ceil_div(t.nkb, kpack_of(t)); }
+// First k-block (relative to kb0) and k-block count of the task's u-th fill.
+// Tasks that share their activation rows run at the same time on different
+// SMs; each starts its k loop at its own rotation, so they do not all pull the
+// same activation k-block through the same L2 slices at once.  The sum order
+// is fixed per task, so results are deterministic.
+__device__ __forceinline__ int fill_kb(const GemmTask& t, int u, int& nk) {
+    const int kp = kpack_of(t), nf = fills_of(t);
+    const int kb = ((u + t.rot) % nf) * kp;
+    nk = min(kp, t.nkb - kb);
+    return kb;
+}
 // Fill layout: [A0 x kp][A1 x kp][B x kp] (every tile 1024-byte aligned); a
 // ragged last fill is placed with the full size.
 __device__ __forceinline__ uint32_t unit_bytes(const GemmTask& t) {
@@ -173,11 +188,13 @@ __device__ __forceinline__ bool post_weights(const GemmTask& t, const Ring& R, C
     if (!ring_reserve(ctl, ps, start, sb, R.bytes, wc)) return false;
     const uint32_t slot = ps.it % kSlots;
     ctl->unit_end[slot] = start + sb;
-    const int kp = kpack_of(t), nk = min(kp, t.nkb - u * kp);
+    const int kp = kpack_of(t);
+    int nk;
+    const int kb = fill_kb(t, u, nk);
     mbar_arrive_expect_tx(&ctl->full[slot], static_cast<uint32_t>(nk) * kblock_bytes(t));
     uint8_t* dst = R.base + start % R.bytes;
     for (int j = 0; j < nk; ++j) {
-        const int kx = (t.kb0 + u * kp + j) * kBlockK;
+        const int kx = (t.kb0 + kb + j) * kBlockK;
         tma_load_2d(dst + j * kABytes, t.a0, &ctl->full[slot], kx, t.a_row, pol_w);
         if (t.a1)
             tma_load_2d(dst + (kp + j) * kABytes, t.a1, &ctl->full[slot], kx, t.a_row, pol_w);
@@ -191,14 +208,19 @@ __device__ __forceinline__ void load_acts(const GemmTask& t, const Ring& R, Ctl*
                                           int u, uint64_t pol_b) {
     const uint32_t slot = f % kSlots;
     const uint32_t start = ctl->unit_end[slot] - unit_bytes(t);
-    const int kp = kpack_of(t), nk = min(kp, t.nkb - u * kp);
+    const int kp = kpack_of(t);
+    int nk;
+    const int kb = fill_kb(t, u, nk);
     const uint32_t bbytes = static_cast<uint32_t>(t.n) * 128u;
     uint8_t* bb = R.base + start % R.bytes + static_cast<uint32_t>(kp) * (t.a1 ? 2u : 1u) * kABytes;
+    const int n64 = t.b64 ? t.n / kBBoxRowsWide * kBBoxRowsWide : 0;  // rows in 64-row boxes
     for (int j = 0; j < nk; ++j) {
-        const int kx = (t.kb0 + u * kp + j) * kBlockK;
-        for (int i = 0; i < t.n / kBBoxRows; ++i)
-            tma_load_2d(bb + j * bbytes + i * (kBBoxRows * 128), t.b, &ctl->full[slot], kx,
-                        t.b_row + i * kBBoxRows, pol_b);
+        const int kx = (t.kb0 + kb + j) * kBlockK;
+        uint8_t* bj = bb + j * bbytes;
+        for (int r = 0; r < n64; r += kBBoxRowsWide)
+            tma_load_2d(bj + r * 128, t.b64, &ctl->full[slot], kx, t.b_row + r, pol_b);
+        for (int r = n64; r < t.n; r += kBBoxRows)
+            tma_load_2d(bj + r * 128, t.b, &ctl->full[slot], kx, t.b_row + r, pol_b);
     }
 }
 
@@ -272,7 +294,8 @@ __device__ __forceinline__ bool mma_task(const GemmTask& t, const Ring& R, Ctl* 
         ctl->consumed = static_cast<int32_t>(ms.it);
         tc_fence_after();
         const uint32_t base = smem_u32(R.base + start % R.bytes);
-        const int nk = min(kp, t.nkb - u * kp);
+        int nk;
+        (void)fill_kb(t, u, nk);
         for (int j = 0; j < nk; ++j) {
             const uint32_t a_s = base + j * kABytes;
             const uint32_t a1_s = base + (kp + j) * kABytes;
@@ -297,7 +320,7 @@ __device__ __forceinline__ bool mma_task(const GemmTask& t, const Ring& R, Ctl* 
 __device__ __forceinline__ void worker_sync() { named_bar_sync(kWorkerBar, kWorkers); }
 
 // A bounded mbarrier wait taken by the whole worker group: one worker thread
-// waits, the decision is broadcast, so all four worker warps always take the
+// waits, the decision is broadcast, so all worker warps always take the
 // same path (a named barrier cannot be bounded, so they must never diverge).
 // `seq` is the caller's running count of worker_wait calls.
 __device__ __forceinline__ bool worker_wait(Ctl* ctl, uint64_t* bar, uint32_t parity,
@@ -362,6 +385,36 @@ __device__ __forceinline__ void ring_return(Ctl* ctl) {
         fence_proxy_async_smem();
         __threadfence_block();
         *reinterpret_cast<volatile int32_t*>(&ctl->ring_ret) = ctl->ring_ret + 1;
+    }
+}
+
+// Split reduction of one row slice: Y[r, col0 .. col0+128) =
+// bf16(sum over s in order 0, 1, .. of part[s][r][col]) for r in [r0, r1).
+// part + s * sstride + r * ld + col addresses partial s (fp32); the worker
+// group reads float4 columns with every split's load in flight at once.
+__device__ __forceinline__ void reduce_slice(const float* part, size_t sstride, int ld, int split,
+                                             int r0, int r1, int col0, bf16* Y, int ldy) {
+    constexpr int kMaxSplit = 16;
+    const int nv = (r1 - r0) * (kTileM / 4);
+    for (int v = static_cast<int>(threadIdx.x) - kEpiWarp0 * 32; v < nv; v += kWorkers) {
+        const int row = r0 + v / (kTileM / 4), col = col0 + (v % (kTileM / 4)) * 4;
+        const float* src = part + static_cast<size_t>(row) * ld + col;
+        float4 q[kMaxSplit];
+#pragma unroll
+        for (int s = 0; s < kMaxSplit; ++s)
+            if (s < split) q[s] = __ldcg(reinterpret_cast<const float4*>(src + s * sstride));
+        float4 acc = q[0];
+#pragma unroll
+        for (int s = 1; s < kMaxSplit; ++s)
+            if (s < split) {
+                acc.x = acc.x + q[s].x;
+                acc.y = acc.y + q[s].y;
+                acc.z = acc.z + q[s].z;
+                acc.w = acc.w + q[s].w;
+            }
+        __nv_bfloat162 o[2] = {__floats2bfloat162_rn(acc.x, acc.y), __floats2bfloat162_rn(acc.z, acc.w)};
+        *reinterpret_cast<uint2*>(Y + static_cast<size_t>(row) * ldy + col) =
+            *reinterpret_cast<const uint2*>(o);
     }
 }
 

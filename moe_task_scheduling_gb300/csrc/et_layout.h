@@ -14,12 +14,13 @@ using bf16 = __nv_bfloat16;
 
 // ---------------------------------------------------------------- tiling constants
 
-constexpr int kThreads = 256;        // 8 warps: 0 TMA, 1 MMA/TMEM, 2-3 spare, 4-7 epilogue
-constexpr int kEpiWarp0 = 4;         // epilogue warp w reads TMEM lanes 32*(w-4) ..
+constexpr int kThreads = 384;        // 12 warps: 0 TMA, 1 MMA/TMEM, 2-3 spare, 4-11 workers
+constexpr int kEpiWarp0 = 4;         // worker warp w reads TMEM lanes 32*(w%4) ..
 constexpr int kTileM = 128;          // weight rows per tile (UMMA M)
 constexpr int kBlockK = 64;          // bf16 elements per k-block = one 128-byte swizzle row
 constexpr int kABytes = kTileM * kBlockK * 2;   // 16 KB weight tile
 constexpr int kBBoxRows = 16;        // activation rows per TMA box
+constexpr int kBBoxRowsWide = 64;    // activation rows per wide TMA box
 constexpr int kTmemCols = 512;       // accumulator 0 at column 0, accumulator 1 at 256
 constexpr int kAcc1Col = 256;
 constexpr int kSmemLimit = 232448;   // 227 KB of opt-in dynamic shared memory per CTA
@@ -111,6 +112,7 @@ struct MoeArgs {
     float* partial;       // [kSplitMax, split_rows_cap, H]
     int mt_max, q_max, split_rows_cap, r_max;
     int wr_box;           // router-weight TMA box height (0: the weight is read in place)
+    int b_wide;           // the 64-row activation maps are valid (enough rows)
     int num_ctas;
     uint64_t* trace;      // optional per-task trace (see et_opts)
     int trace_cap;
@@ -125,6 +127,7 @@ struct SplitKArgs {
     EtHeader* hdr;
     int32_t* ev;          // [ceil(M_max/256) * N/128], self-resetting
     float* partial;       // [split, M_max, N]
+    int b_wide;
     int num_ctas;
     uint64_t timeout_ns;
     int fault_mode, fault_arg;
@@ -144,6 +147,7 @@ struct MlpArgs {
     int32_t* ev_y;        // [mt_max * H/128], self-resetting
     float* partial;       // [kSplitMax, B_max, H]
     int mt_max;
+    int b_wide;
     int num_ctas;
     uint64_t timeout_ns;
     int fault_mode, fault_arg;

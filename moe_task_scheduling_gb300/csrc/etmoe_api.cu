@@ -333,7 +333,7 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
     a.trace = (opts && opts->trace && opts->trace_cap) ? static_cast<uint64_t*>(opts->trace) : nullptr;
     a.trace_cap = opts ? static_cast<int>(opts->trace_cap) : 0;
 
-    CUtensorMap maps[6];
+    CUtensorMap maps[8];
     const uint64_t EF = static_cast<uint64_t>(E) * F, EH = static_cast<uint64_t>(E) * H;
     if ((rc = make_map(&maps[0], w_gate, EF, H, kTileM, "w_gate"))) return rc;
     if ((rc = make_map(&maps[1], w_up, EF, H, kTileM, "w_up"))) return rc;
@@ -344,6 +344,14 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
         if ((rc = make_map_plain(&maps[5], w_router, H, E, 8, a.wr_box, "w_router"))) return rc;
     } else {
         maps[5] = maps[0];  // unused: the router weight is read in place
+    }
+    a.b_wide = L.Tk >= kBBoxRowsWide ? 1 : 0;
+    if (a.b_wide) {
+        if ((rc = make_map(&maps[6], a.xp, L.Tk, H, kBBoxRowsWide, "permuted x"))) return rc;
+        if ((rc = make_map(&maps[7], a.h, L.Tk, F, kBBoxRowsWide, "h"))) return rc;
+    } else {
+        maps[6] = maps[3];
+        maps[7] = maps[4];
     }
     cudaError_t e = launch_moe(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "launch of the MoE megakernel");
@@ -398,9 +406,15 @@ int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t*
     a.timeout_ns = timeout_ns_of(opts);
     a.fault_mode = opts ? opts->fault_mode : 0;
     a.fault_arg = opts ? opts->fault_arg : 0;
-    CUtensorMap maps[2];
+    CUtensorMap maps[3];
     if ((rc = make_map(&maps[0], Wt, N, K, kTileM, "Wt"))) return rc;
     if ((rc = make_map(&maps[1], X, M_max, K, kBBoxRows, "X"))) return rc;
+    a.b_wide = M_max >= kBBoxRowsWide ? 1 : 0;
+    if (a.b_wide) {
+        if ((rc = make_map(&maps[2], X, M_max, K, kBBoxRowsWide, "X"))) return rc;
+    } else {
+        maps[2] = maps[1];
+    }
     cudaError_t e = launch_splitk(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "launch of the split-K kernel");
     return ET_OK;
@@ -459,12 +473,20 @@ int et_mlp_chain(const void* x, const void* gamma, float eps, const void* w_gate
     a.timeout_ns = timeout_ns_of(opts);
     a.fault_mode = opts ? opts->fault_mode : 0;
     a.fault_arg = opts ? opts->fault_arg : 0;
-    CUtensorMap maps[5];
+    CUtensorMap maps[7];
     if ((rc = make_map(&maps[0], w_gate, F, H, kTileM, "w_gate"))) return rc;
     if ((rc = make_map(&maps[1], w_up, F, H, kTileM, "w_up"))) return rc;
     if ((rc = make_map(&maps[2], w_down, H, F, kTileM, "w_down"))) return rc;
     if ((rc = make_map(&maps[3], a.xhat, B_max, H, kBBoxRows, "xhat"))) return rc;
     if ((rc = make_map(&maps[4], a.h, B_max, F, kBBoxRows, "h"))) return rc;
+    a.b_wide = B_max >= kBBoxRowsWide ? 1 : 0;
+    if (a.b_wide) {
+        if ((rc = make_map(&maps[5], a.xhat, B_max, H, kBBoxRowsWide, "xhat"))) return rc;
+        if ((rc = make_map(&maps[6], a.h, B_max, F, kBBoxRowsWide, "h"))) return rc;
+    } else {
+        maps[5] = maps[3];
+        maps[6] = maps[4];
+    }
     cudaError_t e = launch_mlp(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "launch of the MLP chain kernel");
     return ET_OK;

@@ -7,7 +7,10 @@
 //   [0, NR)                 NORM i      8 rows each;      releases ev_norm
 //   [NR, NR + MT*FT)        GATEUP m,f  waits ev_norm >= NR; releases ev_h[m][chunk(f)]
 //   [.., + MT*S*HT)         DOWN m,s,n  waits ev_h[m][s] >= F-tiles per chunk;
-//                                       split partials meet on ev_y[m][n]
+//                                       with a split, stores an fp32 partial and
+//                                       releases ev_y[m][n]
+//   [.., + ceil(B/32)*HT)   REDUCE q,n  (split only) waits ev_y[m][n] >= S, sums
+//                                       rows 32q .. of the partials in chunk order
 // so every wait is on a lower index, which a resident CTA reaches first (the
 // launch is cooperative: all CTAs are resident).  The targets (NR, F-tiles
 // per chunk) are computed on the device from the batch size, which may itself
@@ -20,14 +23,16 @@
 
 namespace et {
 
-constexpr int kNormRows = 8;  // two rows per worker warp
+constexpr int kNormRows = 8;  // one row per worker warp
+
+constexpr int kRedRows = 32;  // rows per REDUCE task
 
 struct MlpPlan {
-    int B, NR, MT, FT, HT, S, n_gu, n_dn, total;
+    int B, NR, MT, FT, HT, S, n_gu, n_dn, n_red, total;
 };
 
 struct MlpTile {
-    int kind;  // 0 norm, 1 gate/up, 2 down
+    int kind;  // 0 norm, 1 gate/up, 2 down, 3 reduce
     int i, mt, ft, s, ht, rows, n;
 };
 
@@ -36,6 +41,13 @@ __device__ __forceinline__ MlpTile mlp_tile(const MlpPlan& P, int task) {
     if (task < P.NR) {
         t.kind = 0;
         t.i = task;
+        return t;
+    }
+    if (task >= P.NR + P.n_gu + P.n_dn) {
+        t.kind = 3;
+        t.i = task - P.NR - P.n_gu - P.n_dn;
+        t.ht = t.i % P.HT;
+        t.s = t.i / P.HT;  // row slice
         return t;
     }
     if (task < P.NR + P.n_gu) {
@@ -99,7 +111,8 @@ __device__ __forceinline__ void norm_rows(const MlpArgs& p, int B, int i) {
 __global__ void __launch_bounds__(kThreads, 1)
 mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                  const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xhat,
-                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ MlpArgs p) {
+                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_xhat64,
+                 const __grid_constant__ CUtensorMap tm_h64, const __grid_constant__ MlpArgs p) {
     extern __shared__ uint8_t smem_raw[];
     Ring ring;
     uint8_t* scratch;
@@ -132,15 +145,17 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     }
     P.n_gu = P.MT * P.FT;
     P.n_dn = P.MT * P.S * P.HT;
-    P.total = P.NR + P.n_gu + P.n_dn;
+    P.n_red = P.S > 1 ? ceil_div(P.B, kRedRows) * P.HT : 0;
+    P.total = P.NR + P.n_gu + P.n_dn + P.n_red;
 
     auto gemm_of = [&](const MlpTile& t) {
         if (t.kind == 1)
-            return GemmTask{&tm_wg, &tm_wu, &tm_xhat, t.ft * kTileM, t.mt * kWideNMax, 0,
-                            p.H / kBlockK, t.n, &p.hdr->ev_norm, P.NR, kWhereNorm};
+            return GemmTask{&tm_wg, &tm_wu, &tm_xhat, p.b_wide ? &tm_xhat64 : nullptr,
+                            t.ft * kTileM, t.mt * kWideNMax, 0, p.H / kBlockK, t.n, t.ft,
+                            &p.hdr->ev_norm, P.NR, kWhereNorm};
         const int fchunk = p.F / P.S;
-        return GemmTask{&tm_wd, nullptr, &tm_h, t.ht * kTileM, t.mt * kWideNMax,
-                        t.s * (fchunk / kBlockK), fchunk / kBlockK, t.n,
+        return GemmTask{&tm_wd, nullptr, &tm_h, p.b_wide ? &tm_h64 : nullptr, t.ht * kTileM,
+                        t.mt * kWideNMax, t.s * (fchunk / kBlockK), fchunk / kBlockK, t.n, t.ht,
                         &p.ev_h[t.mt * kSplitMax + t.s], P.FT / P.S, kWhereH};
     };
 
@@ -150,7 +165,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             ProdState ps;
             for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
                 const MlpTile t = mlp_tile(P, task);
-                if (t.kind == 0) continue;
+                if (t.kind == 0 || t.kind == 3) continue;
                 if (!produce_task(gemm_of(t), ring, ctl, ps, wc, pol_w, pol_b)) break;
             }
         }
@@ -160,13 +175,14 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             MmaState ms;
             for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
                 const MlpTile t = mlp_tile(P, task);
-                if (t.kind == 0) continue;
+                if (t.kind == 0 || t.kind == 3) continue;
                 if (!mma_task(gemm_of(t), ring, ctl, ms, tmem, wc)) break;
             }
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
-        const int q = warp - kEpiWarp0, wtid = threadIdx.x - kEpiWarp0 * 32;
+        const int q = (warp - kEpiWarp0) & 3, half = (warp - kEpiWarp0) >> 2;
+        const int wtid = threadIdx.x - kEpiWarp0 * 32;
         const int H = p.H, F = p.F;
         EpiState es;
         for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
@@ -181,6 +197,18 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 }
                 continue;
             }
+            if (t.kind == 3) {  // REDUCE: row slice t.s of output column tile t.ht
+                const int r0 = t.s * kRedRows, r1 = min(P.B, r0 + kRedRows);
+                const int mt = r0 / kWideNMax;
+                if (wtid == 0)
+                    ctl->flag =
+                        ev_wait_geq(wc, p.ev_y + mt * P.HT + t.ht, P.S, kWhereY) ? 1 : 0;
+                worker_sync();
+                if (!ctl->flag) break;
+                reduce_slice(p.partial, static_cast<size_t>(p.B_max) * H, H, P.S, r0, r1,
+                             t.ht * kTileM, p.out, H);
+                continue;
+            }
             const bool two = t.kind == 1;
             uint32_t acc, acc1;
             if (!epi_acquire(ctl, es, two, t.n, tmem, wc, acc, acc1)) break;
@@ -189,7 +217,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const size_t m0 = static_cast<size_t>(t.mt) * kWideNMax;
             if (t.kind == 1) {
                 const int f = t.ft * kTileM + q * 32 + lane;
-                for (int c0 = 0; c0 < t.n; c0 += 16) {
+                for (int c0 = half * 16; c0 < t.n; c0 += 32) {
                     float gv[16], uv[16];
                     tmem_ld16(lane_base + c0, gv);
                     tmem_ld16(acc1 + lane_off + c0, uv);
@@ -212,7 +240,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             }
             // down projection tile
             const int hh = t.ht * kTileM + q * 32 + lane;
-            for (int c0 = 0; c0 < t.n; c0 += 16) {
+            for (int c0 = half * 16; c0 < t.n; c0 += 32) {
                 float v[16];
                 tmem_ld16(lane_base + c0, v);
                 tmem_ld_wait();
@@ -227,24 +255,11 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 }
             }
             epi_release(ctl, es, false, t.n);
-            if (P.S > 1) {
-                int* ev = p.ev_y + t.mt * P.HT + t.ht;
+            if (P.S > 1) {  // the partial is stored: count it on the tile's event
                 worker_sync();
                 if (wtid == 0) {
                     __threadfence();
-                    ctl->flag = (atom_acq_rel_add(ev, 1) == P.S - 1) ? 1 : 0;
-                }
-                worker_sync();
-                if (ctl->flag) {
-                    for (int j = wtid; j < t.rows * kTileM; j += kWorkers) {
-                        const size_t m = m0 + j / kTileM;
-                        const int c = t.ht * kTileM + (j % kTileM);
-                        float sum = 0.0f;
-                        for (int s2 = 0; s2 < P.S; ++s2)
-                            sum += __ldcg(p.partial + (static_cast<size_t>(s2) * p.B_max + m) * H + c);
-                        p.out[m * H + c] = __float2bfloat16_rn(sum);
-                    }
-                    if (wtid == 0) *ev = 0;
+                    red_release_add(p.ev_y + t.mt * P.HT + t.ht, 1);
                 }
             }
         }
@@ -263,8 +278,8 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         const bool ab = ld_relaxed(&p.hdr->abort) != 0;
         const int mt_clear = ab ? p.mt_max : P.MT;
         for (int j = threadIdx.x; j < mt_clear * kSplitMax; j += kThreads) p.ev_h[j] = 0;
-        if (ab)
-            for (int j = threadIdx.x; j < p.mt_max * P.HT; j += kThreads) p.ev_y[j] = 0;
+        const int y_clear = ab ? p.mt_max : (P.S > 1 ? P.MT : 0);
+        for (int j = threadIdx.x; j < y_clear * P.HT; j += kThreads) p.ev_y[j] = 0;
         __syncthreads();
         if (threadIdx.x == 0) {
             p.hdr->ev_norm = 0;
@@ -290,7 +305,7 @@ cudaError_t launch_mlp(const MlpArgs& a, const CUtensorMap* maps, int grid, int 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, mlp_chain_kernel, maps[0], maps[1], maps[2], maps[3], maps[4],
-                              a);
+                              maps[5], maps[6], a);
 }
 
 cudaError_t prepare_mlp(int smem) {

@@ -99,7 +99,7 @@ __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, 
     const int H = p.H, E = p.E;
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
     constexpr int TB = 4;  // tokens per job
-    constexpr int U = 4;   // h-steps whose weights are loaded ahead of their fmas
+    constexpr int U = 2;   // h-steps whose weights are loaded ahead of their fmas
     const int neb = ec / EBW, ntb = ceil_div(nt, TB);
     for (int job = warp; job < neb * ntb; job += kWorkers / 32) {
         const int tb = job / neb, j0 = (job % neb) * EBW;
@@ -653,6 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xp,
                const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wr,
+               const __grid_constant__ CUtensorMap tm_xp64, const __grid_constant__ CUtensorMap tm_h64,
                const __grid_constant__ MoeArgs p) {
     extern __shared__ uint8_t smem_raw[];
     const uint64_t t_start = globaltimer_ns();
@@ -676,12 +677,14 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
     auto gemm_of = [&](const TaskMsg& m) {
         const int type = m.type & 0xff, S = m.type >> 8;
         if (type == kTaskGateUp)
-            return GemmTask{&tm_wg, &tm_wu, &tm_xp, m.e * p.F + m.b * kTileM, m.row0, 0,
-                            p.H / kBlockK, m.n, &p.hdr->ev_perm, P.R * P.Q, kWherePerm};
+            return GemmTask{&tm_wg, &tm_wu, &tm_xp, p.b_wide ? &tm_xp64 : nullptr,
+                            m.e * p.F + m.b * kTileM, m.row0, 0, p.H / kBlockK, m.n, m.b,
+                            &p.hdr->ev_perm, P.R * P.Q, kWherePerm};
         const int fchunk = p.F / S;
-        return GemmTask{&tm_wd, nullptr, &tm_h, m.e * p.H + m.c * kTileM, m.row0,
-                        m.b * (fchunk / kBlockK), fchunk / kBlockK, m.n,
-                        &p.ev_h[m.a * kSplitMax + m.b], FT / S, kWhereH};
+        return GemmTask{&tm_wd, nullptr, &tm_h, p.b_wide ? &tm_h64 : nullptr,
+                        m.e * p.H + m.c * kTileM, m.row0, m.b * (fchunk / kBlockK),
+                        fchunk / kBlockK, m.n, m.c, &p.ev_h[m.a * kSplitMax + m.b], FT / S,
+                        kWhereH};
     };
 
     if (warp == 0) {
@@ -689,6 +692,9 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
             ProdState ps;
             for (int i = 0;; ++i) {
+                // a SIMT task still out on lease: take no further task before it
+                // is done, so SIMT work spreads over the CTAs that are free
+                if (!ring_lease_wait(ctl, ps, wc)) break;
                 const uint64_t tp = globaltimer_ns();
                 const TaskMsg m = pop_task(p, wc, P);
                 const int slot = i % kTaskRing;
@@ -723,7 +729,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {  // workers: epilogues and SIMT tasks
-        const int q = warp - kEpiWarp0, wtid = wtid_();
+        const int q = (warp - kEpiWarp0) & 3, half = (warp - kEpiWarp0) >> 2, wtid = wtid_();
         const int H = p.H, F = p.F;
         EpiState es;
         uint32_t sphase = 0;
@@ -761,7 +767,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             if (type == kTaskGateUp) {
                 const int ft = m.b;
                 const int f = ft * kTileM + q * 32 + lane;
-                for (int c0 = 0; c0 < n; c0 += 16) {
+                for (int c0 = half * 16; c0 < n; c0 += 32) {
                     float gv[16], uv[16];
                     tmem_ld16(lane_base + c0, gv);
                     tmem_ld16(acc1 + lane_off + c0, uv);
@@ -786,7 +792,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             const int s = m.b, ht = m.c;
             const int hh = ht * kTileM + q * 32 + lane;
             const int cap = p.split_rows_cap;
-            for (int c0 = 0; c0 < n; c0 += 16) {
+            for (int c0 = half * 16; c0 < n; c0 += 32) {
                 float v[16];
                 tmem_ld16(lane_base + c0, v);
                 tmem_ld_wait();
@@ -884,7 +890,7 @@ cudaError_t launch_moe(const MoeArgs& a, const CUtensorMap* maps, int grid, int 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, moe_megakernel, maps[0], maps[1], maps[2], maps[3], maps[4],
-                              maps[5], a);
+                              maps[5], maps[6], maps[7], a);
 }
 
 cudaError_t prepare_moe(int smem) {

@@ -1,15 +1,19 @@
 // splitk_kernel.cu -- split-K GEMM whose partial sums meet through event
 // counters instead of a second kernel:
 //   Y[M,N] = bf16( sum_{s < split} X[:, K_s] Wt[:, K_s]^T )
-// Task (mt, nt, s) computes an fp32 partial of a 256 x 128 output tile over
-// K chunk s and adds 1 to the tile's counter with acquire-release order; the
-// task that sees split-1 sums the partials in chunk order, stores Y and puts
-// the counter back to zero.  No task waits on another, so the schedule cannot
-// deadlock.  M stays symbolic: it may be read from device memory, and the same
-// compiled kernel serves every M up to M_max.
-//
-// Schedule: static, task t runs on CTA t mod grid; every role walks the same
-// task list.
+// Static schedule (task t runs on CTA t mod grid; every role walks the same
+// task list):
+//   [0, G)        TILE (mt, nt, s): fp32 partial of a 256 x 128 output tile over
+//                 K chunk s (bf16 Y directly when split == 1); releases
+//                 ev[mt][nt]
+//   [G, G + R)    REDUCE (q, nt), split > 1 only: waits ev[tile] >= split, then
+//                 sums rows [32q, 32q + 32) of the tile's partials in chunk
+//                 order and stores bf16 Y.
+// Every wait is on a lower task index, and the launch is cooperative (every
+// CTA resident), so the schedule cannot deadlock; the reduction of one tile is
+// spread over many CTAs instead of falling on the last arriver.  The last CTA
+// out returns the tile counters to zero.  M stays symbolic: it may be read
+// from device memory, and the same compiled kernel serves every M up to M_max.
 //
 // Source: "Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
 // Kernels" -- the split-K summation example, where the reduction is gated by
@@ -35,7 +39,7 @@ __device__ __forceinline__ SplitKTile splitk_tile(int task, int split, int NT, i
 
 __global__ void __launch_bounds__(kThreads, 1)
 splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-              const __grid_constant__ SplitKArgs p) {
+              const __grid_constant__ CUtensorMap tm_x64, const __grid_constant__ SplitKArgs p) {
     extern __shared__ uint8_t smem_raw[];
     Ring ring;
     uint8_t* scratch;
@@ -54,10 +58,12 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const int MT = ceil_div(M, kWideNMax), NT = N / kTileM;
     const int kbs = p.K / kBlockK / split;
     const int total = MT * NT * split;
+    constexpr int kRedRows = 32;  // rows per reduce task
+    const int n_red = split > 1 ? ceil_div(M, kRedRows) * NT : 0;
 
     auto gemm_of = [&](const SplitKTile& t) {
-        return GemmTask{&tm_w, nullptr, &tm_x, t.nt * kTileM, t.mt * kWideNMax, t.s * kbs, kbs,
-                        t.n, nullptr, 0, 0};
+        return GemmTask{&tm_w, nullptr, &tm_x, p.b_wide ? &tm_x64 : nullptr, t.nt * kTileM,
+                        t.mt * kWideNMax, t.s * kbs, kbs, t.n, t.nt, nullptr, 0, 0};
     };
 
     if (warp == 0) {
@@ -79,16 +85,28 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
-        const int q = warp - kEpiWarp0, wtid = threadIdx.x - kEpiWarp0 * 32;
+        const int q = (warp - kEpiWarp0) & 3, half = (warp - kEpiWarp0) >> 2;
+        const int wtid = threadIdx.x - kEpiWarp0 * 32;
         EpiState es;
-        for (int task = blockIdx.x; task < total; task += gridDim.x) {
+        for (int task = blockIdx.x; task < total + n_red; task += gridDim.x) {
+            if (task >= total) {  // REDUCE: row slice qs of tile column nt
+                const int r = task - total, nt = r % NT, qs = r / NT;
+                const int r0 = qs * kRedRows, r1 = min(M, r0 + kRedRows), mt = r0 / kWideNMax;
+                if (wtid == 0)
+                    ctl->flag = ev_wait_geq(wc, p.ev + mt * NT + nt, split, kWhereY) ? 1 : 0;
+                worker_sync();
+                if (!ctl->flag) break;
+                reduce_slice(p.partial, static_cast<size_t>(p.M_max) * N, N, split, r0, r1,
+                             nt * kTileM, p.Y, N);
+                continue;
+            }
             const SplitKTile t = splitk_tile(task, split, NT, M);
             uint32_t acc, acc1;
             if (!epi_acquire(ctl, es, false, t.n, tmem, wc, acc, acc1)) break;
             const int col = t.nt * kTileM + q * 32 + lane;
             const uint32_t lane_base = acc + (static_cast<uint32_t>(q * 32) << 16);
             const size_t m0 = static_cast<size_t>(t.mt) * kWideNMax;
-            for (int c0 = 0; c0 < t.n; c0 += 16) {
+            for (int c0 = half * 16; c0 < t.n; c0 += 32) {
                 float v[16];
                 tmem_ld16(lane_base + c0, v);
                 tmem_ld_wait();
@@ -103,24 +121,11 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 }
             }
             epi_release(ctl, es, false, t.n);
-            if (split > 1) {
-                int* ev = p.ev + t.mt * NT + t.nt;
-                worker_sync();  // every partial of this CTA is stored
+            if (split > 1) {  // the partial is stored: count it on the tile's event
+                worker_sync();
                 if (wtid == 0) {
                     __threadfence();
-                    ctl->flag = (atom_acq_rel_add(ev, 1) == split - 1) ? 1 : 0;
-                }
-                worker_sync();
-                if (ctl->flag) {  // last arriver: sum the partials in split order
-                    for (int i = wtid; i < t.rows * kTileM; i += kWorkers) {
-                        const size_t m = m0 + i / kTileM;
-                        const int cc = t.nt * kTileM + (i % kTileM);
-                        float sum = 0.0f;
-                        for (int s2 = 0; s2 < split; ++s2)
-                            sum += __ldcg(p.partial + (static_cast<size_t>(s2) * p.M_max + m) * N + cc);
-                        p.Y[m * N + cc] = __float2bfloat16_rn(sum);
-                    }
-                    if (wtid == 0) *ev = 0;  // every split has arrived: reset for the next call
+                    red_release_add(p.ev + t.mt * NT + t.nt, 1);
                 }
             }
         }
@@ -132,12 +137,11 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     if (threadIdx.x == 0) {
         __threadfence();
         if (atomicAdd(&p.hdr->exit_count, 1) == static_cast<int>(gridDim.x) - 1) {
-            // an aborted launch may leave tile counters behind: clear them all
-            if (ld_relaxed(&p.hdr->abort) != 0) {
-                const int n_ev = ceil_div(p.M_max, kWideNMax) * (N / kTileM);
-                for (int i = 0; i < n_ev; ++i) p.ev[i] = 0;
-                p.hdr->abort = 0;
-            }
+            // the tile counters go back to zero (all of them after an abort)
+            const int n_ev = ld_relaxed(&p.hdr->abort) != 0 ? ceil_div(p.M_max, kWideNMax) * NT
+                                                           : (split > 1 ? MT * NT : 0);
+            for (int i = 0; i < n_ev; ++i) p.ev[i] = 0;
+            p.hdr->abort = 0;
             __threadfence();
             p.hdr->exit_count = 0;
         }
@@ -153,7 +157,12 @@ cudaError_t launch_splitk(const SplitKArgs& a, const CUtensorMap* maps, int grid
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, splitk_kernel, maps[0], maps[1], a);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_kernel, maps[0], maps[1], maps[2], a);
 }
 
 cudaError_t prepare_splitk(int smem) {
