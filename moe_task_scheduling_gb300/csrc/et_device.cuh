@@ -291,12 +291,16 @@ __device__ __forceinline__ bool ev_wait_geq(const WaitCtx& c, const int* ctr, in
 }
 
 // Bounded mbarrier phase wait (same contract as ev_wait_geq).
+// After a short spin the waiter sleeps between polls, so a long wait (an idle
+// MMA or producer thread while the workers run a SIMT task) does not take
+// issue slots from the warps that share its SM sub-partition.
 __device__ __forceinline__ bool mbar_wait(const WaitCtx& c, uint64_t* bar, uint32_t parity,
                                        int where) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (it > 64) __nanosleep(it > 256 ? 256 : 64);
         if ((it & 15u) == 0) {
             if (aborted(c)) return false;
             if (globaltimer_ns() - t0 > c.timeout_ns) {

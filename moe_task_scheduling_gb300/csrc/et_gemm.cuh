@@ -14,11 +14,12 @@
 //   warp 1 lane 0   MMA issuer: per task, waits for free TMEM accumulator
 //                   slots, issues tcgen05.mma per full fill, frees each fill
 //                   with tcgen05.commit, commits the accumulator slots;
-//   warps 4..11     workers: the epilogue (tcgen05.ld from TMEM, stores,
+//   warps 2..9      workers: the epilogue (tcgen05.ld from TMEM, stores,
 //                   event releases) and every non-GEMM task; they sync among
-//                   themselves with named barrier 1.  Warp w reads TMEM lanes
-//                   32*(w%4) ..; warps 4..7 take the even 16-column chunks of
-//                   an accumulator, warps 8..11 the odd ones.
+//                   themselves with named barrier 1.  Warp w may only read TMEM
+//                   lanes 32*(w%4) ..; warps 2..5 take the even 16-column chunks
+//                   of an accumulator, warps 6..9 the odd ones, so each lane
+//                   quadrant is read by one warp of each half.
 //
 // The stage ring is byte-granular: a fill takes exactly the bytes of its
 // k-block (weights 16 or 32 KB, plus n * 128 bytes of activation rows), so a
@@ -37,7 +38,7 @@
 namespace et {
 
 constexpr int kTaskRing = 4;       // dynamic-queue tasks handed from producer to consumers
-constexpr int kWorkers = 256;      // warps 4..11
+constexpr int kWorkers = 256;      // warps 2..9
 constexpr int kWorkerBar = 1;      // named barrier id of the worker group
 constexpr int kSlots = 16;         // ring fills in flight at most (one barrier pair each)
 constexpr int kAccSlotCols = 256;  // TMEM columns per accumulator slot
@@ -152,6 +153,7 @@ __device__ __forceinline__ bool ring_lease_wait(Ctl* ctl, const ProdState& ps, c
     if (*ret < static_cast<int32_t>(ps.leases)) {
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t it = 1; *ret < static_cast<int32_t>(ps.leases); ++it) {
+            __nanosleep(it > 32 ? 256 : 32);  // (a lease lasts a whole SIMT task)
             if ((it & 15u) == 0) {
                 if (aborted(wc)) return false;
                 if (globaltimer_ns() - t0 > wc.timeout_ns) {

@@ -14,8 +14,8 @@ using bf16 = __nv_bfloat16;
 
 // ---------------------------------------------------------------- tiling constants
 
-constexpr int kThreads = 384;        // 12 warps: 0 TMA, 1 MMA/TMEM, 2-3 spare, 4-11 workers
-constexpr int kEpiWarp0 = 4;         // worker warp w reads TMEM lanes 32*(w%4) ..
+constexpr int kThreads = 320;        // 10 warps: 0 TMA, 1 MMA/TMEM, 2-9 workers
+constexpr int kEpiWarp0 = 2;         // worker warp w reads TMEM lanes 32*(w%4) ..
 constexpr int kTileM = 128;          // weight rows per tile (UMMA M)
 constexpr int kBlockK = 64;          // bf16 elements per k-block = one 128-byte swizzle row
 constexpr int kABytes = kTileM * kBlockK * 2;   // 16 KB weight tile
@@ -31,6 +31,8 @@ constexpr int kMoeNMax = 256;        // token rows per expert tile (UMMA N)
 constexpr int kRouterTile = 16;      // tokens per router tile (router and permute tasks)
 constexpr int kCombineTile = 16;     // most tokens per combine task
 constexpr int kMoeSplitRowsCap = 512;  // split the down projection only up to T*k rows
+constexpr int kGuSplitMax = 8;       // most K chunks of a gate/up tile (small batches)
+constexpr int kGuRowsCap = 128;      // K chunks x T*k rows of gate/up partials at most
 
 // split-K GEMM and MLP chain: up to 256 token rows per tile
 constexpr int kWideNMax = 256;
@@ -53,7 +55,8 @@ struct EtHeader {
     int32_t ev_ydone;       // expert output tiles complete
     int32_t ev_norm;        // RMSNorm tasks done (MLP chain)
     int32_t split;          // split of the down projection chosen this call
-    int32_t reserved[51];
+    int32_t gu_split;       // K chunks of a gate/up tile chosen this call
+    int32_t reserved[50];
 };
 static_assert(sizeof(EtHeader) == 256, "header is 256 bytes");
 
@@ -105,11 +108,14 @@ struct MoeArgs {
     int32_t* g_row0;      // [mt_max]: first permuted row of tile g
     int32_t* g_rows;      // [mt_max]: valid rows of tile g
     int32_t* g_n;         // [mt_max]: UMMA N of tile g
-    int4* queue;          // [q_max]
+    int4* queue;          // [q_max][2]: {type|split<<8|K chunks<<16, a, b, c}, {e, row0, rows, n}
     bf16* xp;             // [T_max*k, H]: x rows in permuted order
     bf16* h;              // [T_max*k, F]
     bf16* y;              // [T_max*k, H]
     float* partial;       // [kSplitMax, split_rows_cap, H]
+    float* gu_part;       // [2][gu_cap, F]: gate then up fp32 partials of K-split tiles
+    int32_t* ev_gu;       // [mt_max * F/128]: K chunks done per gate/up tile (self-resetting)
+    int gu_cap;           // rows of each gu_part half
     int mt_max, q_max, split_rows_cap, r_max;
     int wr_box;           // router-weight TMA box height (0: the weight is read in place)
     int b_wide;           // the 64-row activation maps are valid (enough rows)

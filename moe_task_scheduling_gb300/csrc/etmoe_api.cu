@@ -145,9 +145,9 @@ struct Carve {
 // ---------------------------------------------------------------- MoE layout
 
 struct MoeLayout {
-    int Tk, r_max, mt_max, q_max, split_cap;
-    size_t ev_h, ev_y, ev_tile, logits, hist, base, idx, gw, cnt, off, pos, perm, g_expert, g_row0,
-        g_rows, g_n, queue, xp, h, y, partial, total;
+    int Tk, r_max, mt_max, q_max, split_cap, gu_cap;
+    size_t ev_h, ev_y, ev_tile, ev_gu, logits, hist, base, idx, gw, cnt, off, pos, perm, g_expert,
+        g_row0, g_rows, g_n, queue, xp, h, y, partial, gu_part, total;
 };
 
 MoeLayout moe_layout(int T_max, int H, int F, int E, int k) {
@@ -156,12 +156,15 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k) {
     L.r_max = ceil_div(T_max, kRouterTile);
     L.mt_max = ceil_div(L.Tk, kMoeNMax) + E;
     const int FT = F / kTileM, HT = H / kTileM;
-    L.q_max = L.r_max * kRouterTile * k + L.mt_max * FT + L.mt_max * kSplitMax * HT + T_max;
+    L.q_max = L.r_max * kRouterTile * k + L.mt_max * FT * kGuSplitMax +
+              L.mt_max * kSplitMax * HT + T_max;
     L.split_cap = L.Tk < kMoeSplitRowsCap ? L.Tk : kMoeSplitRowsCap;
+    L.gu_cap = L.Tk * kGuSplitMax < kGuRowsCap ? L.Tk * kGuSplitMax : kGuRowsCap;
     Carve c;
     L.ev_h = c.take(sizeof(int) * L.mt_max * kSplitMax);
     L.ev_y = c.take(sizeof(int) * L.mt_max * HT);
     L.ev_tile = c.take(sizeof(int) * L.r_max);
+    L.ev_gu = c.take(sizeof(int) * L.mt_max * FT);
     L.logits = c.take(sizeof(float) * static_cast<size_t>(T_max) * E);
     L.hist = c.take(sizeof(int) * L.r_max * E);
     L.base = c.take(sizeof(int) * L.r_max * E);
@@ -175,11 +178,12 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k) {
     L.g_row0 = c.take(sizeof(int) * L.mt_max);
     L.g_rows = c.take(sizeof(int) * L.mt_max);
     L.g_n = c.take(sizeof(int) * L.mt_max);
-    L.queue = c.take(sizeof(int4) * L.q_max);
+    L.queue = c.take(sizeof(int4) * 2 * static_cast<size_t>(L.q_max));
     L.xp = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
     L.h = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * F, 1024);
     L.y = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
     L.partial = c.take(sizeof(float) * static_cast<size_t>(kSplitMax) * L.split_cap * H, 1024);
+    L.gu_part = c.take(sizeof(float) * 2 * static_cast<size_t>(L.gu_cap) * F, 1024);
     L.total = round_up(c.off, 256);
     return L;
 }
@@ -321,6 +325,9 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
     a.h = reinterpret_cast<bf16*>(ws + L.h);
     a.y = reinterpret_cast<bf16*>(ws + L.y);
     a.partial = reinterpret_cast<float*>(ws + L.partial);
+    a.gu_part = reinterpret_cast<float*>(ws + L.gu_part);
+    a.ev_gu = reinterpret_cast<int32_t*>(ws + L.ev_gu);
+    a.gu_cap = L.gu_cap;
     a.mt_max = L.mt_max;
     a.q_max = L.q_max;
     a.split_rows_cap = L.split_cap;

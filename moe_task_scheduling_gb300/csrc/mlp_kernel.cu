@@ -181,7 +181,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
-        const int q = (warp - kEpiWarp0) & 3, half = (warp - kEpiWarp0) >> 2;
+        const int q = warp & 3, half = (warp - kEpiWarp0) >> 2;  // TMEM lane quadrant, column half
         const int wtid = threadIdx.x - kEpiWarp0 * 32;
         const int H = p.H, F = p.F;
         EpiState es;

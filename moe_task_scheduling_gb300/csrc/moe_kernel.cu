@@ -6,20 +6,26 @@
 // small shared-memory ring; index order is a topological order and every
 // role of a CTA walks its tasks in that order, so every wait is on a task
 // that a resident CTA already holds -- the launch is cooperative):
-//   [0, R)      ROUTER r   fixed-order fp32 logits, top-k, gate weights and
-//                          a per-tile expert histogram;       releases ev_router
-//   R           SCAN       waits ev_router >= R (target computed from the
-//                          device token count), builds counts, offsets, the
-//                          expert row tiles and the split of the down
-//                          projection, then fills the queue:
-//   queue:      PERMUTE r  stable scatter of the tile's rows; releases ev_perm
-//               GATEUP g,f SwiGLU tile of expert row-tile g, F-tile f
-//                          (waits ev_perm >= R); releases ev_h[g][chunk(f)]
+//   [0, R*C)    ROUTER r,c fixed-order fp32 logits of router tile r for expert
+//                          chunk c; the chunk that completes the tile (counter
+//                          ev_tile[r]) takes the top-k, gate weights and the
+//                          tile's expert histogram; the tile that completes
+//                          ev_router (count R, computed from the device token
+//                          count) runs the SCAN: counts, offsets, the expert
+//                          row tiles and the split of the down projection,
+//                          then it fills the queue (and, with a single router
+//                          tile, permutes it inline):
+//   queue:      PERMUTE r,q stable scatter of part q of router tile r's rows;
+//                          releases ev_perm
+//               GATEUP g,f SwiGLU tile of expert row-tile g, F-tile f (waits
+//                          ev_perm >= permute parts); releases ev_h[g][chunk(f)]
 //               DOWN g,s,n down-projection tile, F-chunk s (waits
 //                          ev_h[g][s] >= F-tiles per chunk); with a split the
 //                          last arriver on ev_y[g][n] sums the fp32 partials
-//                          in chunk order; releases ev_ydone
-//               COMBINE c  waits ev_ydone >= tiles, out = sum_j w * y.
+//                          in chunk order; counts ev_ydone
+//               COMBINE c  waits ev_ydone >= tiles, out = sum_j w * y; a
+//                          single combine is run inline by the output tile
+//                          that completes ev_ydone.
 //
 // Sources: "Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
 // Kernels" (MoE routing gives data-dependent event counters that trigger
@@ -60,7 +66,52 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 
 __device__ __forceinline__ int wtid_() { return static_cast<int>(threadIdx.x) - kEpiWarp0 * 32; }
 
-constexpr int kMoeScratch = 18432;  // SIMT scratch: router logits [16][256] f32 + histogram
+// SIMT scratch (bytes): router logits [16][256] f32 at 0, the tile's expert
+// histogram at kHistOff, its top-k picks at kSelOff; the scan's arrays at 0
+// (after the logits are dead); permute rows at kPermOff.
+constexpr int kMoeScratch = 18432;
+constexpr int kHistOff = kRouterTile * 256 * 4;  // int [256]
+constexpr int kSelOff = kHistOff + 256 * 4;      // int [16 * 8]
+constexpr int kPermOff = 8192;                   // int [128] entries, int [128] rows
+
+// ------------------------------------------------------------------ trace
+
+// Optional per-task record (see et_opts.trace): {type | role << 8, a, b, cta,
+// t_begin, t_end}.  role 0 = producer (pop .. loads issued), 1 = workers
+// (task received .. done), 2 = CTA (start .. set-up done), 3 = CTA exit.
+__device__ __forceinline__ void trace_rec(const MoeArgs& p, int type, int role, int a, int b,
+                                          uint64_t t0, uint64_t t1) {
+    if (!p.trace) return;
+    const unsigned long long i = atomicAdd(reinterpret_cast<unsigned long long*>(p.trace), 1ull);
+    if (i >= static_cast<unsigned long long>(p.trace_cap)) return;
+    int4* r = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(p.trace) + 32 + i * 32);
+    r[0] = make_int4(type | (role << 8), a, b, static_cast<int>(blockIdx.x));
+    uint64_t* t = reinterpret_cast<uint64_t*>(r + 1);
+    t[0] = t0;
+    t[1] = t1;
+}
+
+// Sub-phase marks of the front end (worker thread 0, role 4): type 16 + id
+// spans [t_prev, now]; returns now.
+__device__ __forceinline__ uint64_t phase_mark(const MoeArgs& p, int id, uint64_t t_prev) {
+    if (!p.trace || wtid_() != 0) return t_prev;
+    __shared__ long long c_prev;  // SM cycles at the previous mark (field a: cycles in the phase)
+    const long long c = clock64();
+    const uint64_t t = globaltimer_ns();
+    trace_rec(p, 16 + id, 4, static_cast<int>(c - c_prev), 0, t_prev, t);
+    c_prev = clock64();
+    return globaltimer_ns();
+}
+
+struct TraceScope {  // records the workers' task on scope exit (worker thread 0)
+    const MoeArgs& p;
+    int type, a, b;
+    uint64_t t0;
+    bool on;
+    __device__ __forceinline__ ~TraceScope() {
+        if (on) trace_rec(p, type, 1, a, b, t0, globaltimer_ns());
+    }
+};
 
 // ------------------------------------------------------------------ ROUTER
 
@@ -98,8 +149,8 @@ __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, 
                                               float* out) {
     const int H = p.H, E = p.E;
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
-    constexpr int TB = 4;  // tokens per job
-    constexpr int U = 2;   // h-steps whose weights are loaded ahead of their fmas
+    constexpr int TB = 4;                // tokens per job
+    constexpr int U = EBW >= 4 ? 1 : 4;  // h-steps per block; the next block's loads fly meanwhile
     const int neb = ec / EBW, ntb = ceil_div(nt, TB);
     for (int job = warp; job < neb * ntb; job += kWorkers / 32) {
         const int tb = job / neb, j0 = (job % neb) * EBW;
@@ -111,20 +162,38 @@ __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, 
             for (int b = 0; b < EBW; ++b) acc[a][b] = 0.0f;
         const bf16* xr = xb + static_cast<size_t>(tb * TB) * H;
         const bf16* wj = wb + static_cast<size_t>((o + j0) >> 3) * blk + ((o + j0) & 7);
-        for (int h0 = 0; h0 < H; h0 += 32 * U) {  // H is a multiple of 128
-            float wv[U][EBW];
+        float wv[U][EBW], xv[U][TB];
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                load_w<EBW>(wj + static_cast<size_t>(h0 + 32 * u + lane) * rs, wv[u]);
+        for (int u = 0; u < U; ++u) {
+            const int h = 32 * u + lane;
+            load_w<EBW>(wj + static_cast<size_t>(h) * rs, wv[u]);
+#pragma unroll
+            for (int a = 0; a < TB; ++a)
+                xv[u][a] = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
+        }
+        for (int h0 = 0; h0 < H; h0 += 32 * U) {  // H is a multiple of 128
+            float wn[U][EBW], xn[U][TB];
+            const int hn = h0 + 32 * U < H ? h0 + 32 * U : h0;  // (the last block reloads itself)
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int h = h0 + 32 * u + lane;
+                const int h = hn + 32 * u + lane;
+                load_w<EBW>(wj + static_cast<size_t>(h) * rs, wn[u]);
 #pragma unroll
-                for (int a = 0; a < TB; ++a) {
-                    const float xv = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
+                for (int a = 0; a < TB; ++a)
+                    xn[u][a] = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
+            }
 #pragma unroll
-                    for (int b = 0; b < EBW; ++b) acc[a][b] = fmaf(xv, wv[u][b], acc[a][b]);
-                }
+            for (int u = 0; u < U; ++u)  // h = h0 + 32u + lane, ascending per lane
+#pragma unroll
+                for (int a = 0; a < TB; ++a)
+#pragma unroll
+                    for (int b = 0; b < EBW; ++b) acc[a][b] = fmaf(xv[u][a], wv[u][b], acc[a][b]);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+#pragma unroll
+                for (int b = 0; b < EBW; ++b) wv[u][b] = wn[u][b];
+#pragma unroll
+                for (int a = 0; a < TB; ++a) xv[u][a] = xn[u][a];
             }
         }
 #pragma unroll
@@ -162,6 +231,7 @@ struct MoePlan {
     int C, EC;     // router expert chunks per tile, experts per chunk
     int Q;         // permute parts per router tile
     int CT, NC;    // tokens per combine task; combine tasks
+    int NP;        // permute tasks in the queue (0: one router tile, permuted inline)
     bool stage;    // router tiles stage x and their weight chunk in the ring
 };
 
@@ -171,19 +241,21 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     P.T = T;
     P.R = ceil_div(T, kRouterTile);
     // Split the router's experts into chunks when there are few router tiles,
-    // so a small batch still spreads over many CTAs (each chunk >= 2 experts).
+    // so a small batch still spreads over many CTAs; a chunk keeps at least one
+    // expert per worker warp (or all of E).
     const int want = P.R > 0 ? max(1, G / P.R) : 1;
-    P.C = 1;
-    for (int d = 2; d <= E / 2; ++d)
-        if (E % d == 0 && d <= want) P.C = d;
+    const int ecmin = min(E, kWorkers / 32);
+    P.C = 1;  // chunk counts are powers of two (a cheap, uniform search)
+    for (int d = 2; d <= E; d <<= 1)
+        if (E % d == 0 && d <= want && E / d >= ecmin) P.C = d;
     // Staging: the smallest chunking (at least the one above) whose weight
     // blocks fit in the ring next to a full token tile.
     P.stage = false;
     if (p.wr_box > 0) {
         const uint32_t xpad = (static_cast<uint32_t>(min(T, kRouterTile) * H * 2) + 1023u) & ~1023u;
         const uint32_t hp = static_cast<uint32_t>(wr_rows_pad(H, p.wr_box));
-        for (int d = P.C; d <= E && !P.stage; ++d) {
-            if (E % d) continue;
+        for (int d = P.C; d <= E && !P.stage; d <<= 1) {
+            if (E % d) break;
             const int nb = wr_blocks(E / d);
             if (nb > 0 && xpad + static_cast<uint32_t>(nb) * hp * 16u <= ring_bytes) {
                 P.C = d;
@@ -195,8 +267,13 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     P.Q = P.R > 0 ? min(max(1, G / P.R), kRouterTile * k) : 1;
     P.CT = min(kCombineTile, max(1, ceil_div(T, G)));
     P.NC = ceil_div(T, P.CT);
+    P.NP = P.R > 1 ? P.R * P.Q : 0;
     return P;
 }
+
+__device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, uint8_t* smem,
+                                          const Ring& ring, Ctl* ctl, const WaitCtx& wc,
+                                          uint32_t& sphase, uint32_t& seq);
 
 // Logits of router tile r for expert chunk c.  With staging, the token rows
 // (one bulk copy) and the chunk's 8-expert weight blocks (TMA boxes) are
@@ -209,14 +286,16 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
                                             const CUtensorMap* tm_wr, const WaitCtx& wc,
                                             uint32_t& sphase, uint32_t& seq) {
     const int E = p.E, H = p.H, k = p.k;
-    float* lg = reinterpret_cast<float*>(smem);                                  // [16][E]
-    int* hs = reinterpret_cast<int*>(smem + kRouterTile * 256 * sizeof(float));  // [E]
+    float* lg = reinterpret_cast<float*>(smem);        // [16][E]
+    int* hs = reinterpret_cast<int*>(smem + kHistOff);  // [E]
+    int* sel_s = reinterpret_cast<int*>(smem + kSelOff);  // [nt * k]
     const int t0 = r * kRouterTile, nt = min(kRouterTile, P.T - t0);
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
     const int e0 = c * P.EC, ec = P.EC;
     const bf16* xb = p.x + static_cast<size_t>(t0) * H;
     const bf16* wb = p.wr + e0;
     int o = 0, rs = E, blk = 8;
+    uint64_t tm = p.trace ? globaltimer_ns() : 0;
     if (P.stage) {
         const uint32_t xbytes = static_cast<uint32_t>(nt * H * 2);
         const uint32_t xpad = (xbytes + 1023u) & ~1023u;
@@ -233,6 +312,7 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
                                 (eb0 + b) * 8, h0, pol);
         }
         if (!staging_wait(ctl, sphase, wc, seq)) return false;
+        tm = phase_mark(p, 0, tm);
         xb = reinterpret_cast<const bf16*>(ring.base);
         wb = reinterpret_cast<const bf16*>(wdst);
         o = e0 & 7;
@@ -241,17 +321,25 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     }
     float* out = P.C == 1 ? lg : p.logits + static_cast<size_t>(t0) * E;
     // the widest expert block (<= 8) that divides the chunk (and E when the
-    // weight is read in place, for aligned vector loads)
-    const int ew = P.stage ? ec : (ec | E);
-    if (ew % 8 == 0)
+    // weight is read in place, for aligned vector loads) and still gives every
+    // worker warp a job, else one expert per job
+    const int ew = P.stage ? ec : (ec | E), ntb = ceil_div(nt, 4);
+    int ebw = 1;
+    for (int c = 8; c > 1; c >>= 1)
+        if (ew % c == 0 && (ec / c) * ntb >= kWorkers / 32) {
+            ebw = c;
+            break;
+        }
+    if (ebw == 8)
         router_logits<8>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
-    else if (ew % 4 == 0)
+    else if (ebw == 4)
         router_logits<4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
-    else if (ew % 2 == 0)
+    else if (ebw == 2)
         router_logits<2>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
     else
         router_logits<1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
     worker_sync();
+    tm = phase_mark(p, 1, tm);
     if (P.C > 1) {  // tile reduction through the tile's event counter
         if (wtid_() == 0) {
             __threadfence();
@@ -263,10 +351,14 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
         for (int i = wtid_(); i < nt * E; i += kWorkers)
             lg[i] = __ldcg(p.logits + static_cast<size_t>(t0) * E + i);
         worker_sync();
+        tm = phase_mark(p, 2, tm);
     }
     for (int e = wtid_(); e < E; e += kWorkers) hs[e] = 0;
     worker_sync();
-    // top-k per token (warp per token): order (logit desc, index asc)
+    tm = phase_mark(p, 10, tm);
+    // top-k per token (warp per token): order (logit desc, index asc).  After
+    // round j every lane holds the j-th pick; lane j keeps it.  The rounds stay
+    // rolled: this code runs once per call, often with cold instruction caches.
     for (int tt = warp; tt < nt; tt += kWorkers / 32) {
         const float* L = lg + tt * E;
         float v[8];
@@ -276,11 +368,10 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
             v[i] = e < E ? L[e] : 0.0f;
         }
         uint32_t taken = 0;
-        float selL[8];
-        int selE[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j >= k) break;
+        float myL = 0.0f;
+        int myE = 0;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
             float bv = 0.0f;
             int be = 0x7fffffff;
 #pragma unroll
@@ -304,58 +395,72 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
                 }
             }
             if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            selL[j] = bv;
-            selE[j] = be;
+            if (lane == j) {
+                myL = bv;
+                myE = be;
+            }
         }
-        if (lane == 0) {
+        // gate weights over the k picks: exp(L_j - L_0) / sum_i exp(L_i - L_0)
+        const float L0 = __shfl_sync(0xffffffffu, myL, 0);
+        const float ex = lane < k ? expf(myL - L0) : 0.0f;
+        float z = ex;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        if (lane < k) {
             const int t = t0 + tt;
-            float ex[8], z = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (j >= k) break;
-                ex[j] = expf(selL[j] - selL[0]);
-                z += ex[j];
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (j >= k) break;
-                p.idx[static_cast<size_t>(t) * k + j] = selE[j];
-                p.gw[static_cast<size_t>(t) * k + j] = ex[j] / z;
-                atomicAdd(&hs[selE[j]], 1);
-            }
+            p.idx[static_cast<size_t>(t) * k + lane] = myE;
+            p.gw[static_cast<size_t>(t) * k + lane] = ex / z;
+            sel_s[tt * k + lane] = myE;
+            atomicAdd(&hs[myE], 1);
         }
     }
+    tm = phase_mark(p, 11, tm);
     worker_sync();
     for (int e = wtid_(); e < E; e += kWorkers) p.hist[static_cast<size_t>(r) * E + e] = hs[e];
     worker_sync();
+    tm = phase_mark(p, 3, tm);
+    // the last router tile to finish runs the scan: no task waits for it
     if (wtid_() == 0) {
         __threadfence();
-        red_release_add(&p.hdr->ev_router, 1);
+        ctl->flag = (atom_acq_rel_add(&p.hdr->ev_router, 1) == P.R - 1) ? 1 : 0;
     }
-    return true;
+    worker_sync();
+    tm = phase_mark(p, 4, tm);
+    if (!ctl->flag) return true;
+    return scan_task(p, P, smem, ring, ctl, wc, sphase, seq);  // hs, sel_s stay valid
 }
 
 // ------------------------------------------------------------------ SCAN
 
-// Counts, offsets, expert row tiles, split choice, and the task queue.  The
-// targets the later waits use (R permute tiles; F-tiles per chunk; the total
-// number of output tiles) are all derived here, on the device, from the
-// routing of this very call.  The per-tile histograms are staged in the ring
-// (many loads in flight) and scanned per expert there.
+__device__ __forceinline__ bool permute_rows(const MoeArgs& p, const MoePlan& P, int r, int i0,
+                                             int i1, uint8_t* smem, const Ring& ring, Ctl* ctl,
+                                             const WaitCtx& wc, uint32_t& sphase, uint32_t& seq,
+                                             const int* ie_src, const int* base_src, bool x_staged);
+
+// Counts, offsets, expert row tiles, split choice, and the task queue, run by
+// the last router tile to finish (every tile's histogram is visible through
+// the acquire-release count).  The targets the later waits use (permute
+// parts; F-tiles per chunk; the total number of output tiles) are all derived
+// here, on the device, from the routing of this very call.  With one router
+// tile the counts are this CTA's own histogram (smem), the permute is done
+// here from the staged x tile and the top-k picks in smem; otherwise the
+// per-tile histograms are staged in the ring and scanned per expert there.
 __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, uint8_t* smem,
-                                          const Ring& ring, Ctl* ctl, const WaitCtx& wc) {
+                                          const Ring& ring, Ctl* ctl, const WaitCtx& wc,
+                                          uint32_t& sphase, uint32_t& seq) {
     const int E = p.E, k = p.k, R = P.R, T = P.T;
-    if (wtid_() == 0) ctl->flag = ev_wait_geq(wc, &p.hdr->ev_router, R, kWhereRouter) ? 1 : 0;
-    worker_sync();
-    if (!ctl->flag) return false;
+    uint64_t tm = p.trace ? globaltimer_ns() : 0;
+    const int* hs1 = reinterpret_cast<const int*>(smem + kHistOff);  // R == 1: the counts
     int* cnt_s = reinterpret_cast<int*>(smem);  // [256]
     int* off_s = cnt_s + 256;                   // [257]
     int* n_s = off_s + 264;                     // [256]
     int* mtb_s = n_s + 256;                     // [257]
     const int RE = R * E;
-    const bool staged = static_cast<size_t>(RE) * 4 <= ring.bytes;
+    const bool staged = R > 1 && static_cast<size_t>(RE) * 4 <= ring.bytes;
     int* hs = reinterpret_cast<int*>(ring.base);
-    if (staged) {
+    if (R == 1) {
+        for (int e = wtid_(); e < E; e += kWorkers) cnt_s[e] = hs1[e];
+    } else if (staged) {
         const int n4 = RE / 4;
         const int4* src = reinterpret_cast<const int4*>(p.hist);
         int4* dst = reinterpret_cast<int4*>(hs);
@@ -392,34 +497,78 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         }
     }
     worker_sync();
+    tm = phase_mark(p, 5, tm);
     const int FT = p.F / kTileM, HT = p.H / kTileM;
-    if (wtid_() == 0) {
-        off_s[0] = 0;
-        mtb_s[0] = 0;
-        for (int e = 0; e < E; ++e) {
+    // offsets and row-tile starts: one warp, a block of experts per lane and a
+    // shuffle scan across lanes
+    if (wtid_() < 32) {
+        const int lane = wtid_(), per = ceil_div(E, 32);
+        int csum = 0, msum = 0;
+        for (int i = 0; i < per; ++i) {
+            const int e = lane * per + i;
+            if (e >= E) break;
             const int c = cnt_s[e];
-            off_s[e + 1] = off_s[e] + c;
             const int n = c == 0 ? 0 : min(kMoeNMax, (c + 15) / 16 * 16);
             n_s[e] = n;
-            mtb_s[e + 1] = mtb_s[e] + (c == 0 ? 0 : ceil_div(c, n));
+            csum += c;
+            msum += c == 0 ? 0 : ceil_div(c, n);
         }
+        int cx = csum, mx = msum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, cx, off), b = __shfl_up_sync(0xffffffffu, mx, off);
+            if (lane >= off) {
+                cx += a;
+                mx += b;
+            }
+        }
+        cx -= csum;  // exclusive prefixes
+        mx -= msum;
+        for (int i = 0; i < per; ++i) {
+            const int e = lane * per + i;
+            if (e >= E) break;
+            off_s[e] = cx;
+            mtb_s[e] = mx;
+            const int c = cnt_s[e];
+            cx += c;
+            mx += c == 0 ? 0 : ceil_div(c, n_s[e]);
+        }
+        if (lane == 31) {
+            off_s[E] = cx;
+            mtb_s[E] = mx;
+        }
+    }
+    worker_sync();
+    if (wtid_() == 0) {
         const int total_mt = mtb_s[E];
+        // split of the down projection: with few output tiles, the smallest
+        // divisor of FT (<= 8) that gives the grid about three tasks a CTA
         int S = 1;
-        if (T * k <= p.split_rows_cap && total_mt > 0 && total_mt * HT < p.num_ctas) {
+        if (T * k <= p.split_rows_cap && total_mt > 0 && total_mt * HT < 3 * p.num_ctas) {
             const int down = total_mt * HT;
             int best = 1;
             for (int d = 2; d <= kSplitMax; ++d) {
                 if (FT % d) continue;
+                if (p.F / kBlockK / d < 4) break;  // keep >= 4 k-blocks a chunk
                 best = d;
-                if (down * d >= p.num_ctas) break;
+                if (down * d >= 3 * p.num_ctas) break;
             }
             S = best;
         }
+        // K chunks of a gate/up tile: a small batch has few (weight-streaming)
+        // tiles, so they are cut along K until the grid has a few per CTA
+        int KC = 1;
+        const int nkb = p.H / kBlockK;
+        while (KC < kGuSplitMax && total_mt * FT * KC < 3 * p.num_ctas && nkb % (2 * KC) == 0 &&
+               nkb / (2 * KC) >= 8 && T * k * 2 * KC <= p.gu_cap)
+            KC *= 2;
         ctl->scratch[0] = total_mt;
         ctl->scratch[1] = S;
+        ctl->scratch[2] = KC;
     }
     worker_sync();
-    const int total_mt = ctl->scratch[0], S = ctl->scratch[1];
+    tm = phase_mark(p, 6, tm);
+    const int total_mt = ctl->scratch[0], S = ctl->scratch[1], KC = ctl->scratch[2];
     for (int e = wtid_(); e < E; e += kWorkers) {
         p.cnt[e] = cnt_s[e];
         p.off[e] = off_s[e];
@@ -432,37 +581,78 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
             p.g_n[g] = n;
         }
     }
-    if (staged) {
+    if (R == 1) {
+        for (int e = wtid_(); e < E; e += kWorkers) p.base[e] = off_s[e];
+    } else if (staged) {
         for (int i = wtid_(); i < RE; i += kWorkers) p.base[i] = hs[i] + off_s[i % E];
     } else {
         for (int i = wtid_(); i < RE; i += kWorkers) p.base[i] += off_s[i % E];
     }
-    const int n_perm = R * P.Q, n_gu = total_mt * FT, n_dn = total_mt * S * HT, n_cb = P.NC;
-    const int total = n_perm + n_gu + n_dn + n_cb;
+    tm = phase_mark(p, 7, tm);
+    // Queue: [permute parts][gate/up tiles, by chunk][down tiles, by chunk]
+    // [combine tasks].  A chunk c = (row tile g, F-chunk s) has u gate/up and
+    // d down tasks; every down task comes after the gate/up tasks it waits for.
+    // (Down tiles placed right behind their chunk's gate/up tiles were
+    // measured slower on decode and large batches: popped early, they stall
+    // their CTA on the dependency.)
+    const int u = (FT / S) * KC, d = HT, NCH = total_mt * S;
+    const int n_perm = P.NP, n_tiles = NCH * (u + d);
+    const int n_cb = P.NC > 1 ? P.NC : 0;  // a single combine runs inline (last down tile)
+    const int total = n_perm + n_tiles + n_cb;
     if (total > p.q_max) {  // cannot happen for a valid workspace; fail loudly
         if (wtid_() == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereQueue);
         return false;
     }
-    for (int q = wtid_(); q < total; q += kWorkers) {
-        int4 d;
-        if (q < n_perm) {
-            d = make_int4(kTaskPermute, q / P.Q, q % P.Q, 0);
-        } else if (q < n_perm + n_gu) {
-            const int i = q - n_perm;
-            d = make_int4(kTaskGateUp, i / FT, i % FT, 0);
-        } else if (q < n_perm + n_gu + n_dn) {
-            const int i = q - n_perm - n_gu;
-            const int g = i / (S * HT), rem = i % (S * HT);
-            d = make_int4(kTaskDown, g, rem / HT, rem % HT);
-        } else {
-            d = make_int4(kTaskCombine, q - n_perm - n_gu - n_dn, 0, 0);
+    const int flags = (S << 8) | (KC << 16);
+    int4* qd = p.queue;  // two int4 per entry: {type|flags, a, b, c}, {e, row0, rows, n}
+    for (int q = wtid_(); q < n_perm; q += kWorkers) {
+        qd[2 * q] = make_int4(kTaskPermute, q / P.Q, q % P.Q, 0);
+        qd[2 * q + 1] = make_int4(0, 0, 0, 0);
+    }
+    for (int q = wtid_(); q < n_cb; q += kWorkers) {
+        const int qq = n_perm + n_tiles + q;
+        qd[2 * qq] = make_int4(kTaskCombine, q, 0, 0);
+        qd[2 * qq + 1] = make_int4(0, 0, 0, 0);
+    }
+    {  // a warp per chunk, its lanes over the chunk's entries
+        const int warp = wtid_() >> 5, lane = wtid_() & 31;
+        for (int c = warp; c < NCH; c += kWorkers / 32) {
+            const int g = c / S, sc = c % S;
+            int e = 0;  // the expert of row tile g: mtb_s[e] <= g < mtb_s[e + 1]
+            for (int lo = 0, hi = E - 1; lo <= hi;) {
+                const int mid = (lo + hi) >> 1;
+                if (mtb_s[mid] <= g) {
+                    e = mid;
+                    lo = mid + 1;
+                } else {
+                    hi = mid - 1;
+                }
+            }
+            const int n = n_s[e], mt = g - mtb_s[e];
+            const int4 gi = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n), n);
+            const int gu0 = n_perm + c * u, dn0 = n_perm + NCH * u + c * d;
+            for (int r = lane; r < u; r += 32) {
+                qd[2 * (gu0 + r)] = make_int4(kTaskGateUp | flags, g, sc * (FT / S) + r / KC, r % KC);
+                qd[2 * (gu0 + r) + 1] = gi;
+            }
+            for (int r = lane; r < d; r += 32) {
+                qd[2 * (dn0 + r)] = make_int4(kTaskDown | flags, g, sc, r);
+                qd[2 * (dn0 + r) + 1] = gi;
+            }
         }
-        p.queue[q] = d;
     }
     worker_sync();
+    tm = phase_mark(p, 8, tm);
+    if (R == 1) {  // permute inline: base = off, x rows already staged if the router staged them
+        const int* sel = reinterpret_cast<const int*>(smem + kSelOff);
+        if (!permute_rows(p, P, 0, 0, T * k, smem, ring, ctl, wc, sphase, seq, sel, off_s, P.stage))
+            return false;
+    }
+    tm = phase_mark(p, 9, tm);
     if (wtid_() == 0) {
         p.hdr->total_mt = total_mt;
         p.hdr->split = S;
+        p.hdr->gu_split = KC;
         p.hdr->q_total = total;
         __threadfence();
         st_release(&p.hdr->q_ready, 1);
@@ -475,49 +665,74 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
 // Stable dispatch of router tile r: row (t, j) goes to off[e] + (rank of t
 // among this call's tokens routed to e), and its x row is copied there.  The
 // part's token rows come into the ring by bulk copy (the first batch is
-// issued before the ranks are computed, so it flies meanwhile); each routed
-// row then leaves with one bulk shared -> global copy.
-__device__ __forceinline__ bool permute_task(const MoeArgs& p, const MoePlan& P, int r, int part,
-                                             uint8_t* smem, const Ring& ring, Ctl* ctl,
-                                             const WaitCtx& wc, uint32_t& sphase, uint32_t& seq) {
+// issued before the ranks are computed, so it flies meanwhile) unless the
+// router already staged the whole tile there (x_staged); each routed row then
+// leaves with one bulk shared -> global copy.  ie_src / base_src: the tile's
+// top-k picks and first rows per expert when already in smem (else global).
+__device__ __forceinline__ bool permute_rows(const MoeArgs& p, const MoePlan& P, int r, int i0,
+                                             int i1, uint8_t* smem, const Ring& ring, Ctl* ctl,
+                                             const WaitCtx& wc, uint32_t& sphase, uint32_t& seq,
+                                             const int* ie_src, const int* base_src, bool x_staged) {
     const int k = p.k, E = p.E, H = p.H;
     const int t0 = r * kRouterTile, nt = min(kRouterTile, P.T - t0), nent = nt * k;
-    const int i0 = part * nent / P.Q, i1 = (part + 1) * nent / P.Q;  // this part's entries
-    int* ie = reinterpret_cast<int*>(smem);  // [128]
-    int* slot = ie + 128;                    // [128]
+    int* ie = reinterpret_cast<int*>(smem + kPermOff);  // [128]
+    int* slot = ie + 128;                               // [128]
     const int tl0 = i0 / k, ntok = i1 > i0 ? (i1 - 1) / k - tl0 + 1 : 0;
     const uint32_t rowb = static_cast<uint32_t>(H) * 2u;
-    const int per = static_cast<int>(ring.bytes / rowb);  // token rows per batch (>= k)
+    const int per = x_staged ? kRouterTile : static_cast<int>(ring.bytes / rowb);  // rows a batch
     auto issue = [&](int c0) {  // worker thread 0: token rows tl0 + c0 .. of the part
         const int nc = min(per, ntok - c0);
         mbar_arrive_expect_tx(&ctl->sbar, nc * rowb);
         bulk_g2s(ring.base, p.x + static_cast<size_t>(t0 + tl0 + c0) * H, nc * rowb, &ctl->sbar);
     };
-    if (ntok > 0 && wtid_() == 0) issue(0);
-    for (int i = wtid_(); i < nent; i += kWorkers)
-        ie[i] = __ldcg(p.idx + static_cast<size_t>(t0) * k + i);
-    worker_sync();
+    if (!x_staged && ntok > 0 && wtid_() == 0) issue(0);
+    const int* iv = ie_src;
+    if (!iv) {
+        for (int i = wtid_(); i < nent; i += kWorkers)
+            ie[i] = __ldcg(p.idx + static_cast<size_t>(t0) * k + i);
+        worker_sync();
+        iv = ie;
+    }
     for (int i = i0 + wtid_(); i < i1; i += kWorkers) {
-        const int e = ie[i], tl = i / k;
+        const int e = iv[i], tl = i / k;
         int rank = 0;  // tokens before t in this tile routed to e (each at most once)
-        for (int i2 = 0; i2 < tl * k; ++i2) rank += (ie[i2] == e);
-        const int pp = __ldcg(p.base + static_cast<size_t>(r) * E + e) + rank;
+        for (int i2 = 0; i2 < tl * k; ++i2) rank += (iv[i2] == e);
+        const int pp = (base_src ? base_src[e] : __ldcg(p.base + static_cast<size_t>(r) * E + e)) + rank;
         p.perm[pp] = t0 * k + i;
         p.pos[static_cast<size_t>(t0) * k + i] = pp;
         slot[i] = pp;
     }
-    for (int c0 = 0; c0 < ntok; c0 += per) {
-        if (c0 > 0 && wtid_() == 0) issue(c0);
-        if (!staging_wait(ctl, sphase, wc, seq)) return false;
-        const int ia = max(i0, (tl0 + c0) * k), ib = min(i1, (tl0 + c0 + per) * k);
-        for (int i = ia + wtid_(); i < ib; i += kWorkers)
-            bulk_s2g(p.xp + static_cast<size_t>(slot[i]) * H, ring.base + (i / k - tl0 - c0) * rowb,
-                     rowb);
-        bulk_commit_wait_all();  // rows written (and the batch read) before the next one
+    if (x_staged) {  // the tile's rows are at ring.base + (token - t0) * rowb
         worker_sync();
+        for (int i = i0 + wtid_(); i < i1; i += kWorkers)
+            bulk_s2g(p.xp + static_cast<size_t>(slot[i]) * H, ring.base + (i / k) * rowb, rowb);
+        bulk_commit_wait_all();
+        worker_sync();
+    } else {
+        for (int c0 = 0; c0 < ntok; c0 += per) {
+            if (c0 > 0 && wtid_() == 0) issue(c0);
+            if (!staging_wait(ctl, sphase, wc, seq)) return false;
+            const int ia = max(i0, (tl0 + c0) * k), ib = min(i1, (tl0 + c0 + per) * k);
+            for (int i = ia + wtid_(); i < ib; i += kWorkers)
+                bulk_s2g(p.xp + static_cast<size_t>(slot[i]) * H, ring.base + (i / k - tl0 - c0) * rowb,
+                         rowb);
+            bulk_commit_wait_all();  // rows written (and the batch read) before the next one
+            worker_sync();
+        }
     }
     if (ntok > 0) fence_proxy_async_global();  // the rows are read back by TMA
     worker_sync();
+    return true;
+}
+
+// Permute task: part `part` of router tile r (entries split evenly in Q parts).
+__device__ __forceinline__ bool permute_task(const MoeArgs& p, const MoePlan& P, int r, int part,
+                                             uint8_t* smem, const Ring& ring, Ctl* ctl,
+                                             const WaitCtx& wc, uint32_t& sphase, uint32_t& seq) {
+    const int t0 = r * kRouterTile, nent = min(kRouterTile, P.T - t0) * p.k;
+    if (!permute_rows(p, P, r, part * nent / P.Q, (part + 1) * nent / P.Q, smem, ring, ctl, wc,
+                      sphase, seq, nullptr, nullptr, false))
+        return false;
     if (wtid_() == 0) {
         __threadfence();
         red_release_add(&p.hdr->ev_perm, 1);
@@ -580,43 +795,38 @@ __device__ __forceinline__ bool combine_task(const MoeArgs& p, const MoePlan& P,
     return true;
 }
 
-// ------------------------------------------------------------------ trace
-
-// Optional per-task record (see et_opts.trace): {type | role << 8, a, b, cta,
-// t_begin, t_end}.  role 0 = producer (pop .. loads issued), 1 = workers
-// (task received .. done), 2 = CTA (start .. set-up done), 3 = CTA exit.
-__device__ __forceinline__ void trace_rec(const MoeArgs& p, int type, int role, int a, int b,
-                                          uint64_t t0, uint64_t t1) {
-    if (!p.trace) return;
-    const unsigned long long i = atomicAdd(reinterpret_cast<unsigned long long*>(p.trace), 1ull);
-    if (i >= static_cast<unsigned long long>(p.trace_cap)) return;
-    int4* r = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(p.trace) + 32 + i * 32);
-    r[0] = make_int4(type | (role << 8), a, b, static_cast<int>(blockIdx.x));
-    uint64_t* t = reinterpret_cast<uint64_t*>(r + 1);
-    t[0] = t0;
-    t[1] = t1;
-}
-
-struct TraceScope {  // records the workers' task on scope exit (worker thread 0)
-    const MoeArgs& p;
-    int type, a, b;
-    uint64_t t0;
-    bool on;
-    __device__ __forceinline__ ~TraceScope() {
-        if (on) trace_rec(p, type, 1, a, b, t0, globaltimer_ns());
+// All T (<= kCombineTile) tokens at once with plain loads: run by the last
+// output tile to finish, inside its epilogue, while the ring may hold fills.
+__device__ __forceinline__ void combine_inline(const MoeArgs& p, const MoePlan& P) {
+    const int H = p.H, k = p.k, vpr = H / 8;
+    for (int v = wtid_(); v < P.T * vpr; v += kWorkers) {
+        const int t = v / vpr, cc = v % vpr;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int j = 0; j < k; ++j) {  // fp32 sum in slot order j = 0 .. k-1
+            const float wj = __ldcg(p.gw + static_cast<size_t>(t) * k + j);
+            const int pp = __ldcg(p.pos + static_cast<size_t>(t) * k + j);
+            float yv[8];
+            unpack8(__ldcg(reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(pp) * H) + cc), yv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, yv[i], acc[i]);
+        }
+        reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * H)[cc] = pack8(acc);
     }
-};
+}
 
 // ------------------------------------------------------------------ queue pop
 
 // Producer thread: next task of this CTA (EXIT when the queue is exhausted or
-// the launch aborted).  GEMM tasks carry their expert row-tile parameters,
-// read after the acquire of the published queue.
-__device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc, const MoePlan& P) {
+// the launch aborted).  `claim` is a queue index taken ahead of time (or -1);
+// the published queue size is read once and kept in `q_total`.
+__device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc, const MoePlan& P,
+                                            int claim, int& q_total) {
     TaskMsg m{};
     m.type = kTaskExit;
-    if (aborted(wc)) return m;
-    const int i = atomicAdd(&p.hdr->q_head, 1);
+    if (aborted(wc) || P.R == 0) return m;  // T == 0: no task at all
+    const int i = claim >= 0 ? claim : atomicAdd(&p.hdr->q_head, 1);
     const int nr = P.R * P.C;
     if (i < nr) {
         m.type = kTaskRouter;
@@ -624,26 +834,21 @@ __device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc,
         m.b = i % P.C;
         return m;
     }
-    if (i == nr) {
-        m.type = kTaskScan;
-        return m;
+    const int j = i - nr;
+    if (q_total < 0) {
+        if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
+        q_total = ld_relaxed(&p.hdr->q_total);
     }
-    const int j = i - nr - 1;
-    if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
-    if (j >= ld_relaxed(&p.hdr->q_total)) return m;
-    const int4 d = __ldcg(p.queue + j);
-    m.type = d.x;
-    m.a = d.y;
-    m.b = d.z;
-    m.c = d.w;
-    if (d.x == kTaskGateUp || d.x == kTaskDown) {
-        const int g = d.y;
-        m.e = __ldcg(p.g_expert + g);
-        m.row0 = __ldcg(p.g_row0 + g);
-        m.rows = __ldcg(p.g_rows + g);
-        m.n = __ldcg(p.g_n + g);
-        m.type |= ld_relaxed(&p.hdr->split) << 8;
-    }
+    if (j >= q_total) return m;
+    const int4 d0 = __ldcg(p.queue + 2 * j), d1 = __ldcg(p.queue + 2 * j + 1);
+    m.type = d0.x;
+    m.a = d0.y;
+    m.b = d0.z;
+    m.c = d0.w;
+    m.e = d1.x;
+    m.row0 = d1.y;
+    m.rows = d1.z;
+    m.n = d1.w;
     return m;
 }
 
@@ -675,11 +880,13 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
     const int FT = p.F / kTileM, HT = p.H / kTileM;
 
     auto gemm_of = [&](const TaskMsg& m) {
-        const int type = m.type & 0xff, S = m.type >> 8;
-        if (type == kTaskGateUp)
+        const int type = m.type & 0xff, S = (m.type >> 8) & 0xff, KC = (m.type >> 16) & 0xff;
+        if (type == kTaskGateUp) {
+            const int nkb = p.H / kBlockK / KC;
             return GemmTask{&tm_wg, &tm_wu, &tm_xp, p.b_wide ? &tm_xp64 : nullptr,
-                            m.e * p.F + m.b * kTileM, m.row0, 0, p.H / kBlockK, m.n, m.b,
-                            &p.hdr->ev_perm, P.R * P.Q, kWherePerm};
+                            m.e * p.F + m.b * kTileM, m.row0, m.c * nkb, nkb, m.n, m.b,
+                            &p.hdr->ev_perm, P.NP, kWherePerm};
+        }
         const int fchunk = p.F / S;
         return GemmTask{&tm_wd, nullptr, &tm_h, p.b_wide ? &tm_h64 : nullptr,
                         m.e * p.H + m.c * kTileM, m.row0, m.b * (fchunk / kBlockK),
@@ -691,12 +898,14 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         if (lane == 0) {  // producer: pop, hand over, load
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
             ProdState ps;
+            int claim = -1, q_total = -1;
             for (int i = 0;; ++i) {
                 // a SIMT task still out on lease: take no further task before it
                 // is done, so SIMT work spreads over the CTAs that are free
                 if (!ring_lease_wait(ctl, ps, wc)) break;
                 const uint64_t tp = globaltimer_ns();
-                const TaskMsg m = pop_task(p, wc, P);
+                const TaskMsg m = pop_task(p, wc, P, claim, q_total);
+                claim = -1;
                 const int slot = i % kTaskRing;
                 if (!mbar_wait(wc, &ctl->tq_empty[slot], ((i / kTaskRing) & 1) ^ 1, kWhereQueue))
                     break;
@@ -705,6 +914,8 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 const int type = m.type & 0xff;
                 if (type == kTaskExit) break;
                 if (type == kTaskGateUp || type == kTaskDown) {
+                    // claim the next task now: the atomic's latency hides behind the loads
+                    claim = atomicAdd(&p.hdr->q_head, 1);
                     if (!produce_task(gemm_of(m), ring, ctl, ps, wc, pol_w, pol_b)) break;
                 } else {
                     ++ps.leases;  // a SIMT task holds the ring until the workers return it
@@ -729,7 +940,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {  // workers: epilogues and SIMT tasks
-        const int q = (warp - kEpiWarp0) & 3, half = (warp - kEpiWarp0) >> 2, wtid = wtid_();
+        const int q = warp & 3, half = (warp - kEpiWarp0) >> 2, wtid = wtid_();  // TMEM quadrant, column half
         const int H = p.H, F = p.F;
         EpiState es;
         uint32_t sphase = 0;
@@ -740,7 +951,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             const TaskMsg m = ctl->tq[slot];
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->tq_empty[slot]);
-            const int type = m.type & 0xff, S = m.type >> 8;
+            const int type = m.type & 0xff, S = (m.type >> 8) & 0xff, KC = (m.type >> 16) & 0xff;
             if (type == kTaskExit) break;
             TraceScope trace_scope{p, type, m.a, m.b, p.trace ? globaltimer_ns() : 0ull,
                                    p.trace != nullptr && wtid == 0};
@@ -748,8 +959,6 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 bool ok;
                 if (type == kTaskRouter)
                     ok = router_task(p, P, m.a, m.b, scratch, ring, ctl, &tm_wr, wc, sphase, es.seq);
-                else if (type == kTaskScan)
-                    ok = scan_task(p, P, scratch, ring, ctl, wc);
                 else if (type == kTaskPermute)
                     ok = permute_task(p, P, m.a, m.b, scratch, ring, ctl, wc, sphase, es.seq);
                 else
@@ -767,18 +976,52 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             if (type == kTaskGateUp) {
                 const int ft = m.b;
                 const int f = ft * kTileM + q * 32 + lane;
+                // K-split tile: fp32 partials of chunk m.c, rows of this call
+                const size_t tk = static_cast<size_t>(P.T) * p.k;
+                float* gpart = p.gu_part + (static_cast<size_t>(m.c) * tk) * F;
+                float* upart = gpart + static_cast<size_t>(p.gu_cap) * F;
                 for (int c0 = half * 16; c0 < n; c0 += 32) {
                     float gv[16], uv[16];
                     tmem_ld16(lane_base + c0, gv);
                     tmem_ld16(acc1 + lane_off + c0, uv);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        if (c0 + c < rows)
-                            p.h[static_cast<size_t>(row0 + c0 + c) * F + f] =
-                                __float2bfloat16_rn(silu_mul(gv[c], uv[c]));
+                    for (int c = 0; c < 16; ++c) {
+                        if (c0 + c >= rows) continue;
+                        const size_t r = static_cast<size_t>(row0 + c0 + c);
+                        if (KC == 1) {
+                            p.h[r * F + f] = __float2bfloat16_rn(silu_mul(gv[c], uv[c]));
+                        } else {
+                            gpart[r * F + f] = gv[c];
+                            upart[r * F + f] = uv[c];
+                        }
+                    }
                 }
                 epi_release(ctl, es, true, n);
+                if (KC > 1) {  // the chunk that completes the tile sums the partials
+                    int* ev = p.ev_gu + m.a * FT + ft;
+                    worker_sync();
+                    if (wtid == 0) {
+                        __threadfence();
+                        ctl->flag = (atom_acq_rel_add(ev, 1) == KC - 1) ? 1 : 0;
+                    }
+                    worker_sync();
+                    if (!ctl->flag) continue;
+                    if (wtid == 0) *ev = 0;  // every chunk arrived: reset for the next call
+                    const float* g0 = p.gu_part;
+                    const float* u0 = p.gu_part + static_cast<size_t>(p.gu_cap) * F;
+                    for (int j = wtid; j < rows * kTileM; j += kWorkers) {
+                        const size_t r = static_cast<size_t>(row0 + j / kTileM);
+                        const int ff = ft * kTileM + j % kTileM;
+                        float gs = 0.0f, us = 0.0f;  // chunk order kc = 0 .. KC-1
+                        for (int kc = 0; kc < KC; ++kc) {
+                            const size_t o = (static_cast<size_t>(kc) * tk + r) * F + ff;
+                            gs += __ldcg(g0 + o);
+                            us += __ldcg(u0 + o);
+                        }
+                        p.h[r * F + ff] = __float2bfloat16_rn(silu_mul(gs, us));
+                    }
+                }
                 fence_proxy_async_global();  // h is read back by TMA
                 worker_sync();
                 if (wtid == 0) {
@@ -830,9 +1073,19 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                     worker_sync();
                 }
             }
-            if (done && wtid == 0) {
-                __threadfence();
-                red_release_add(&p.hdr->ev_ydone, 1);
+            if (done && P.NC > 1) {
+                if (wtid == 0) {
+                    __threadfence();
+                    red_release_add(&p.hdr->ev_ydone, 1);
+                }
+            } else if (done) {  // one combine: the last output tile to finish runs it
+                if (wtid == 0) {
+                    __threadfence();
+                    const int target = ld_relaxed(&p.hdr->total_mt) * HT;
+                    ctl->flag = (atom_acq_rel_add(&p.hdr->ev_ydone, 1) == target - 1) ? 1 : 0;
+                }
+                worker_sync();
+                if (ctl->flag) combine_inline(p, P);
             }
         }
     }
@@ -855,6 +1108,10 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         const int mt = clean ? ld_relaxed(&p.hdr->total_mt) : p.mt_max;
         for (int i = threadIdx.x; i < mt * kSplitMax; i += kThreads) p.ev_h[i] = 0;
         for (int i = threadIdx.x; i < mt * HT; i += kThreads) p.ev_y[i] = 0;
+        if (!clean) {  // self-resetting counters an aborted launch may have left behind
+            for (int i = threadIdx.x; i < p.mt_max * FT; i += kThreads) p.ev_gu[i] = 0;
+            for (int i = threadIdx.x; i < p.r_max; i += kThreads) p.ev_tile[i] = 0;
+        }
         __syncthreads();
         if (threadIdx.x == 0) {
             EtHeader* hd = p.hdr;
@@ -866,6 +1123,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             hd->ev_perm = 0;
             hd->ev_ydone = 0;
             hd->split = 0;
+            hd->gu_split = 0;
             hd->abort = 0;
             __threadfence();
             hd->exit_count = 0;

@@ -85,7 +85,7 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
-        const int q = (warp - kEpiWarp0) & 3, half = (warp - kEpiWarp0) >> 2;
+        const int q = warp & 3, half = (warp - kEpiWarp0) >> 2;  // TMEM lane quadrant, column half
         const int wtid = threadIdx.x - kEpiWarp0 * 32;
         EpiState es;
         for (int task = blockIdx.x; task < total + n_red; task += gridDim.x) {
