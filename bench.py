@@ -407,6 +407,8 @@ def run_ours(args, world, rank, local):
         "wall_s_timed": round(wall, 3),
         "clocks": clk.summary(),
     }
+    if world == 1 and not args.no_per_op:
+        line["per_op_baseline"] = per_op_baseline(b, cfg)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(b, cfg, args)
     return line
@@ -427,6 +429,59 @@ def run_single(args, local):
     code, detail = b.etmoe.et_status(b.ws)
     return {"single": args.single, "workload": args.workload, "launches": args.warmup + 1,
             "status": [code, detail]}
+
+
+def per_op_layer(inp, cfg, T):
+    """The MoE layer as a sequence of plain PyTorch ops (one launch each, no
+    Triton), with a host sync for the per-expert counts: the same-GPU per-op
+    baseline.  Router in fp32, expert GEMMs in bf16 (cuBLAS)."""
+    x = inp["x"][:T]
+    logits = x.float() @ inp["wr"].float()
+    if inp["bias"] is not None:
+        logits = logits + inp["bias"]
+    w, idx = torch.topk(torch.softmax(logits, dim=-1), cfg.k, dim=-1)
+    w = (w / w.sum(dim=-1, keepdim=True)).reshape(-1)
+    flat = idx.reshape(-1)
+    order = torch.argsort(flat, stable=True)
+    counts = torch.bincount(flat, minlength=cfg.E).tolist()  # host sync
+    out = torch.zeros((T, cfg.H), dtype=torch.float32, device=x.device)
+    start = 0
+    for e, c in enumerate(counts):
+        if c == 0:
+            continue
+        rows = order[start:start + c]
+        start += c
+        tok = rows // cfg.k
+        xe = x[tok]
+        h = torch.nn.functional.silu(xe @ inp["wg"][e].T) * (xe @ inp["wu"][e].T)
+        y = h @ inp["wd"][e].T
+        out.index_add_(0, tok, y.float() * w[rows, None])
+    return out.to(torch.bfloat16), sum(1 for c in counts if c)
+
+
+def per_op_baseline(b, cfg, reps=3):
+    """Median CUDA-event time per T of per_op_layer over the same sweep (L2
+    flushed before each call, host sync included), as tokens/s."""
+    per_T, launches = {}, {}
+    for T in cfg.T_sweep:
+        ts = []
+        for i in range(reps + 1):
+            b.flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(b.stream)
+            _, touched = per_op_layer(b.inp, cfg, T)
+            e.record(b.stream)
+            e.synchronize()
+            if i:
+                ts.append(s.elapsed_time(e) / 1e3)
+        per_T[T] = statistics.median(ts)
+        launches[T] = 12 + 9 * touched  # router ops + per touched expert (gather, 3 GEMMs, act, add)
+    tot = sum(per_T.values())
+    return {"value": round(sum(cfg.T_sweep) / tot, 1), "unit": "tokens/s",
+            "kind": "same-GPU per-op PyTorch (router matmul/softmax/topk, stable argsort, "
+                    "bincount host sync, per-expert cuBLAS GEMMs, index_add_)",
+            "us_per_layer": {str(T): round(t * 1e6, 1) for T, t in per_T.items()},
+            "launches_per_layer": {str(T): n for T, n in launches.items()}}
 
 
 def cpu_baseline(b, cfg, args):
@@ -495,6 +550,7 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-op", action="store_true", help="skip the same-GPU per-op baseline")
     ap.add_argument("--single", type=int, default=None,
                     help="MoE workloads: run warmup+1 calls at this token count and exit "
                          "(for profiler captures; prints no bench line)")
