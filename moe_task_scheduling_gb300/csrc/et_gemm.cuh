@@ -89,6 +89,8 @@ struct GemmTask {
     const int* dep;          // wait *dep >= dep_target before activation loads
     int dep_target;
     int dep_where;
+    int a1_off = 0;          // row offset of the second weight tile (gate/up: 0, same rows of
+                             // another matrix; a 256-row down tile: 128, the next rows)
 };
 
 // One k-block: [A0 16K][A1 16K if gate/up][B n*128].  A fill packs several
@@ -203,7 +205,8 @@ __device__ __forceinline__ bool post_weights(const GemmTask& t, const Ring& R, C
         const int kx = (t.kb0 + kb + j) * kBlockK;
         tma_load_2d(dst + j * kABytes, t.a0, &ctl->full[slot], kx, t.a_row, pol_w);
         if (t.a1)
-            tma_load_2d(dst + (kp + j) * kABytes, t.a1, &ctl->full[slot], kx, t.a_row, pol_w);
+            tma_load_2d(dst + (kp + j) * kABytes, t.a1, &ctl->full[slot], kx, t.a_row + t.a1_off,
+                        pol_w);
     }
     ++ps.it;
     return true;

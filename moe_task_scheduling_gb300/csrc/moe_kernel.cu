@@ -595,7 +595,10 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     // (Down tiles placed right behind their chunk's gate/up tiles were
     // measured slower on decode and large batches: popped early, they stall
     // their CTA on the dependency.)
-    const int u = (FT / S) * KC, d = HT, NCH = total_mt * S;
+    // Wide down tiles (256 output columns: two weight boxes share one h tile, so
+    // each expert's h rows are read half as often) when tiles are tall.
+    const int wide = (S == 1 && HT % 2 == 0 && T * k >= 64 * total_mt) ? 1 : 0;
+    const int u = (FT / S) * KC, d = wide ? HT / 2 : HT, NCH = total_mt * S;
     const int n_perm = P.NP, n_tiles = NCH * (u + d);
     const int n_cb = P.NC > 1 ? P.NC : 0;  // a single combine runs inline (last down tile)
     const int total = n_perm + n_tiles + n_cb;
@@ -603,7 +606,7 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         if (wtid_() == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereQueue);
         return false;
     }
-    const int flags = (S << 8) | (KC << 16);
+    const int flags = (S << 8) | (KC << 16) | (wide << 24);
     int4* qd = p.queue;  // two int4 per entry: {type|flags, a, b, c}, {e, row0, rows, n}
     for (int q = wtid_(); q < n_perm; q += kWorkers) {
         qd[2 * q] = make_int4(kTaskPermute, q / P.Q, q % P.Q, 0);
@@ -635,7 +638,7 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
                 qd[2 * (gu0 + r)] = make_int4(kTaskGateUp | flags, g, sc * (FT / S) + r / KC, r % KC);
                 qd[2 * (gu0 + r) + 1] = gi;
             }
-            for (int r = lane; r < d; r += 32) {
+            for (int r = lane; r < d; r += 32) {  // r: output tile (of 128, or 256 if wide)
                 qd[2 * (dn0 + r)] = make_int4(kTaskDown | flags, g, sc, r);
                 qd[2 * (dn0 + r) + 1] = gi;
             }
@@ -887,11 +890,11 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                             m.e * p.F + m.b * kTileM, m.row0, m.c * nkb, nkb, m.n, m.b,
                             &p.hdr->ev_perm, P.NP, kWherePerm};
         }
-        const int fchunk = p.F / S;
-        return GemmTask{&tm_wd, nullptr, &tm_h, p.b_wide ? &tm_h64 : nullptr,
-                        m.e * p.H + m.c * kTileM, m.row0, m.b * (fchunk / kBlockK),
+        const int fchunk = p.F / S, wide = (m.type >> 24) & 1;
+        return GemmTask{&tm_wd, wide ? &tm_wd : nullptr, &tm_h, p.b_wide ? &tm_h64 : nullptr,
+                        m.e * p.H + m.c * (kTileM << wide), m.row0, m.b * (fchunk / kBlockK),
                         fchunk / kBlockK, m.n, m.c, &p.ev_h[m.a * kSplitMax + m.b], FT / S,
-                        kWhereH};
+                        kWhereH, wide ? kTileM : 0};
     };
 
     if (warp == 0) {
@@ -952,6 +955,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->tq_empty[slot]);
             const int type = m.type & 0xff, S = (m.type >> 8) & 0xff, KC = (m.type >> 16) & 0xff;
+            const int wide = (m.type >> 24) & 1;
             if (type == kTaskExit) break;
             TraceScope trace_scope{p, type, m.a, m.b, p.trace ? globaltimer_ns() : 0ull,
                                    p.trace != nullptr && wtid == 0};
@@ -967,7 +971,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 ring_return(ctl);
                 continue;
             }
-            const bool two = type == kTaskGateUp;
+            const bool two = type == kTaskGateUp || wide;
             uint32_t acc, acc1;
             if (!epi_acquire(ctl, es, two, m.n, tmem, wc, acc, acc1)) break;
             const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
@@ -1031,25 +1035,29 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 }
                 continue;
             }
-            // DOWN: y (S == 1) or an fp32 partial of F-chunk s
+            // DOWN: y (S == 1) or an fp32 partial of F-chunk s; a wide tile holds
+            // output columns [256 ht, +128) in acc and [256 ht + 128, +128) in acc1
             const int s = m.b, ht = m.c;
-            const int hh = ht * kTileM + q * 32 + lane;
             const int cap = p.split_rows_cap;
-            for (int c0 = half * 16; c0 < n; c0 += 32) {
-                float v[16];
-                tmem_ld16(lane_base + c0, v);
-                tmem_ld_wait();
+            for (int w = 0; w <= wide; ++w) {
+                const int hh = ht * (kTileM << wide) + w * kTileM + q * 32 + lane;
+                const uint32_t ab = (w ? acc1 : acc) + lane_off;
+                for (int c0 = half * 16; c0 < n; c0 += 32) {
+                    float v[16];
+                    tmem_ld16(ab + c0, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    if (c0 + c >= rows) continue;
-                    const size_t row = static_cast<size_t>(row0 + c0 + c);
-                    if (S == 1)
-                        p.y[row * H + hh] = __float2bfloat16_rn(v[c]);
-                    else
-                        p.partial[(static_cast<size_t>(s) * cap + row) * H + hh] = v[c];
+                    for (int c = 0; c < 16; ++c) {
+                        if (c0 + c >= rows) continue;
+                        const size_t row = static_cast<size_t>(row0 + c0 + c);
+                        if (S == 1)
+                            p.y[row * H + hh] = __float2bfloat16_rn(v[c]);
+                        else
+                            p.partial[(static_cast<size_t>(s) * cap + row) * H + hh] = v[c];
+                    }
                 }
             }
-            epi_release(ctl, es, false, n);
+            epi_release(ctl, es, two, n);
             fence_proxy_async_global();  // y is gathered by bulk copies in the combine
             worker_sync();  // the tile's stores are done
             bool done = true;
@@ -1073,16 +1081,18 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                     worker_sync();
                 }
             }
+            const int ntiles = 1 + wide;  // 128-column output tiles completed
             if (done && P.NC > 1) {
                 if (wtid == 0) {
                     __threadfence();
-                    red_release_add(&p.hdr->ev_ydone, 1);
+                    red_release_add(&p.hdr->ev_ydone, ntiles);
                 }
             } else if (done) {  // one combine: the last output tile to finish runs it
                 if (wtid == 0) {
                     __threadfence();
                     const int target = ld_relaxed(&p.hdr->total_mt) * HT;
-                    ctl->flag = (atom_acq_rel_add(&p.hdr->ev_ydone, 1) == target - 1) ? 1 : 0;
+                    ctl->flag =
+                        (atom_acq_rel_add(&p.hdr->ev_ydone, ntiles) == target - ntiles) ? 1 : 0;
                 }
                 worker_sync();
                 if (ctl->flag) combine_inline(p, P);

@@ -71,9 +71,11 @@ SMALL_MIX = wl.MoEConfig("mixtral_small", 3, H=512, F=384, E=8, k=2, T_sweep=(1,
 SMALL_FINE = wl.MoEConfig("fine_small", 4, H=256, F=256, E=128, k=8, T_sweep=(1, 7, 64, 300),
                           zipf_s=1.2)
 ODD = wl.MoEConfig("odd_experts", 5, H=128, F=640, E=12, k=3, T_sweep=(1, 2, 31, 77))
+# tall expert tiles, no down split: the 256-column (two weight box) down tiles
+WIDE = wl.MoEConfig("wide_down", 6, H=512, F=256, E=4, k=2, T_sweep=(300, 520))
 
 
-@pytest.mark.parametrize("cfg", [SMALL_MIX, SMALL_FINE, ODD], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [SMALL_MIX, SMALL_FINE, ODD, WIDE], ids=lambda c: c.name)
 @pytest.mark.parametrize("unit", [True, False])
 def test_small_shapes(cuda_lib, oracle, cfg, unit):
     inp = wl.moe_inputs(cfg, device="cpu", unit_scale=unit)
