@@ -143,14 +143,12 @@ __device__ __forceinline__ void load_w(const bf16* wrow, float (&w)[EBW]) {
 // and the staged one (blocks of 8 experts, 16 bytes a row).  EBW divides
 // both ec and 8, so a job's EBW columns never straddle a block.  Logit
 // (t, e0 + j) goes to out[t * E + e0 + j].
-template <int EBW>
+template <int EBW, int TB>
 __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, const bf16* wb,
                                               int o, int rs, int blk, int nt, int e0, int ec,
                                               float* out) {
     const int H = p.H, E = p.E;
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
-    constexpr int TB = 4;                // tokens per job
-    constexpr int U = EBW >= 4 ? 1 : 4;  // h-steps per block; the next block's loads fly meanwhile
     const int neb = ec / EBW, ntb = ceil_div(nt, TB);
     for (int job = warp; job < neb * ntb; job += kWorkers / 32) {
         const int tb = job / neb, j0 = (job % neb) * EBW;
@@ -162,38 +160,17 @@ __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, 
             for (int b = 0; b < EBW; ++b) acc[a][b] = 0.0f;
         const bf16* xr = xb + static_cast<size_t>(tb * TB) * H;
         const bf16* wj = wb + static_cast<size_t>((o + j0) >> 3) * blk + ((o + j0) & 7);
-        float wv[U][EBW], xv[U][TB];
+        // A plain loop, unrolled (the compiler hoists the loads of later steps):
+        // measured faster than explicit software pipelining here.
+#pragma unroll 2
+        for (int h = lane; h < H; h += 32) {  // h ascending per lane
+            float wv[EBW];
+            load_w<EBW>(wj + static_cast<size_t>(h) * rs, wv);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int h = 32 * u + lane;
-            load_w<EBW>(wj + static_cast<size_t>(h) * rs, wv[u]);
+            for (int a = 0; a < TB; ++a) {
+                const float xv = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
 #pragma unroll
-            for (int a = 0; a < TB; ++a)
-                xv[u][a] = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
-        }
-        for (int h0 = 0; h0 < H; h0 += 32 * U) {  // H is a multiple of 128
-            float wn[U][EBW], xn[U][TB];
-            const int hn = h0 + 32 * U < H ? h0 + 32 * U : h0;  // (the last block reloads itself)
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int h = hn + 32 * u + lane;
-                load_w<EBW>(wj + static_cast<size_t>(h) * rs, wn[u]);
-#pragma unroll
-                for (int a = 0; a < TB; ++a)
-                    xn[u][a] = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u)  // h = h0 + 32u + lane, ascending per lane
-#pragma unroll
-                for (int a = 0; a < TB; ++a)
-#pragma unroll
-                    for (int b = 0; b < EBW; ++b) acc[a][b] = fmaf(xv[u][a], wv[u][b], acc[a][b]);
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-#pragma unroll
-                for (int b = 0; b < EBW; ++b) wv[u][b] = wn[u][b];
-#pragma unroll
-                for (int a = 0; a < TB; ++a) xv[u][a] = xn[u][a];
+                for (int b = 0; b < EBW; ++b) acc[a][b] = fmaf(xv, wv[b], acc[a][b]);
             }
         }
 #pragma unroll
@@ -265,7 +242,9 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     }
     P.EC = E / P.C;
     P.Q = P.R > 0 ? min(max(1, G / P.R), kRouterTile * k) : 1;
-    P.CT = min(kCombineTile, max(1, ceil_div(T, G)));
+    // a combine task's k rows per token fit the ring in one staging batch
+    const int per_batch = max(1, static_cast<int>(ring_bytes / (static_cast<uint32_t>(k) * H * 2)));
+    P.CT = min(min(kCombineTile, per_batch), max(1, ceil_div(T, G)));
     P.NC = ceil_div(T, P.CT);
     P.NP = P.R > 1 ? P.R * P.Q : 0;
     return P;
@@ -323,21 +302,41 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     // the widest expert block (<= 8) that divides the chunk (and E when the
     // weight is read in place, for aligned vector loads) and still gives every
     // worker warp a job, else one expert per job
-    const int ew = P.stage ? ec : (ec | E), ntb = ceil_div(nt, 4);
-    int ebw = 1;
-    for (int c = 8; c > 1; c >>= 1)
-        if (ew % c == 0 && (ec / c) * ntb >= kWorkers / 32) {
-            ebw = c;
-            break;
+    // A job is TB tokens x EBW experts on one warp.  Shapes in order of FMAs per
+    // shared-memory wavefront (TB x EBW / (TB + 4)): 4x8, 8x4, 4x4, 8x2, 4x2,
+    // 8x1, 4x1 (8x8 measured no faster than 4x8 and would need 64 accumulators);
+    // the first that gives every worker warp a job wins (8-token jobs only when
+    // the tile has more than 4 tokens).  EBW divides the chunk (and E when the
+    // weight is read in place, for aligned vector loads).
+    const int ew = P.stage ? ec : (ec | E);
+    int tb = 4, ebw = 1;
+    {
+        const int cand[7][2] = {{4, 8}, {8, 4}, {4, 4}, {8, 2}, {4, 2}, {8, 1}, {4, 1}};
+        for (int i = 0; i < 7; ++i) {
+            const int ct = cand[i][0], ce = cand[i][1];
+            if ((ct == 8 && nt <= 4) || ew % ce != 0) continue;
+            tb = ct;
+            ebw = ce;
+            if ((ec / ce) * ceil_div(nt, ct) >= kWorkers / 32) break;
         }
-    if (ebw == 8)
-        router_logits<8>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
-    else if (ebw == 4)
-        router_logits<4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
-    else if (ebw == 2)
-        router_logits<2>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
-    else
-        router_logits<1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    }
+    if (tb == 8) {
+        if (ebw == 4)
+            router_logits<4, 8>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+        else if (ebw == 2)
+            router_logits<2, 8>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+        else
+            router_logits<1, 8>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    } else {
+        if (ebw == 8)
+            router_logits<8, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+        else if (ebw == 4)
+            router_logits<4, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+        else if (ebw == 2)
+            router_logits<2, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+        else
+            router_logits<1, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    }
     worker_sync();
     tm = phase_mark(p, 1, tm);
     if (P.C > 1) {  // tile reduction through the tile's event counter
@@ -356,48 +355,43 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     for (int e = wtid_(); e < E; e += kWorkers) hs[e] = 0;
     worker_sync();
     tm = phase_mark(p, 10, tm);
-    // top-k per token (warp per token): order (logit desc, index asc).  After
-    // round j every lane holds the j-th pick; lane j keeps it.  The rounds stay
-    // rolled: this code runs once per call, often with cold instruction caches.
+    // top-k per token (warp per token): order (logit desc, index asc).  A round
+    // takes each lane's best remaining entry, then the warp's largest key and,
+    // among lanes holding it, the smallest expert index (two redux
+    // instructions).  The key is an order-preserving map of the fp32 logit,
+    // with -0.0 taken as +0.0 (they tie).  After round j every lane holds the
+    // j-th pick; lane j keeps it.  The rounds stay rolled: this code runs once
+    // per call, often with cold instruction caches.
     for (int tt = warp; tt < nt; tt += kWorkers / 32) {
         const float* L = lg + tt * E;
-        float v[8];
+        uint32_t key[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int e = lane + 32 * i;
-            v[i] = e < E ? L[e] : 0.0f;
+            const float v = e < E ? L[e] : 0.0f;
+            const uint32_t b = __float_as_uint(v == 0.0f ? 0.0f : v);
+            key[i] = e < E ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
         }
         uint32_t taken = 0;
         float myL = 0.0f;
         int myE = 0;
 #pragma unroll 1
         for (int j = 0; j < k; ++j) {
-            float bv = 0.0f;
-            int be = 0x7fffffff;
+            uint32_t bk = 0, bi = 0xffffffffu;  // this lane's best remaining (key, index)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u)) {
-                    if (be == 0x7fffffff || v[i] > bv || (v[i] == bv && e < be)) {
-                        bv = v[i];
-                        be = e;
-                    }
+                if (e < E && !((taken >> i) & 1u) && (bi == 0xffffffffu || key[i] > bk)) {
+                    bk = key[i];
+                    bi = static_cast<uint32_t>(e);
                 }
             }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (oe != 0x7fffffff &&
-                    (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, bi == 0xffffffffu ? 0u : bk);
+            const uint32_t win = __reduce_min_sync(0xffffffffu, (bi != 0xffffffffu && bk == kmax) ? bi : 0xffffffffu);
+            if ((win & 31u) == static_cast<uint32_t>(lane)) taken |= 1u << (win >> 5);
             if (lane == j) {
-                myL = bv;
-                myE = be;
+                myE = static_cast<int>(win);
+                myL = L[win];
             }
         }
         // gate weights over the k picks: exp(L_j - L_0) / sum_i exp(L_i - L_0)
@@ -717,8 +711,8 @@ __device__ __forceinline__ bool permute_rows(const MoeArgs& p, const MoePlan& P,
             if (!staging_wait(ctl, sphase, wc, seq)) return false;
             const int ia = max(i0, (tl0 + c0) * k), ib = min(i1, (tl0 + c0 + per) * k);
             for (int i = ia + wtid_(); i < ib; i += kWorkers)
-                bulk_s2g(p.xp + static_cast<size_t>(slot[i]) * H, ring.base + (i / k - tl0 - c0) * rowb,
-                         rowb);
+                bulk_s2g(p.xp + static_cast<size_t>(slot[i]) * H,
+                         ring.base + (i / k - tl0 - c0) * rowb, rowb);
             bulk_commit_wait_all();  // rows written (and the batch read) before the next one
             worker_sync();
         }
