@@ -149,6 +149,23 @@ def moe_inputs(cfg: MoEConfig, device="cpu", T_max: Optional[int] = None, unit_s
     return dict(x=x, wr=wr, bias=bias, wg=wg, wu=wu, wd=wd)
 
 
+def block_extra_inputs(cfg: MoEConfig, Fs: int, device="cpu", unit_scale=False):
+    """The fused MoE block's extra inputs (drawn from their own seed, so the
+    layer's inputs are unchanged): gamma [H] = 1 + N(0, 0.02), the shared
+    expert sg/su [Fs,H], sd [H,Fs] (None when Fs = 0), eps = 1e-5."""
+    g = _gen(device, 2000 + cfg.index)
+    H = cfg.H
+    gamma = (1.0 + torch.randn((H,), generator=g, device=device) * WEIGHT_STD).to(torch.bfloat16)
+    sg = su = sd = None
+    if Fs:
+        sh = 1.0 / math.sqrt(H) if unit_scale else WEIGHT_STD
+        sf = 1.0 / math.sqrt(Fs) if unit_scale else WEIGHT_STD
+        sg = _randn_bf16((Fs, H), sh, g, device, chunk_rows=1024)
+        su = _randn_bf16((Fs, H), sh, g, device, chunk_rows=1024)
+        sd = _randn_bf16((H, Fs), sf, g, device, chunk_rows=512)
+    return dict(gamma=gamma, sg=sg, su=su, sd=sd, eps=1e-5)
+
+
 def splitk_inputs(cfg: SplitKConfig, device="cpu", M_max: Optional[int] = None, unit_scale=False):
     """X [M_max,K], Wt [N,K] (the weight stored transposed, K contiguous), bf16."""
     M_max = M_max or cfg.M_max

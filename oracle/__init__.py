@@ -64,6 +64,10 @@ def lib():
         L.eto_mlp_chain.argtypes = [_u16p, _u16p, ctypes.c_float, _u16p, _u16p, _u16p,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int,
                                     _u16p, ctypes.c_int]
+        L.eto_moe_block.restype = ctypes.c_int
+        L.eto_moe_block.argtypes = [_u16p, _u16p, ctypes.c_float, _u16p, _f32p, _u16p, _u16p,
+                                    _u16p, _u16p, _u16p, _u16p] + [ctypes.c_int] * 6 + \
+            [_i32p, ctypes.c_int, _u16p, _u16p, _i32p, _f32p, _i32p, _i32p, ctypes.c_int]
         _lib = L
     return _lib
 
@@ -215,3 +219,31 @@ def mlp_chain(x, gamma, eps, wg, wu, wd, rows=None, nthreads=None):
     if rc != 0:
         raise ValueError("oracle mlp_chain rejected its arguments")
     return out
+
+
+def moe_block(x, gamma, eps, wr, bias, wg, wu, wd, sg=None, su=None, sd=None, k=2, tokens=None,
+              nthreads=None):
+    """The fused MoE block (R14): routing of x_hat = RMSNorm(x) * gamma, routed
+    experts and the shared expert (sg/su [Fs,H], sd [H,Fs]; None = none) on x_hat,
+    out = bf16(x + sum_j w_j y_j + y_s).  Returns dict(out, xhat, idx, w, cnt, perm)."""
+    x, gamma, wr, wg, wu, wd = _u16(x), _u16(gamma), _u16(wr), _u16(wg), _u16(wu), _u16(wd)
+    T, H = x.shape
+    E, F, _ = wg.shape
+    Fs = 0 if sg is None else _u16(sg).shape[0]
+    sg, su, sd = (_u16(sg), _u16(su), _u16(sd)) if Fs else (None, None, None)
+    tok = _i32(tokens)
+    out = np.empty((len(tok) if tok is not None else T, H), dtype=np.uint16)
+    res = dict(xhat=np.empty((T, H), np.uint16), idx=np.empty((T, k), np.int32),
+               w=np.empty((T, k), np.float32), cnt=np.empty(E, np.int32),
+               perm=np.empty(T * k, np.int32))
+    b = _f32(bias)
+    rc = lib().eto_moe_block(
+        _p(x, _u16p), _p(gamma, _u16p), float(eps), _p(wr, _u16p), _p(b, _f32p), _p(wg, _u16p),
+        _p(wu, _u16p), _p(wd, _u16p), _p(sg, _u16p), _p(su, _u16p), _p(sd, _u16p), T, H, F, Fs, E,
+        k, _p(tok, _i32p), 0 if tok is None else len(tok), _p(out, _u16p), _p(res["xhat"], _u16p),
+        _p(res["idx"], _i32p), _p(res["w"], _f32p), _p(res["cnt"], _i32p), _p(res["perm"], _i32p),
+        nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle moe_block rejected its arguments")
+    res["out"] = out
+    return res

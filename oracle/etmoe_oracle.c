@@ -31,6 +31,9 @@
  *     h and y are stored as bf16 (rounded once from the fp64 value).
  *  R5 The combine is out[t] = bf16(sum_j w[t,j] y[t,j]).
  *  R6 RMSNorm: xhat = bf16(x / sqrt(mean(x^2) + eps) * gamma), no residual.
+ *  R14 The fused MoE block routes x_hat = R6(x), runs the routed experts and
+ *     a shared SwiGLU expert on x_hat and adds the residual:
+ *     out = bf16(x + sum_j w_j y_j + y_s), one rounding of the fp64 sum.
  *
  * Precision: every accumulation except R1 is fp64; each stored bf16 value is
  * rounded once, round-to-nearest-even, from the fp64 value.
@@ -424,4 +427,94 @@ int eto_mlp_chain(const uint16_t* x, const uint16_t* gamma, float eps, const uin
     mlp_ctx c = {x, gamma, wg, wu, wd, (double)eps, rows, H, F, out};
     parallel_for(rows ? n_rows : B, nthreads, mlp_rows, &c);
     return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* The fused MoE block (R14): x_hat = RMSNorm(x) * gamma, routed MoE   */
+/* on x_hat, a shared SwiGLU expert on x_hat, residual add:            */
+/*   out = bf16( x + sum_j w_j * y_j + y_s )  (fp64 sum, one rounding)  */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t *x, *xhat, *wg, *wu, *wd, *sg, *su, *sd;
+    const int32_t* idx;
+    const float* w;
+    const int32_t* tokens;
+    int H, F, Fs, k;
+    uint16_t* out;
+} block_ctx;
+
+static void block_rows(void* c, int64_t b, int64_t e) {
+    block_ctx* m = (block_ctx*)c;
+    uint16_t* y = (uint16_t*)malloc((size_t)m->H * sizeof(uint16_t));
+    double* acc = (double*)malloc((size_t)m->H * sizeof(double));
+    const int64_t ew = (int64_t)m->F * m->H;
+    for (int64_t r = b; r < e; ++r) {
+        int64_t t = m->tokens ? m->tokens[r] : r;
+        const uint16_t* xh = m->xhat + t * m->H;
+        for (int i = 0; i < m->H; ++i) acc[i] = bf(m->x[t * m->H + i]);  /* the residual */
+        for (int j = 0; j < m->k; ++j) {                                  /* routed experts */
+            int ex = m->idx[t * m->k + j];
+            eto_swiglu_row(xh, m->wg + ex * ew, m->wu + ex * ew, m->wd + ex * ew, m->H, m->F,
+                           NULL, y);
+            double wj = (double)m->w[t * m->k + j];
+            for (int i = 0; i < m->H; ++i) acc[i] += wj * bf(y[i]);
+        }
+        if (m->Fs > 0) {                                                  /* shared expert */
+            eto_swiglu_row(xh, m->sg, m->su, m->sd, m->H, m->Fs, NULL, y);
+            for (int i = 0; i < m->H; ++i) acc[i] += bf(y[i]);
+        }
+        for (int i = 0; i < m->H; ++i) m->out[r * m->H + i] = eto_f64_to_bf16(acc[i]);
+    }
+    free(acc);
+    free(y);
+}
+
+typedef struct {
+    const uint16_t *x, *gamma;
+    double eps;
+    int H;
+    uint16_t* xhat;
+} norm_ctx;
+
+static void norm_rows_range(void* c, int64_t b, int64_t e) {
+    norm_ctx* m = (norm_ctx*)c;
+    for (int64_t r = b; r < e; ++r)
+        eto_rmsnorm_row(m->x + r * m->H, m->gamma, m->eps, m->H, m->xhat + r * m->H);
+}
+
+/* x bf16 [T,H]; gamma bf16 [H]; routed weights as in eto_moe_layer; shared
+ * expert sg, su bf16 [Fs,H], sd bf16 [H,Fs] (Fs = 0: none, pointers ignored).
+ * Routing outputs as in eto_moe_layer (routing of x_hat); out bf16 one row per
+ * produced token (tokens[] or all T); xhat_out bf16 [T,H] or NULL. */
+int eto_moe_block(const uint16_t* x, const uint16_t* gamma, float eps, const uint16_t* wr,
+                  const float* bias, const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
+                  const uint16_t* sg, const uint16_t* su, const uint16_t* sd, int T, int H, int F,
+                  int Fs, int E, int k, const int32_t* tokens, int n_tokens, uint16_t* out,
+                  uint16_t* xhat_out, int32_t* idx_out, float* w_out, int32_t* cnt_out,
+                  int32_t* perm_out, int nthreads) {
+    if (T < 0 || H <= 0 || F <= 0 || Fs < 0 || E <= 0 || k <= 0 || k > E) return 1;
+    uint16_t* xhat = (uint16_t*)malloc(((size_t)T * H + 1) * sizeof(uint16_t));
+    norm_ctx nc = {x, gamma, (double)eps, H, xhat};
+    parallel_for(T, nthreads, norm_rows_range, &nc);
+    int32_t* idx = (int32_t*)malloc(((size_t)T * k + 1) * sizeof(int32_t));
+    float* w = (float*)malloc(((size_t)T * k + 1) * sizeof(float));
+    int32_t* cnt = (int32_t*)malloc((size_t)E * sizeof(int32_t));
+    int32_t* off = (int32_t*)malloc((size_t)(E + 1) * sizeof(int32_t));
+    int rc = eto_moe_layer(xhat, wr, bias, wg, wu, wd, T, H, F, E, k, NULL, 0, NULL, idx, w, cnt,
+                           off, perm_out, NULL, nthreads);
+    if (rc == 0 && out) {
+        block_ctx c = {x, xhat, wg, wu, wd, sg, su, sd, idx, w, tokens, H, F, Fs, k, out};
+        parallel_for(tokens ? n_tokens : T, nthreads, block_rows, &c);
+    }
+    if (idx_out) memcpy(idx_out, idx, (size_t)T * k * sizeof(int32_t));
+    if (w_out) memcpy(w_out, w, (size_t)T * k * sizeof(float));
+    if (cnt_out) memcpy(cnt_out, cnt, (size_t)E * sizeof(int32_t));
+    if (xhat_out) memcpy(xhat_out, xhat, (size_t)T * H * sizeof(uint16_t));
+    free(off);
+    free(cnt);
+    free(w);
+    free(idx);
+    free(xhat);
+    return rc;
 }

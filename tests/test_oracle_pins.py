@@ -390,3 +390,80 @@ def test_mlp_chain_is_norm_then_single_expert(oracle):
     xnb = wl.bits(xn.to(torch.float32).to(torch.bfloat16))
     _, y_ref = _torch_swiglu_f64(xnb, wg, wu, wd)
     np.testing.assert_allclose(to_f64(out), y_ref.numpy(), rtol=2.0 ** -5, atol=2e-2)
+
+
+# --------------------------------------------------------------------- the fused MoE block (R14)
+
+def _block_case(unit, Fs=96, seed_cfg=wl.TINY):
+    inp = wl.moe_inputs(seed_cfg, unit_scale=unit)
+    ex = wl.block_extra_inputs(seed_cfg, Fs, unit_scale=unit)
+    b = {k: wl.bits(v) for k, v in inp.items() if v is not None and v.dtype == torch.bfloat16}
+    b.update({k: wl.bits(v) for k, v in ex.items() if isinstance(v, torch.Tensor)})
+    return b, ex["eps"], seed_cfg
+
+
+def test_block_zero_weights_is_residual(oracle):
+    """Every expert weight zero (routed and shared): out = x exactly."""
+    b, eps, cfg = _block_case(True)
+    z = {n: np.zeros_like(b[n]) for n in ("wg", "wu", "wd", "sg", "su", "sd")}
+    r = oracle.moe_block(b["x"], b["gamma"], eps, b["wr"], None, z["wg"], z["wu"], z["wd"],
+                         z["sg"], z["su"], z["sd"], k=cfg.k)
+    assert np.array_equal(r["out"], b["x"])
+
+
+def test_block_routing_is_layer_routing_of_normed_x(oracle):
+    b, eps, cfg = _block_case(True)
+    r = oracle.moe_block(b["x"], b["gamma"], eps, b["wr"], None, b["wg"], b["wu"], b["wd"],
+                         b["sg"], b["su"], b["sd"], k=cfg.k)
+    xh = np.stack([oracle.rmsnorm_row(b["x"][t], b["gamma"], eps) for t in range(b["x"].shape[0])])
+    assert np.array_equal(r["xhat"], xh)
+    lay = oracle.moe_layer(xh, b["wr"], None, b["wg"], b["wu"], b["wd"], k=cfg.k, want_out=False)
+    for n in ("idx", "w", "cnt", "perm"):
+        assert np.array_equal(r[n], lay[n]), n
+
+
+def test_block_shared_only_is_residual_plus_mlp_chain(oracle):
+    """Routed down weights zero: out = bf16(x + y_s), y_s = the RMSNorm -> SwiGLU
+    chain of x (two bf16 values add exactly in fp64: one rounding, bit-exact)."""
+    b, eps, cfg = _block_case(True)
+    r = oracle.moe_block(b["x"], b["gamma"], eps, b["wr"], None, b["wg"], b["wu"],
+                         np.zeros_like(b["wd"]), b["sg"], b["su"], b["sd"], k=cfg.k)
+    ys = oracle.mlp_chain(b["x"], b["gamma"], eps, b["sg"], b["su"], b["sd"])
+    ref = np.array([[oracle.f64_to_bf16(a + c) for a, c in zip(xr, yr)]
+                    for xr, yr in zip(to_f64(b["x"]), to_f64(ys))], dtype=np.uint16)
+    assert np.array_equal(r["out"], ref)
+
+
+def test_block_vs_torch_f64(oracle):
+    """The whole block restated with torch fp64 primitives (RMSNorm, full softmax
+    + lexsort top-k on the oracle's fixed-order logits, per-token SwiGLU of the
+    routed and the shared expert, residual)."""
+    b, eps, cfg = _block_case(True)
+    r = oracle.moe_block(b["x"], b["gamma"], eps, b["wr"], None, b["wg"], b["wu"], b["wd"],
+                         b["sg"], b["su"], b["sd"], k=cfg.k)
+    xd = torch.from_numpy(to_f64(b["x"]))
+    xn = xd * torch.rsqrt((xd * xd).mean(1, keepdim=True) + eps) * torch.from_numpy(to_f64(b["gamma"]))
+    xnb = wl.bits(xn.to(torch.float32).to(torch.bfloat16))
+    L = oracle.router_logits(xnb, b["wr"]).astype(np.float64)
+    T = xd.shape[0]
+    out_ref = to_f64(b["x"]).copy()
+    for t in range(T):
+        order = np.lexsort((np.arange(cfg.E), -L[t]))[:cfg.k]
+        assert r["idx"][t].tolist() == order.tolist()
+        p = np.exp(L[t] - L[t].max())
+        wsel = p[order] / p[order].sum()
+        for j, e in enumerate(order):
+            _, y = _torch_swiglu_f64(xnb[t:t + 1], b["wg"][e], b["wu"][e], b["wd"][e])
+            out_ref[t] += wsel[j] * y[0].numpy()
+        _, ys = _torch_swiglu_f64(xnb[t:t + 1], b["sg"], b["su"], b["sd"])
+        out_ref[t] += ys[0].numpy()
+    np.testing.assert_allclose(to_f64(r["out"]), out_ref, rtol=2.0 ** -6, atol=2e-2)
+
+
+def test_block_token_subset_equals_full(oracle):
+    b, eps, cfg = _block_case(False)
+    args = (b["x"], b["gamma"], eps, b["wr"], None, b["wg"], b["wu"], b["wd"], b["sg"], b["su"],
+            b["sd"])
+    full = oracle.moe_block(*args, k=cfg.k)
+    sub = oracle.moe_block(*args, k=cfg.k, tokens=[5, 0, 15])
+    assert np.array_equal(sub["out"], full["out"][[5, 0, 15]])
