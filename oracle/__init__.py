@@ -64,6 +64,8 @@ def lib():
         L.eto_mlp_chain.argtypes = [_u16p, _u16p, ctypes.c_float, _u16p, _u16p, _u16p,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int,
                                     _u16p, ctypes.c_int]
+        L.eto_rmsnorm_row_f32.restype = None
+        L.eto_rmsnorm_row_f32.argtypes = [_u16p, _u16p, ctypes.c_float, ctypes.c_int, _u16p]
         L.eto_moe_block.restype = ctypes.c_int
         L.eto_moe_block.argtypes = [_u16p, _u16p, ctypes.c_float, _u16p, _f32p, _u16p, _u16p,
                                     _u16p, _u16p, _u16p, _u16p] + [ctypes.c_int] * 6 + \
@@ -203,6 +205,15 @@ def rmsnorm_row(x, gamma, eps):
     x, gamma = _u16(x), _u16(gamma)
     out = np.empty_like(x)
     lib().eto_rmsnorm_row(_p(x, _u16p), _p(gamma, _u16p), float(eps), x.shape[0], _p(out, _u16p))
+    return out
+
+
+def rmsnorm_row_f32(x, gamma, eps):
+    """R15: the block's fp32 fixed-order RMSNorm of one row."""
+    x, gamma = _u16(x), _u16(gamma)
+    out = np.empty_like(x)
+    lib().eto_rmsnorm_row_f32(_p(x, _u16p), _p(gamma, _u16p), float(eps), x.shape[0],
+                              _p(out, _u16p))
     return out
 
 

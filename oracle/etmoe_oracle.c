@@ -31,9 +31,13 @@
  *     h and y are stored as bf16 (rounded once from the fp64 value).
  *  R5 The combine is out[t] = bf16(sum_j w[t,j] y[t,j]).
  *  R6 RMSNorm: xhat = bf16(x / sqrt(mean(x^2) + eps) * gamma), no residual.
- *  R14 The fused MoE block routes x_hat = R6(x), runs the routed experts and
- *     a shared SwiGLU expert on x_hat and adds the residual:
+ *  R14 The fused MoE block routes x_hat, runs the routed experts and a shared
+ *     SwiGLU expert on x_hat and adds the residual:
  *     out = bf16(x + sum_j w_j y_j + y_s), one rounding of the fp64 sum.
+ *  R15 In the block, x_hat feeds the (bit-exact) routing, so it is defined in
+ *     fp32 with one fixed order, like R1: ss = sum of x^2 in the R1 order
+ *     (32 strided partial sums, halving tree), r = 1 / sqrt(ss / H + eps),
+ *     x_hat = bf16((x * r) * gamma); each step one IEEE-rounded fp32 op.
  *
  * Precision: every accumulation except R1 is fp64; each stored bf16 value is
  * rounded once, round-to-nearest-even, from the fp64 value.
@@ -435,6 +439,24 @@ int eto_mlp_chain(const uint16_t* x, const uint16_t* gamma, float eps, const uin
 /*   out = bf16( x + sum_j w_j * y_j + y_s )  (fp64 sum, one rounding)  */
 /* ------------------------------------------------------------------ */
 
+/* R15: x_hat of one row in fp32, fixed order.  x^2 is exact in fp32 (a bf16
+ * square), so the R1 sum of x*x is the fixed-order sum of squares. */
+void eto_rmsnorm_row_f32(const uint16_t* x, const uint16_t* gamma, float eps, int H,
+                         uint16_t* xhat) {
+    float p[32];
+    for (int l = 0; l < 32; ++l) p[l] = 0.0f;
+    for (int h = 0; h < H; ++h) {
+        const float v = eto_bf16_to_f32(x[h]);
+        p[h % 32] = p[h % 32] + v * v;
+    }
+    for (int off = 16; off >= 1; off /= 2)
+        for (int l = 0; l < off; ++l) p[l] = p[l] + p[l + off];
+    const float ms = p[0] / (float)H;
+    const float r = 1.0f / sqrtf(ms + eps);
+    for (int h = 0; h < H; ++h)
+        xhat[h] = eto_f32_to_bf16((eto_bf16_to_f32(x[h]) * r) * eto_bf16_to_f32(gamma[h]));
+}
+
 typedef struct {
     const uint16_t *x, *xhat, *wg, *wu, *wd, *sg, *su, *sd;
     const int32_t* idx;
@@ -472,7 +494,7 @@ static void block_rows(void* c, int64_t b, int64_t e) {
 
 typedef struct {
     const uint16_t *x, *gamma;
-    double eps;
+    float eps;
     int H;
     uint16_t* xhat;
 } norm_ctx;
@@ -480,7 +502,7 @@ typedef struct {
 static void norm_rows_range(void* c, int64_t b, int64_t e) {
     norm_ctx* m = (norm_ctx*)c;
     for (int64_t r = b; r < e; ++r)
-        eto_rmsnorm_row(m->x + r * m->H, m->gamma, m->eps, m->H, m->xhat + r * m->H);
+        eto_rmsnorm_row_f32(m->x + r * m->H, m->gamma, m->eps, m->H, m->xhat + r * m->H);
 }
 
 /* x bf16 [T,H]; gamma bf16 [H]; routed weights as in eto_moe_layer; shared
@@ -495,7 +517,7 @@ int eto_moe_block(const uint16_t* x, const uint16_t* gamma, float eps, const uin
                   int32_t* perm_out, int nthreads) {
     if (T < 0 || H <= 0 || F <= 0 || Fs < 0 || E <= 0 || k <= 0 || k > E) return 1;
     uint16_t* xhat = (uint16_t*)malloc(((size_t)T * H + 1) * sizeof(uint16_t));
-    norm_ctx nc = {x, gamma, (double)eps, H, xhat};
+    norm_ctx nc = {x, gamma, eps, H, xhat};
     parallel_for(T, nthreads, norm_rows_range, &nc);
     int32_t* idx = (int32_t*)malloc(((size_t)T * k + 1) * sizeof(int32_t));
     float* w = (float*)malloc(((size_t)T * k + 1) * sizeof(float));

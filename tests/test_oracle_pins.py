@@ -415,20 +415,22 @@ def test_block_routing_is_layer_routing_of_normed_x(oracle):
     b, eps, cfg = _block_case(True)
     r = oracle.moe_block(b["x"], b["gamma"], eps, b["wr"], None, b["wg"], b["wu"], b["wd"],
                          b["sg"], b["su"], b["sd"], k=cfg.k)
-    xh = np.stack([oracle.rmsnorm_row(b["x"][t], b["gamma"], eps) for t in range(b["x"].shape[0])])
+    xh = np.stack([oracle.rmsnorm_row_f32(b["x"][t], b["gamma"], eps)
+                   for t in range(b["x"].shape[0])])
     assert np.array_equal(r["xhat"], xh)
     lay = oracle.moe_layer(xh, b["wr"], None, b["wg"], b["wu"], b["wd"], k=cfg.k, want_out=False)
     for n in ("idx", "w", "cnt", "perm"):
         assert np.array_equal(r[n], lay[n]), n
 
 
-def test_block_shared_only_is_residual_plus_mlp_chain(oracle):
-    """Routed down weights zero: out = bf16(x + y_s), y_s = the RMSNorm -> SwiGLU
-    chain of x (two bf16 values add exactly in fp64: one rounding, bit-exact)."""
+def test_block_shared_only_is_residual_plus_shared_expert(oracle):
+    """Routed down weights zero: out = bf16(x + y_s), y_s = the shared SwiGLU of
+    x_hat (two bf16 values add exactly in fp64: one rounding, bit-exact)."""
     b, eps, cfg = _block_case(True)
     r = oracle.moe_block(b["x"], b["gamma"], eps, b["wr"], None, b["wg"], b["wu"],
                          np.zeros_like(b["wd"]), b["sg"], b["su"], b["sd"], k=cfg.k)
-    ys = oracle.mlp_chain(b["x"], b["gamma"], eps, b["sg"], b["su"], b["sd"])
+    ys = np.stack([oracle.swiglu_row(r["xhat"][t], b["sg"], b["su"], b["sd"])[1]
+                   for t in range(b["x"].shape[0])])
     ref = np.array([[oracle.f64_to_bf16(a + c) for a, c in zip(xr, yr)]
                     for xr, yr in zip(to_f64(b["x"]), to_f64(ys))], dtype=np.uint16)
     assert np.array_equal(r["out"], ref)
@@ -467,3 +469,35 @@ def test_block_token_subset_equals_full(oracle):
     full = oracle.moe_block(*args, k=cfg.k)
     sub = oracle.moe_block(*args, k=cfg.k, tokens=[5, 0, 15])
     assert np.array_equal(sub["out"], full["out"][[5, 0, 15]])
+
+
+def test_block_rmsnorm_f32_sum_is_router_order(oracle):
+    """R15's sum of squares uses R1's order: for any row, ss equals the (golden-
+    pinned) fixed-order router logit of x against itself, so x_hat must equal
+    the formula evaluated from that logit."""
+    rng = np.random.default_rng(21)
+    H = 512
+    for _ in range(5):
+        xb = bf16_bits_of(rng.normal(0, 1, H) * np.exp(rng.normal(0, 2, H)))
+        gb = bf16_bits_of(1.0 + rng.normal(0, 0.02, H))
+        ss = np.float32(oracle.router_logit_one(xb, xb))
+        r = np.float32(1.0) / np.sqrt(np.float32(ss / np.float32(H)) + np.float32(1e-5))
+        ref = bf16_bits_of(((to_f64(xb).astype(np.float32) * r) * to_f64(gb).astype(np.float32)))
+        assert np.array_equal(oracle.rmsnorm_row_f32(xb, gb, 1e-5), ref)
+
+
+def test_block_rmsnorm_f32_close_to_f64_and_constant_row(oracle):
+    rng = np.random.default_rng(22)
+    H = 1024
+    gb = bf16_bits_of(1.0 + rng.normal(0, 0.02, H))
+    for _ in range(5):
+        xb = bf16_bits_of(rng.normal(0, 1, H))
+        a = to_f64(oracle.rmsnorm_row_f32(xb, gb, 1e-5))
+        d = to_f64(oracle.rmsnorm_row(xb, gb, 1e-5))
+        assert np.all(np.abs(a - d) <= 2.0 ** -7 * np.abs(d) + 1e-30)
+    # constant row c: ss = H c^2 exactly, x_hat = bf16(c / sqrt(c^2 + eps) * gamma)
+    c = 0.5
+    xb = bf16_bits_of(np.full(H, c))
+    got = to_f64(oracle.rmsnorm_row_f32(xb, gb, 1e-5))
+    want = c / math.sqrt(c * c + 1e-5) * to_f64(gb)
+    assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want))
