@@ -8,7 +8,11 @@ L2 is flushed (256 MiB write) before every layer call and each call is timed
 with CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload mixtral|fine|splitk|mlp]
+                  [--workload mixtral|fine|mixtral_block|fine_block|splitk|mlp]
+
+The *_block workloads run the fused MoE block (RMSNorm, routed experts, a
+shared expert of width 2F on the fine-grained shape, residual add) over the
+same sweep; they print their own line with their own metric.
 
 Prints ONE JSON line on rank 0.  With N > 1 (torchrun, one process per GPU)
 every rank runs an independent replica of the same sweep ("replicas only":
@@ -37,6 +41,11 @@ import torch  # noqa: E402
 from moe_task_scheduling_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "MoE-layer tokens/s over the token-count sweep (us/layer per T; % of HBM roofline)"
+METRIC_BLOCK = ("Fused MoE-block tokens/s over the token-count sweep (RMSNorm + routed and shared "
+                "experts + residual; us/block per T; % of HBM roofline)")
+# workload -> (configuration, shared-expert width; None = the plain layer)
+MOE_WORKLOADS = {"mixtral": (wl.MIXTRAL, None), "fine": (wl.FINE, None),
+                 "mixtral_block": (wl.MIXTRAL, 0), "fine_block": (wl.FINE, 2 * wl.FINE.F)}
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["et_device.cuh", "et_gemm.cuh", "et_layout.h", "moe_kernel.cu",
                   "splitk_kernel.cu", "mlp_kernel.cu", "etmoe_api.cu"]
@@ -172,37 +181,54 @@ def sum_over_ranks(x, world, device):
 
 # ----------------------------------------------------------------------------- MoE workload
 
-def moe_algorithmic_bytes(cfg, T, n_touched):
+def moe_algorithmic_bytes(cfg, T, n_touched, Fs=None):
     """Bytes the layer must move: the expert weights it touches (gate, up, down),
-    the router weight, x in and out.  h, y and split-K partials are the
+    the router weight, x in and out (the block adds gamma and the shared
+    expert's weights).  h, y, x_hat and split-K partials are the
     implementation's own traffic and are not counted."""
-    return (n_touched * 3 * cfg.F * cfg.H * 2 + cfg.H * cfg.E * 2 + 2 * T * cfg.H * 2
-            + (cfg.E * 4 if cfg.zipf_s is not None else 0))
+    b = (n_touched * 3 * cfg.F * cfg.H * 2 + cfg.H * cfg.E * 2 + 2 * T * cfg.H * 2
+         + (cfg.E * 4 if cfg.zipf_s is not None else 0))
+    if Fs is not None:
+        b += cfg.H * 2 + 3 * Fs * cfg.H * 2
+    return b
 
 
-def moe_algorithmic_flops(cfg, T):
-    return 2 * T * cfg.k * 3 * cfg.H * cfg.F + 2 * T * cfg.H * cfg.E
+def moe_algorithmic_flops(cfg, T, Fs=None):
+    return 2 * T * cfg.k * 3 * cfg.H * cfg.F + 2 * T * cfg.H * cfg.E + 2 * T * 3 * cfg.H * (Fs or 0)
 
 
 class MoeBench:
-    def __init__(self, cfg, device):
+    """The MoE layer (Fs None) or the fused block with a shared expert of width Fs."""
+
+    def __init__(self, cfg, device, Fs=None):
         from moe_task_scheduling_gb300 import etmoe
         self.etmoe = etmoe
         etmoe.load()
         self.cfg = cfg
+        self.Fs = Fs
         self.dev = device
         self.inp = wl.moe_inputs(cfg, device=device)
+        self.blk = wl.block_extra_inputs(cfg, Fs, device=device) if Fs is not None else None
         T_max = cfg.T_max
         self.out = torch.empty((T_max, cfg.H), dtype=torch.bfloat16, device=device)
         self.cnt = torch.zeros((cfg.E,), dtype=torch.int32, device=device)
-        self.ws = etmoe.alloc_workspace(etmoe.et_moe_workspace_bytes(T_max, cfg.H, cfg.F, cfg.E,
-                                                                     cfg.k), device=device)
+        nbytes = (etmoe.et_moe_workspace_bytes(T_max, cfg.H, cfg.F, cfg.E, cfg.k) if Fs is None else
+                  etmoe.et_moe_block_workspace_bytes(T_max, cfg.H, cfg.F, cfg.E, cfg.k, Fs))
+        self.ws = etmoe.alloc_workspace(nbytes, device=device)
         self.d_T = torch.zeros(1, dtype=torch.int32, device=device)
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
         self.stream = torch.cuda.current_stream(device)
 
     def call(self, x=None, out=None):
         i = self.inp
+        if self.blk is not None:
+            b = self.blk
+            self.etmoe.et_moe_block(x if x is not None else i["x"], b["gamma"], b["eps"], i["wr"],
+                                    i["bias"], i["wg"], i["wu"], i["wd"], b["sg"], b["su"], b["sd"],
+                                    out if out is not None else self.out, k=self.cfg.k, T=0,
+                                    d_T=self.d_T, T_max=self.cfg.T_max, expert_counts=self.cnt,
+                                    workspace=self.ws, stream=self.stream)
+            return
         self.etmoe.et_moe_layer(x if x is not None else i["x"], i["wr"], i["bias"], i["wg"], i["wu"],
                                 i["wd"], out if out is not None else self.out, k=self.cfg.k, T=0,
                                 d_T=self.d_T, T_max=self.cfg.T_max, expert_counts=self.cnt,
@@ -336,8 +362,8 @@ def run_ours(args, world, rank, local):
     assert torch.cuda.is_available(), "bench.py needs a CUDA GPU for --impl ours"
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    cfg = {"mixtral": wl.MIXTRAL, "fine": wl.FINE}[args.workload]
-    b = MoeBench(cfg, device)
+    cfg, Fs = MOE_WORKLOADS[args.workload]
+    b = MoeBench(cfg, device, Fs)
     touched = b.touched()
     for _ in range(args.warmup):
         b.step()
@@ -369,17 +395,20 @@ def run_ours(args, world, rank, local):
     bytes_total = 0.0
     for T in cfg.T_sweep:
         t = statistics.median(per_T[T])
-        by = moe_algorithmic_bytes(cfg, T, touched[T])
+        by = moe_algorithmic_bytes(cfg, T, touched[T], Fs)
         bytes_total += by * len(per_T[T])
         sweep.append({"T": T, "us_per_layer": round(t * 1e6, 2), "us_min": round(min(per_T[T]) * 1e6, 2),
                       "tokens_per_s": round(T / t, 1), "experts_touched": touched[T],
                       "hbm_frac": round(by / t / 1e9 / pk["hbm_gbs"], 4),
-                      "tensor_frac": round(moe_algorithmic_flops(cfg, T) / t / 1e12 / pk["bf16_tflops"], 4)})
+                      "tensor_frac": round(moe_algorithmic_flops(cfg, T, Fs) / t / 1e12 /
+                                           pk["bf16_tflops"], 4)})
     achieved = bytes_total / kernel_time / 1e9
     traffic = profiled_traffic(args.workload)
     n_launch = args.steps * len(cfg.T_sweep)
+    what = "MoE layer" if Fs is None else (f"fused MoE block (shared expert Fs={Fs})" if Fs else
+                                           "fused MoE block (no shared expert)")
     line = {
-        "metric": METRIC,
+        "metric": METRIC if Fs is None else METRIC_BLOCK,
         "value": round(tok_all / t_max, 1),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -391,8 +420,9 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) bf16 weights and activations)",
-        "config": {"workload": f"{cfg.name} MoE layer, T sweep {list(cfg.T_sweep)}",
+        "config": {"workload": f"{cfg.name} {what}, T sweep {list(cfg.T_sweep)}",
                    "H": cfg.H, "F": cfg.F, "E": cfg.E, "k": cfg.k,
+                   **({} if Fs is None else {"Fs": Fs, "eps": 1e-5}),
                    "l2": "flushed (256 MiB write) before every layer call",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "symbolic_T": "one compiled kernel, T read from device memory"},
@@ -419,8 +449,8 @@ def run_single(args, local):
     flushed before each): the launch an ncu capture selects with -s/-c."""
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    cfg = {"mixtral": wl.MIXTRAL, "fine": wl.FINE}[args.workload]
-    b = MoeBench(cfg, device)
+    cfg, Fs = MOE_WORKLOADS[args.workload]
+    b = MoeBench(cfg, device, Fs)
     b.d_T.fill_(args.single)
     for _ in range(args.warmup + 1):
         b.flush.zero_()
@@ -431,11 +461,17 @@ def run_single(args, local):
             "status": [code, detail]}
 
 
-def per_op_layer(inp, cfg, T):
+def per_op_layer(inp, cfg, T, blk=None):
     """The MoE layer as a sequence of plain PyTorch ops (one launch each, no
     Triton), with a host sync for the per-expert counts: the same-GPU per-op
-    baseline.  Router in fp32, expert GEMMs in bf16 (cuBLAS)."""
-    x = inp["x"][:T]
+    baseline.  Router in fp32, expert GEMMs in bf16 (cuBLAS).  With `blk` the
+    fused block: RMSNorm first, the shared expert and the residual after."""
+    x0 = inp["x"][:T]
+    x = x0
+    if blk is not None:
+        xf = x0.float()
+        x = (xf * torch.rsqrt(xf.square().mean(-1, keepdim=True) + blk["eps"]) *
+             blk["gamma"].float()).to(torch.bfloat16)
     logits = x.float() @ inp["wr"].float()
     if inp["bias"] is not None:
         logits = logits + inp["bias"]
@@ -456,6 +492,11 @@ def per_op_layer(inp, cfg, T):
         h = torch.nn.functional.silu(xe @ inp["wg"][e].T) * (xe @ inp["wu"][e].T)
         y = h @ inp["wd"][e].T
         out.index_add_(0, tok, y.float() * w[rows, None])
+    if blk is not None:
+        out += x0.float()
+        if blk["sg"] is not None:
+            hs = torch.nn.functional.silu(x @ blk["sg"].T) * (x @ blk["su"].T)
+            out += (hs @ blk["sd"].T).float()
     return out.to(torch.bfloat16), sum(1 for c in counts if c)
 
 
@@ -469,17 +510,21 @@ def per_op_baseline(b, cfg, reps=3):
             b.flush.zero_()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(b.stream)
-            _, touched = per_op_layer(b.inp, cfg, T)
+            _, touched = per_op_layer(b.inp, cfg, T, b.blk)
             e.record(b.stream)
             e.synchronize()
             if i:
                 ts.append(s.elapsed_time(e) / 1e3)
         per_T[T] = statistics.median(ts)
         launches[T] = 12 + 9 * touched  # router ops + per touched expert (gather, 3 GEMMs, act, add)
+        if b.blk is not None:
+            launches[T] += 8 + (6 if b.blk["sg"] is not None else 0)  # norm, residual, shared
     tot = sum(per_T.values())
     return {"value": round(sum(cfg.T_sweep) / tot, 1), "unit": "tokens/s",
-            "kind": "same-GPU per-op PyTorch (router matmul/softmax/topk, stable argsort, "
-                    "bincount host sync, per-expert cuBLAS GEMMs, index_add_)",
+            "kind": "same-GPU per-op PyTorch (" + ("RMSNorm, " if b.blk is not None else "") +
+                    "router matmul/softmax/topk, stable argsort, bincount host sync, per-expert "
+                    "cuBLAS GEMMs, index_add_" +
+                    (", shared expert, residual" if b.blk is not None else "") + ")",
             "us_per_layer": {str(T): round(t * 1e6, 1) for T, t in per_T.items()},
             "launches_per_layer": {str(T): n for T, n in launches.items()}}
 
@@ -492,13 +537,30 @@ def cpu_baseline(b, cfg, args):
     hb = {k: (wl.bits(v) if v is not None and v.dtype == torch.bfloat16 else
               (None if v is None else v.detach().cpu().numpy())) for k, v in b.inp.items()}
     threads = oracle.default_threads()
+    run = oracle_call(oracle, hb, block_bits(b.blk), cfg, n, threads)
     t0 = time.perf_counter()
-    oracle.moe_layer(hb["x"][:n], hb["wr"], hb["bias"], hb["wg"], hb["wu"], hb["wd"], k=cfg.k,
-                     nthreads=threads)
+    run()
     dt = time.perf_counter() - t0
+    what = "layer" if b.blk is None else "block"
     return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} tokens of the {cfg.name} layer (all routing + outputs), one call, "
+            "sample": f"{n} tokens of the {cfg.name} {what} (all routing + outputs), one call, "
                       f"{dt:.1f} s"}
+
+
+def block_bits(blk):
+    if blk is None:
+        return None
+    return {k: (wl.bits(v) if isinstance(v, torch.Tensor) else v) for k, v in blk.items()}
+
+
+def oracle_call(oracle, hb, bb, cfg, n, threads):
+    """The oracle over the first n tokens: the layer, or the block when bb is given."""
+    if bb is None:
+        return lambda: oracle.moe_layer(hb["x"][:n], hb["wr"], hb["bias"], hb["wg"], hb["wu"],
+                                        hb["wd"], k=cfg.k, nthreads=threads)
+    return lambda: oracle.moe_block(hb["x"][:n], bb["gamma"], bb["eps"], hb["wr"], hb["bias"],
+                                    hb["wg"], hb["wu"], hb["wd"], bb["sg"], bb["su"], bb["sd"],
+                                    k=cfg.k, nthreads=threads)
 
 
 def run_reference(args, world, rank):
@@ -507,17 +569,19 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     import oracle
-    cfg = {"mixtral": wl.MIXTRAL, "fine": wl.FINE}[args.workload]
-    inp = wl.moe_inputs(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+    if args.workload not in MOE_WORKLOADS:
+        return {"impl": "reference", "unavailable": "the reference arm covers the MoE workloads"}
+    cfg, Fs = MOE_WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = wl.moe_inputs(cfg, device=dev)
     hb = {k: (wl.bits(v) if v is not None and v.dtype == torch.bfloat16 else
               (None if v is None else v.detach().cpu().numpy())) for k, v in inp.items()}
+    bb = block_bits(wl.block_extra_inputs(cfg, Fs, device=dev)) if Fs is not None else None
     del inp
     n = args.ref_tokens
     threads = oracle.default_threads()
-
-    def one():
-        oracle.moe_layer(hb["x"][:n], hb["wr"], hb["bias"], hb["wg"], hb["wu"], hb["wd"],
-                         k=cfg.k, nthreads=threads)
+    one = oracle_call(oracle, hb, bb, cfg, n, threads)
+    what = "MoE layer" if Fs is None else f"fused MoE block (Fs={Fs})"
 
     for _ in range(args.warmup):
         one()
@@ -527,15 +591,16 @@ def run_reference(args, world, rank):
     dt = time.perf_counter() - t0
     v = round(args.steps * n / dt, 3)
     return {
-        "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if Fs is None else METRIC_BLOCK, "value": v, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,0.02) bf16 weights and activations)", "impl": "reference",
-        "config": {"workload": f"{cfg.name} MoE layer, T sweep {list(cfg.T_sweep)}",
+        "config": {"workload": f"{cfg.name} {what}, T sweep {list(cfg.T_sweep)}",
                    "H": cfg.H, "F": cfg.F, "E": cfg.E, "k": cfg.k,
                    "sample_per_step": f"{n} tokens"},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{n} tokens of the {cfg.name} layer per step"},
+                         "sample": f"{n} tokens of the {cfg.name} {what} per step"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -546,7 +611,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["mixtral", "fine", "splitk", "mlp"], default="mixtral")
+    ap.add_argument("--workload", choices=list(MOE_WORKLOADS) + ["splitk", "mlp"],
+                    default="mixtral")
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -559,7 +625,7 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
     if args.single is not None:
-        if args.workload not in ("mixtral", "fine"):
+        if args.workload not in MOE_WORKLOADS:
             ap.error("--single applies to the MoE workloads")
         line = run_single(args, local) if rank == 0 else None
     elif args.impl == "reference":

@@ -107,6 +107,41 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias,
                  void* workspace, size_t workspace_bytes, const et_opts* opts, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Fused MoE block: RMSNorm before the router, the routed experts, an optional
+ * shared SwiGLU expert, and the residual add after the combine -- the layers
+ * either side of the MoE layers the episode "Prompt Boundary-Aware Scheduling
+ * with Event Tensors for Dynamic Kernels" discusses, joined to them in the
+ * same launch.  All of it is one persistent cooperative launch: RMSNorm
+ * tasks release an event the router and the shared expert's gate/up tiles
+ * wait on; the shared expert's tiles carry no routing dependency and run
+ * beside the router; the combine waits for both the routed and the shared
+ * output tiles.
+ *
+ *   x_hat[t]  = bf16( (x[t] * r_t) * gamma ),  r_t = 1 / sqrt(ss_t / H + eps),
+ *               ss_t = sum_h x[t,h]^2 in the router's fp32 order, and each
+ *               step one IEEE-rounded fp32 operation;
+ *   routing, h and y as et_moe_layer, with x_hat in place of x;
+ *   ys[t]     = bf16( bf16( silu(x_hat Wsg^T) * (x_hat Wsu^T) ) Wsd^T )  (Fs > 0);
+ *   out[t]    = bf16( x[t] + sum_j w[t,j] * y[t,j] + ys[t] ),  fp32 sum in
+ *               that order, one rounding.
+ *
+ * gamma bf16 [H]; eps > 0; ws_gate, ws_up bf16 [Fs,H]; ws_down bf16 [H,Fs]
+ * (NULL when Fs == 0); Fs a multiple of 128, or 0 for no shared expert.
+ * x_hat: optional bf16 [T_max,H] output of the normalised rows (NULL = kept
+ * in the workspace).  Other arguments as et_moe_layer.  Additionally
+ * (k + 2) * H * 2 bytes must fit in the stage ring (ET_ERR_UNSUPPORTED).
+ * ---------------------------------------------------------------------- */
+size_t et_moe_block_workspace_bytes(int T_max, int H, int F, int E, int k, int Fs);
+
+int et_moe_block(const void* x, const void* gamma, float eps, const void* w_router,
+                 const float* router_bias, const void* w_gate, const void* w_up,
+                 const void* w_down, const void* ws_gate, const void* ws_up,
+                 const void* ws_down, int Fs, void* out, void* x_hat, int32_t* topk_idx,
+                 float* topk_w, int32_t* expert_counts, int32_t* perm, int T,
+                 const int32_t* d_T, int T_max, int H, int F, int E, int k, void* workspace,
+                 size_t workspace_bytes, const et_opts* opts, void* stream);
+
+/* ------------------------------------------------------------------------
  * Split-K GEMM with event-counter reduction:
  *   Y[M,N] = bf16( sum_{s<split} X[:,K_s] Wt[:,K_s]^T ),  K_s = s-th of `split`
  * equal K chunks.  Each (row tile, column tile, split) is one task; the task

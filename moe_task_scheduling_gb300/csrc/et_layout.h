@@ -56,7 +56,8 @@ struct EtHeader {
     int32_t ev_norm;        // RMSNorm tasks done (MLP chain)
     int32_t split;          // split of the down projection chosen this call
     int32_t gu_split;       // K chunks of a gate/up tile chosen this call
-    int32_t reserved[50];
+    int32_t ev_sdone;       // shared-expert output tiles complete (fused block)
+    int32_t reserved[49];
 };
 static_assert(sizeof(EtHeader) == 256, "header is 256 bytes");
 
@@ -80,7 +81,7 @@ enum WaitWhere {
 // Task descriptor of the dynamic queue: {type, a, b, c}
 enum TaskType { kTaskExit = 0, kTaskRouter = 1, kTaskScan = 2, kTaskPermute = 3,
                 kTaskGateUp = 4, kTaskDown = 5, kTaskCombine = 6, kTaskNorm = 7,
-                kTaskSplitK = 8 };
+                kTaskSplitK = 8, kTaskShGateUp = 9, kTaskShDown = 10 };
 
 // ---------------------------------------------------------------- kernel argument blocks
 
@@ -120,6 +121,18 @@ struct MoeArgs {
     int wr_box;           // router-weight TMA box height (0: the weight is read in place)
     int b_wide;           // the 64-row activation maps are valid (enough rows)
     int num_ctas;
+    // fused MoE block (gamma != null): x_hat = RMSNorm(x) * gamma routes and feeds
+    // the experts; a shared SwiGLU expert (Fs > 0) and the residual join the combine
+    const bf16* gamma;    // [H] or null (plain layer)
+    float eps;
+    int Fs;               // shared expert width (multiple of 128) or 0
+    bf16* xn;             // [T_max, H]: x_hat
+    bf16* hs;             // [T_max, Fs]: shared expert h
+    bf16* ys;             // [T_max, H]: shared expert output
+    int32_t* ev_hs;       // [mts_max * kSplitMax]: shared h tiles done per F-chunk
+    int32_t* ev_ys;       // [mts_max * H/128]: shared split partials (self-resetting)
+    float* partial_s;     // [kSplitMax, split_rows_cap, H]
+    int mts_max;
     uint64_t* trace;      // optional per-task trace (see et_opts)
     int trace_cap;
     uint64_t timeout_ns;

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <mutex>
 #include <string>
 
@@ -145,12 +146,16 @@ struct Carve {
 // ---------------------------------------------------------------- MoE layout
 
 struct MoeLayout {
-    int Tk, r_max, mt_max, q_max, split_cap, gu_cap;
+    int Tk, r_max, mt_max, q_max, split_cap, gu_cap, mts_max;
     size_t ev_h, ev_y, ev_tile, ev_gu, logits, hist, base, idx, gw, cnt, off, pos, perm, g_expert,
-        g_row0, g_rows, g_n, queue, xp, h, y, partial, gu_part, total;
+        g_row0, g_rows, g_n, queue, xp, h, y, partial, gu_part;
+    size_t xn, hs, ys, ev_hs, ev_ys, partial_s;  // fused block only (block == true)
+    size_t total;
 };
 
-MoeLayout moe_layout(int T_max, int H, int F, int E, int k) {
+// block: the fused MoE block's extra regions (x_hat; with Fs > 0 the shared
+// expert's h, y, counters and split partials).
+MoeLayout moe_layout(int T_max, int H, int F, int E, int k, bool block = false, int Fs = 0) {
     MoeLayout L{};
     L.Tk = T_max * k;
     L.r_max = ceil_div(T_max, kRouterTile);
@@ -184,6 +189,17 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k) {
     L.y = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
     L.partial = c.take(sizeof(float) * static_cast<size_t>(kSplitMax) * L.split_cap * H, 1024);
     L.gu_part = c.take(sizeof(float) * 2 * static_cast<size_t>(L.gu_cap) * F, 1024);
+    if (block) {
+        L.xn = c.take(sizeof(uint16_t) * static_cast<size_t>(T_max) * H, 1024);
+        if (Fs > 0) {
+            L.mts_max = ceil_div(T_max, kWideNMax);
+            L.ev_hs = c.take(sizeof(int) * L.mts_max * kSplitMax);
+            L.ev_ys = c.take(sizeof(int) * L.mts_max * HT);
+            L.hs = c.take(sizeof(uint16_t) * static_cast<size_t>(T_max) * Fs, 1024);
+            L.ys = c.take(sizeof(uint16_t) * static_cast<size_t>(T_max) * H, 1024);
+            L.partial_s = c.take(sizeof(float) * static_cast<size_t>(kSplitMax) * L.split_cap * H, 1024);
+        }
+    }
     L.total = round_up(c.off, 256);
     return L;
 }
@@ -203,6 +219,31 @@ bool moe_shape_ok(int T_max, int H, int F, int E, int k, std::string* why) {
     }
     return true;
 }
+
+// The fused block stages k + 2 rows per token in the combine (the k expert
+// rows, the residual and the shared expert's row).
+bool block_shape_ok(int T_max, int H, int F, int E, int k, int Fs, std::string* why) {
+    if (!moe_shape_ok(T_max, H, F, E, k, why)) return false;
+    if (Fs < 0 || Fs % 128 || Fs > 65536) {
+        *why = "Fs must be 0 or a positive multiple of 128 (<= 65536)"; return false;
+    }
+    const long long rows = k + 1 + (Fs > 0 ? 1 : 0);
+    if (rows * H * 2 > moe_ring_bytes()) {
+        *why = "(k+2)*H*2 bytes must fit in the stage ring (" + std::to_string(moe_ring_bytes()) + ")";
+        return false;
+    }
+    return true;
+}
+
+// Fused-block inputs of the shared launch path (on == false: the plain layer).
+struct BlockIn {
+    bool on;
+    const void* gamma;
+    float eps;
+    int Fs;
+    const void *ws_gate, *ws_up, *ws_down;
+    void* x_hat;
+};
 
 // ---------------------------------------------------------------- split-K layout
 
@@ -263,21 +304,24 @@ size_t et_moe_workspace_bytes(int T_max, int H, int F, int E, int k) {
     return moe_layout(T_max, H, F, E, k).total;
 }
 
-int et_moe_layer(const void* x, const void* w_router, const float* router_bias, const void* w_gate,
-                 const void* w_up, const void* w_down, void* out, int32_t* topk_idx, float* topk_w,
-                 int32_t* expert_counts, int32_t* perm, int T, const int32_t* d_T, int T_max, int H,
-                 int F, int E, int k, void* workspace, size_t workspace_bytes, const et_opts* opts,
-                 void* stream) {
-    g_last_error.clear();
-    std::string why;
-    if (!moe_shape_ok(T_max, H, F, E, k, &why)) return fail(ET_ERR_UNSUPPORTED, why);
+}  // extern "C"
+
+namespace {
+
+// The plain layer and the fused block share one launch path; `b.on` selects
+// the block (the shapes were validated by the caller).
+int moe_run(const void* x, const BlockIn& b, const void* w_router, const float* router_bias,
+            const void* w_gate, const void* w_up, const void* w_down, void* out, int32_t* topk_idx,
+            float* topk_w, int32_t* expert_counts, int32_t* perm, int T, const int32_t* d_T,
+            int T_max, int H, int F, int E, int k, void* workspace, size_t workspace_bytes,
+            const et_opts* opts, void* stream) {
     if (!x || !w_router || !w_gate || !w_up || !w_down || !out)
         return fail(ET_ERR_INVALID, "x, w_router, w_gate, w_up, w_down and out must be non-NULL");
     if (!d_T && (T < 0 || T > T_max)) return fail(ET_ERR_INVALID, "T must be in [0, T_max]");
     const void* need16[] = {x, w_router, w_gate, w_up, w_down, out};
     for (const void* p : need16)
         if (!aligned<void>(p, 16)) return fail(ET_ERR_INVALID, "tensors must be 16-byte aligned");
-    const MoeLayout L = moe_layout(T_max, H, F, E, k);
+    const MoeLayout L = moe_layout(T_max, H, F, E, k, b.on, b.Fs);
     int rc = check_ws(workspace, workspace_bytes, L.total);
     if (rc) return rc;
     if (!d_T && T == 0) return ET_OK;
@@ -339,8 +383,22 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
     a.fault_arg = opts ? opts->fault_arg : 0;
     a.trace = (opts && opts->trace && opts->trace_cap) ? static_cast<uint64_t*>(opts->trace) : nullptr;
     a.trace_cap = opts ? static_cast<int>(opts->trace_cap) : 0;
+    if (b.on) {
+        a.gamma = static_cast<const bf16*>(b.gamma);
+        a.eps = b.eps;
+        a.Fs = b.Fs;
+        a.xn = b.x_hat ? static_cast<bf16*>(b.x_hat) : reinterpret_cast<bf16*>(ws + L.xn);
+        if (b.Fs > 0) {
+            a.hs = reinterpret_cast<bf16*>(ws + L.hs);
+            a.ys = reinterpret_cast<bf16*>(ws + L.ys);
+            a.ev_hs = reinterpret_cast<int32_t*>(ws + L.ev_hs);
+            a.ev_ys = reinterpret_cast<int32_t*>(ws + L.ev_ys);
+            a.partial_s = reinterpret_cast<float*>(ws + L.partial_s);
+            a.mts_max = L.mts_max;
+        }
+    }
 
-    CUtensorMap maps[8];
+    CUtensorMap maps[13];
     const uint64_t EF = static_cast<uint64_t>(E) * F, EH = static_cast<uint64_t>(E) * H;
     if ((rc = make_map(&maps[0], w_gate, EF, H, kTileM, "w_gate"))) return rc;
     if ((rc = make_map(&maps[1], w_up, EF, H, kTileM, "w_up"))) return rc;
@@ -360,9 +418,64 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
         maps[6] = maps[3];
         maps[7] = maps[4];
     }
+    for (int i = 8; i < 13; ++i) maps[i] = maps[0];  // unused unless the shared expert runs
+    if (b.on && b.Fs > 0) {
+        const uint64_t Fs = static_cast<uint64_t>(b.Fs);
+        if ((rc = make_map(&maps[8], b.ws_gate, Fs, H, kTileM, "ws_gate"))) return rc;
+        if ((rc = make_map(&maps[9], b.ws_up, Fs, H, kTileM, "ws_up"))) return rc;
+        if ((rc = make_map(&maps[10], b.ws_down, H, Fs, kTileM, "ws_down"))) return rc;
+        if ((rc = make_map(&maps[11], a.xn, T_max, H, kBBoxRows, "x_hat"))) return rc;
+        if ((rc = make_map(&maps[12], a.hs, T_max, Fs, kBBoxRows, "shared h"))) return rc;
+    }
     cudaError_t e = launch_moe(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "launch of the MoE megakernel");
     return ET_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int et_moe_layer(const void* x, const void* w_router, const float* router_bias, const void* w_gate,
+                 const void* w_up, const void* w_down, void* out, int32_t* topk_idx, float* topk_w,
+                 int32_t* expert_counts, int32_t* perm, int T, const int32_t* d_T, int T_max, int H,
+                 int F, int E, int k, void* workspace, size_t workspace_bytes, const et_opts* opts,
+                 void* stream) {
+    g_last_error.clear();
+    std::string why;
+    if (!moe_shape_ok(T_max, H, F, E, k, &why)) return fail(ET_ERR_UNSUPPORTED, why);
+    BlockIn b{};
+    return moe_run(x, b, w_router, router_bias, w_gate, w_up, w_down, out, topk_idx, topk_w,
+                   expert_counts, perm, T, d_T, T_max, H, F, E, k, workspace, workspace_bytes, opts,
+                   stream);
+}
+
+size_t et_moe_block_workspace_bytes(int T_max, int H, int F, int E, int k, int Fs) {
+    std::string why;
+    if (!block_shape_ok(T_max, H, F, E, k, Fs, &why)) return 0;
+    return moe_layout(T_max, H, F, E, k, true, Fs).total;
+}
+
+int et_moe_block(const void* x, const void* gamma, float eps, const void* w_router,
+                 const float* router_bias, const void* w_gate, const void* w_up, const void* w_down,
+                 const void* ws_gate, const void* ws_up, const void* ws_down, int Fs, void* out,
+                 void* x_hat, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                 int32_t* perm, int T, const int32_t* d_T, int T_max, int H, int F, int E, int k,
+                 void* workspace, size_t workspace_bytes, const et_opts* opts, void* stream) {
+    g_last_error.clear();
+    std::string why;
+    if (!block_shape_ok(T_max, H, F, E, k, Fs, &why)) return fail(ET_ERR_UNSUPPORTED, why);
+    if (!gamma) return fail(ET_ERR_INVALID, "gamma must be non-NULL");
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return fail(ET_ERR_INVALID, "eps must be finite and > 0");
+    if (Fs > 0 && (!ws_gate || !ws_up || !ws_down))
+        return fail(ET_ERR_INVALID, "ws_gate, ws_up and ws_down must be non-NULL when Fs > 0");
+    const void* need16[] = {gamma, ws_gate, ws_up, ws_down, x_hat};
+    for (const void* q : need16)
+        if (q && !aligned<void>(q, 16)) return fail(ET_ERR_INVALID, "tensors must be 16-byte aligned");
+    BlockIn b{true, gamma, eps, Fs, ws_gate, ws_up, ws_down, x_hat};
+    return moe_run(x, b, w_router, router_bias, w_gate, w_up, w_down, out, topk_idx, topk_w,
+                   expert_counts, perm, T, d_T, T_max, H, F, E, k, workspace, workspace_bytes, opts,
+                   stream);
 }
 
 size_t et_splitk_workspace_bytes(int M_max, int N, int K, int split) {

@@ -210,6 +210,10 @@ struct MoePlan {
     int CT, NC;    // tokens per combine task; combine tasks
     int NP;        // permute tasks in the queue (0: one router tile, permuted inline)
     bool stage;    // router tiles stage x and their weight chunk in the ring
+    // fused block: norm tasks (16 rows each), shared expert row tiles (256 rows),
+    // F-tiles and down split; the static prefix [norm][router][shared gate/up]
+    // [shared down] precedes the routing-driven queue
+    int NRN, MTS, FTS, SS, NSG, NSD, NS0;
 };
 
 __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint32_t ring_bytes) {
@@ -243,16 +247,65 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     P.EC = E / P.C;
     P.Q = P.R > 0 ? min(max(1, G / P.R), kRouterTile * k) : 1;
     // a combine task's k rows per token fit the ring in one staging batch
-    const int per_batch = max(1, static_cast<int>(ring_bytes / (static_cast<uint32_t>(k) * H * 2)));
+    const int rpt = k + (p.gamma ? 1 : 0) + (p.gamma && p.Fs > 0 ? 1 : 0);  // rows per token
+    const int per_batch = max(1, static_cast<int>(ring_bytes / (static_cast<uint32_t>(rpt) * H * 2)));
     P.CT = min(min(kCombineTile, per_batch), max(1, ceil_div(T, G)));
     P.NC = ceil_div(T, P.CT);
     P.NP = P.R > 1 ? P.R * P.Q : 0;
+    const int HT = H / kTileM;
+    const bool block = p.gamma != nullptr;
+    P.NRN = block ? P.R : 0;
+    P.MTS = (block && p.Fs > 0) ? ceil_div(T, kWideNMax) : 0;
+    P.FTS = p.Fs / kTileM;
+    P.SS = 1;
+    if (P.MTS > 0 && T <= p.split_rows_cap && P.MTS * HT < 3 * G) {
+        for (int d = 2; d <= kSplitMax; ++d) {
+            if (P.FTS % d) continue;
+            if (p.Fs / kBlockK / d < 4) break;  // keep >= 4 k-blocks a chunk
+            P.SS = d;
+            if (P.MTS * HT * d >= 3 * G) break;
+        }
+    }
+    P.NSG = P.MTS * P.FTS;
+    P.NSD = P.MTS * P.SS * HT;
+    P.NS0 = P.NRN + P.R * P.C + P.NSG + P.NSD;
     return P;
 }
 
 __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, uint8_t* smem,
                                           const Ring& ring, Ctl* ctl, const WaitCtx& wc,
                                           uint32_t& sphase, uint32_t& seq);
+
+// ------------------------------------------------------------------ NORM (fused block)
+
+// x_hat rows of router tile r, defined in fp32 so the routing that depends on
+// them is reproducible bit for bit: the sum of squares in the router-logit
+// order (lane l sums h = l, l + 32, ... -- each square exact in fp32 -- then
+// the halving tree), r = 1 / sqrt(ss / H + eps), x_hat = bf16((x * r) * gamma),
+// every step one IEEE-rounded fp32 operation.  Warp w takes rows 2w, 2w + 1.
+__device__ __forceinline__ void norm_task(const MoeArgs& p, const MoePlan& P, int r) {
+    const int H = p.H, warp = wtid_() >> 5, lane = wtid_() & 31;
+    constexpr int kRowsPerWarp = kRouterTile / (kWorkers / 32);
+    for (int q = 0; q < kRowsPerWarp; ++q) {
+        const int t = r * kRouterTile + warp * kRowsPerWarp + q;
+        if (t >= P.T) break;
+        const bf16* xr = p.x + static_cast<size_t>(t) * H;
+        float acc = 0.0f;
+        for (int h = lane; h < H; h += 32) {
+            const float v = bf2f(xr[h]);
+            acc = fmaf(v, v, acc);  // v * v is exact: fma == add of the square
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) acc = acc + __shfl_down_sync(0xffffffffu, acc, off);
+        float rr = 0.0f;
+        if (lane == 0)
+            rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, static_cast<float>(H)), p.eps)));
+        rr = __shfl_sync(0xffffffffu, rr, 0);
+        bf16* on = p.xn + static_cast<size_t>(t) * H;
+        for (int h = lane; h < H; h += 32)
+            on[h] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(bf2f(xr[h]), rr), bf2f(p.gamma[h])));
+    }
+}
 
 // Logits of router tile r for expert chunk c.  With staging, the token rows
 // (one bulk copy) and the chunk's 8-expert weight blocks (TMA boxes) are
@@ -271,7 +324,14 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     const int t0 = r * kRouterTile, nt = min(kRouterTile, P.T - t0);
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
     const int e0 = c * P.EC, ec = P.EC;
-    const bf16* xb = p.x + static_cast<size_t>(t0) * H;
+    if (p.gamma) {  // fused block: route x_hat, once every norm task is done
+        if (wtid_() == 0) ctl->flag = ev_wait_geq(wc, &p.hdr->ev_norm, P.NRN, kWhereNorm) ? 1 : 0;
+        worker_sync();
+        if (!ctl->flag) return false;
+        fence_proxy_async_global();  // x_hat rows written by generic stores, read by bulk copies
+    }
+    const bf16* xsrc = p.gamma ? p.xn : p.x;
+    const bf16* xb = xsrc + static_cast<size_t>(t0) * H;
     const bf16* wb = p.wr + e0;
     int o = 0, rs = E, blk = 8;
     uint64_t tm = p.trace ? globaltimer_ns() : 0;
@@ -680,8 +740,10 @@ __device__ __forceinline__ bool permute_rows(const MoeArgs& p, const MoePlan& P,
     auto issue = [&](int c0) {  // worker thread 0: token rows tl0 + c0 .. of the part
         const int nc = min(per, ntok - c0);
         mbar_arrive_expect_tx(&ctl->sbar, nc * rowb);
-        bulk_g2s(ring.base, p.x + static_cast<size_t>(t0 + tl0 + c0) * H, nc * rowb, &ctl->sbar);
+        bulk_g2s(ring.base, (p.gamma ? p.xn : p.x) + static_cast<size_t>(t0 + tl0 + c0) * H,
+                 nc * rowb, &ctl->sbar);
     };
+    if (p.gamma && wtid_() == 0) fence_proxy_async_global();  // x_hat: generic stores
     if (!x_staged && ntok > 0 && wtid_() == 0) issue(0);
     const int* iv = ie_src;
     if (!iv) {
@@ -739,21 +801,33 @@ __device__ __forceinline__ bool permute_task(const MoeArgs& p, const MoePlan& P,
 
 // ------------------------------------------------------------------ COMBINE
 
-// out[t] = bf16(sum_j w[t, j] * y[pos(t, j)]) in slot order.  The k expert
-// output rows of a batch of tokens are gathered into the ring with bulk
-// copies (as many tokens as fit), then summed from shared memory.
+// out[t] = bf16(sum_j w[t, j] * y[pos(t, j)]) in slot order -- in the fused
+// block bf16(x[t] + sum_j w[t, j] * y[pos(t, j)] + ys[t]), summed in that order.
+// The rows of a batch of tokens (k expert outputs, then x and ys in the
+// block) are gathered into the ring with bulk copies, then summed from there.
+__device__ __forceinline__ int combine_rows_per_token(const MoeArgs& p, const MoePlan& P) {
+    return p.k + (p.gamma ? 1 : 0) + (P.MTS > 0 ? 1 : 0);
+}
+
+// Wait (worker thread 0, bounded) until every output tile is done: routed
+// tiles on ev_ydone, shared-expert tiles on ev_sdone.
+__device__ __forceinline__ bool combine_wait(const MoeArgs& p, const MoePlan& P, const WaitCtx& wc) {
+    const int HT = p.H / kTileM;
+    const int target = ld_relaxed(&p.hdr->total_mt) * HT;
+    if (!ev_wait_geq(wc, &p.hdr->ev_ydone, target, kWhereY)) return false;
+    return P.MTS == 0 || ev_wait_geq(wc, &p.hdr->ev_sdone, P.MTS * HT, kWhereY);
+}
+
 __device__ __forceinline__ bool combine_task(const MoeArgs& p, const MoePlan& P, int c,
                                              uint8_t* smem, const Ring& ring, Ctl* ctl,
                                              const WaitCtx& wc, uint32_t& sphase, uint32_t& seq) {
     const int H = p.H, k = p.k;
-    if (wtid_() == 0) {
-        const int target = ld_relaxed(&p.hdr->total_mt) * (H / kTileM);
-        ctl->flag = ev_wait_geq(wc, &p.hdr->ev_ydone, target, kWhereY) ? 1 : 0;
-    }
+    if (wtid_() == 0) ctl->flag = combine_wait(p, P, wc) ? 1 : 0;
     worker_sync();
     if (!ctl->flag) return false;
     fence_proxy_async_global();  // y rows written by other CTAs' generic stores
     const int t0 = c * P.CT, nt = min(P.CT, P.T - t0), vpr = H / 8;
+    const int rpt = combine_rows_per_token(p, P), hx = p.gamma ? 1 : 0, hs = P.MTS > 0 ? 1 : 0;
     const uint32_t rowb = static_cast<uint32_t>(H) * 2u;
     float* w_s = reinterpret_cast<float*>(smem);                   // [16 * k]
     int* pos_s = reinterpret_cast<int*>(smem) + kCombineTile * 8;  // [16 * k]
@@ -761,32 +835,46 @@ __device__ __forceinline__ bool combine_task(const MoeArgs& p, const MoePlan& P,
         w_s[i] = __ldcg(p.gw + static_cast<size_t>(t0) * k + i);
         pos_s[i] = __ldcg(p.pos + static_cast<size_t>(t0) * k + i);
     }
-    const int per = static_cast<int>(ring.bytes / (static_cast<uint32_t>(k) * rowb));
-    if (wtid_() == 0 && nt > 0) mbar_arrive_expect_tx(&ctl->sbar, min(per, nt) * k * rowb);
+    const int per = static_cast<int>(ring.bytes / (static_cast<uint32_t>(rpt) * rowb));
+    if (wtid_() == 0 && nt > 0) mbar_arrive_expect_tx(&ctl->sbar, min(per, nt) * rpt * rowb);
     worker_sync();
     for (int b0 = 0; b0 < nt; b0 += per) {
         const int nb = min(per, nt - b0);
-        for (int q = wtid_(); q < nb * k; q += kWorkers)
-            bulk_g2s(ring.base + q * rowb, p.y + static_cast<size_t>(pos_s[b0 * k + q]) * H, rowb,
-                     &ctl->sbar);
+        for (int q = wtid_(); q < nb * rpt; q += kWorkers) {  // row q % rpt of token q / rpt
+            const int tt = q / rpt, j = q % rpt, t = t0 + b0 + tt;
+            const bf16* src = j < k ? p.y + static_cast<size_t>(pos_s[(b0 + tt) * k + j]) * H
+                                    : (j == k && hx ? p.x : p.ys) + static_cast<size_t>(t) * H;
+            bulk_g2s(ring.base + q * rowb, src, rowb, &ctl->sbar);
+        }
         if (!staging_wait(ctl, sphase, wc, seq)) return false;
         for (int v = wtid_(); v < nb * vpr; v += kWorkers) {
             const int tt = v / vpr, cc = v % vpr;
+            const uint8_t* rows = ring.base + tt * rpt * rowb;
             float acc[8];
+            if (hx) {
+                unpack8(reinterpret_cast<const uint4*>(rows + k * rowb)[cc], acc);  // residual
+            } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+                for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            }
             for (int j = 0; j < k; ++j) {  // fp32 sum in slot order j = 0 .. k-1
                 const float wj = w_s[(b0 + tt) * k + j];
                 float yv[8];
-                unpack8(reinterpret_cast<const uint4*>(ring.base + (tt * k + j) * rowb)[cc], yv);
+                unpack8(reinterpret_cast<const uint4*>(rows + j * rowb)[cc], yv);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, yv[i], acc[i]);
+            }
+            if (hs) {  // the shared expert
+                float yv[8];
+                unpack8(reinterpret_cast<const uint4*>(rows + (k + hx) * rowb)[cc], yv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = acc[i] + yv[i];
             }
             reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t0 + b0 + tt) * H)[cc] = pack8(acc);
         }
         worker_sync();  // the batch is consumed before the ring is refilled
         if (wtid_() == 0 && b0 + per < nt)
-            mbar_arrive_expect_tx(&ctl->sbar, min(per, nt - b0 - per) * k * rowb);
+            mbar_arrive_expect_tx(&ctl->sbar, min(per, nt - b0 - per) * rpt * rowb);
         worker_sync();
     }
     return true;
@@ -799,8 +887,12 @@ __device__ __forceinline__ void combine_inline(const MoeArgs& p, const MoePlan& 
     for (int v = wtid_(); v < P.T * vpr; v += kWorkers) {
         const int t = v / vpr, cc = v % vpr;
         float acc[8];
+        if (p.gamma) {
+            unpack8(__ldcg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H) + cc), acc);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        }
         for (int j = 0; j < k; ++j) {  // fp32 sum in slot order j = 0 .. k-1
             const float wj = __ldcg(p.gw + static_cast<size_t>(t) * k + j);
             const int pp = __ldcg(p.pos + static_cast<size_t>(t) * k + j);
@@ -808,6 +900,12 @@ __device__ __forceinline__ void combine_inline(const MoeArgs& p, const MoePlan& 
             unpack8(__ldcg(reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(pp) * H) + cc), yv);
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, yv[i], acc[i]);
+        }
+        if (P.MTS > 0) {
+            float yv[8];
+            unpack8(__ldcg(reinterpret_cast<const uint4*>(p.ys + static_cast<size_t>(t) * H) + cc), yv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = acc[i] + yv[i];
         }
         reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * H)[cc] = pack8(acc);
     }
@@ -823,7 +921,13 @@ __device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc,
     TaskMsg m{};
     m.type = kTaskExit;
     if (aborted(wc) || P.R == 0) return m;  // T == 0: no task at all
-    const int i = claim >= 0 ? claim : atomicAdd(&p.hdr->q_head, 1);
+    int i = claim >= 0 ? claim : atomicAdd(&p.hdr->q_head, 1);
+    if (i < P.NRN) {  // fused block: RMSNorm of router tile i's rows
+        m.type = kTaskNorm;
+        m.a = i;
+        return m;
+    }
+    i -= P.NRN;
     const int nr = P.R * P.C;
     if (i < nr) {
         m.type = kTaskRouter;
@@ -831,7 +935,26 @@ __device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc,
         m.b = i % P.C;
         return m;
     }
-    const int j = i - nr;
+    i -= nr;
+    if (i < P.NSG + P.NSD) {  // fused block: shared expert tiles (no routing needed)
+        const int HT = p.H / kTileM;
+        if (i < P.NSG) {
+            m.type = kTaskShGateUp;
+            m.a = i / P.FTS;  // row tile
+            m.b = i % P.FTS;  // F-tile
+        } else {
+            i -= P.NSG;
+            m.type = kTaskShDown | (P.SS << 8);
+            m.a = i / (P.SS * HT);
+            m.b = (i % (P.SS * HT)) / HT;  // F-chunk
+            m.c = i % HT;                  // output tile
+        }
+        m.row0 = m.a * kWideNMax;
+        m.rows = min(kWideNMax, P.T - m.row0);
+        m.n = (m.rows + 15) / 16 * 16;
+        return m;
+    }
+    const int j = i - P.NSG - P.NSD;
     if (q_total < 0) {
         if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
         q_total = ld_relaxed(&p.hdr->q_total);
@@ -856,7 +979,9 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xp,
                const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wr,
                const __grid_constant__ CUtensorMap tm_xp64, const __grid_constant__ CUtensorMap tm_h64,
-               const __grid_constant__ MoeArgs p) {
+               const __grid_constant__ CUtensorMap tm_sg, const __grid_constant__ CUtensorMap tm_su,
+               const __grid_constant__ CUtensorMap tm_sd, const __grid_constant__ CUtensorMap tm_xn,
+               const __grid_constant__ CUtensorMap tm_hs, const __grid_constant__ MoeArgs p) {
     extern __shared__ uint8_t smem_raw[];
     const uint64_t t_start = globaltimer_ns();
     Ring ring;
@@ -876,8 +1001,21 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
     const MoePlan P = moe_plan(p, T, static_cast<int>(gridDim.x), ring.bytes);
     const int FT = p.F / kTileM, HT = p.H / kTileM;
 
+    auto is_gemm = [](int type) {
+        return type == kTaskGateUp || type == kTaskDown || type == kTaskShGateUp ||
+               type == kTaskShDown;
+    };
     auto gemm_of = [&](const TaskMsg& m) {
         const int type = m.type & 0xff, S = (m.type >> 8) & 0xff, KC = (m.type >> 16) & 0xff;
+        if (type == kTaskShGateUp)  // shared expert over the rows of x_hat
+            return GemmTask{&tm_sg, &tm_su, &tm_xn, nullptr, m.b * kTileM, m.row0, 0,
+                            p.H / kBlockK, m.n, m.b, &p.hdr->ev_norm, P.NRN, kWhereNorm};
+        if (type == kTaskShDown) {
+            const int fch = p.Fs / S;
+            return GemmTask{&tm_sd, nullptr, &tm_hs, nullptr, m.c * kTileM, m.row0,
+                            m.b * (fch / kBlockK), fch / kBlockK, m.n, m.c,
+                            &p.ev_hs[m.a * kSplitMax + m.b], P.FTS / S, kWhereH};
+        }
         if (type == kTaskGateUp) {
             const int nkb = p.H / kBlockK / KC;
             return GemmTask{&tm_wg, &tm_wu, &tm_xp, p.b_wide ? &tm_xp64 : nullptr,
@@ -910,7 +1048,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 mbar_arrive(&ctl->tq_full[slot]);
                 const int type = m.type & 0xff;
                 if (type == kTaskExit) break;
-                if (type == kTaskGateUp || type == kTaskDown) {
+                if (is_gemm(type)) {
                     // claim the next task now: the atomic's latency hides behind the loads
                     claim = atomicAdd(&p.hdr->q_head, 1);
                     if (!produce_task(gemm_of(m), ring, ctl, ps, wc, pol_w, pol_b)) break;
@@ -931,7 +1069,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 mbar_arrive(&ctl->tq_empty[slot]);
                 const int type = m.type & 0xff;
                 if (type == kTaskExit) break;
-                if (type == kTaskGateUp || type == kTaskDown)
+                if (is_gemm(type))
                     if (!mma_task(gemm_of(m), ring, ctl, ms, tmem, wc)) break;
             }
         }
@@ -953,9 +1091,17 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             if (type == kTaskExit) break;
             TraceScope trace_scope{p, type, m.a, m.b, p.trace ? globaltimer_ns() : 0ull,
                                    p.trace != nullptr && wtid == 0};
-            if (type != kTaskGateUp && type != kTaskDown) {  // SIMT task on the leased ring
-                bool ok;
-                if (type == kTaskRouter)
+            if (!is_gemm(type)) {  // SIMT task on the leased ring
+                bool ok = true;
+                if (type == kTaskNorm) {
+                    norm_task(p, P, m.a);
+                    fence_proxy_async_global();  // x_hat is read by TMA and bulk copies
+                    worker_sync();
+                    if (wtid == 0) {
+                        __threadfence();
+                        red_release_add(&p.hdr->ev_norm, 1);
+                    }
+                } else if (type == kTaskRouter)
                     ok = router_task(p, P, m.a, m.b, scratch, ring, ctl, &tm_wr, wc, sphase, es.seq);
                 else if (type == kTaskPermute)
                     ok = permute_task(p, P, m.a, m.b, scratch, ring, ctl, wc, sphase, es.seq);
@@ -965,12 +1111,83 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 ring_return(ctl);
                 continue;
             }
-            const bool two = type == kTaskGateUp || wide;
+            const bool two = type == kTaskGateUp || type == kTaskShGateUp || wide;
             uint32_t acc, acc1;
             if (!epi_acquire(ctl, es, two, m.n, tmem, wc, acc, acc1)) break;
             const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
             const uint32_t lane_base = acc + lane_off;
             const int row0 = m.row0, rows = m.rows, n = m.n;
+            if (type == kTaskShGateUp) {  // shared expert: hs = bf16(silu(g) * u)
+                const int Fs = p.Fs, ft = m.b, f = ft * kTileM + q * 32 + lane;
+                for (int c0 = half * 16; c0 < n; c0 += 32) {
+                    float gv[16], uv[16];
+                    tmem_ld16(lane_base + c0, gv);
+                    tmem_ld16(acc1 + lane_off + c0, uv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        if (c0 + c < rows)
+                            p.hs[static_cast<size_t>(row0 + c0 + c) * Fs + f] =
+                                __float2bfloat16_rn(silu_mul(gv[c], uv[c]));
+                }
+                epi_release(ctl, es, true, n);
+                fence_proxy_async_global();  // hs is read back by TMA
+                worker_sync();
+                if (wtid == 0) {
+                    __threadfence();
+                    red_release_add(&p.ev_hs[m.a * kSplitMax + ft / (P.FTS / P.SS)], 1);
+                }
+                continue;
+            }
+            if (type == kTaskShDown) {  // shared expert: ys (or an fp32 partial of F-chunk s)
+                const int s = m.b, ht = m.c, hh = ht * kTileM + q * 32 + lane;
+                const int cap = p.split_rows_cap;
+                for (int c0 = half * 16; c0 < n; c0 += 32) {
+                    float v[16];
+                    tmem_ld16(lane_base + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        if (c0 + c >= rows) continue;
+                        const size_t row = static_cast<size_t>(row0 + c0 + c);
+                        if (S == 1)
+                            p.ys[row * H + hh] = __float2bfloat16_rn(v[c]);
+                        else
+                            p.partial_s[(static_cast<size_t>(s) * cap + row) * H + hh] = v[c];
+                    }
+                }
+                epi_release(ctl, es, false, n);
+                fence_proxy_async_global();  // ys is gathered by bulk copies in the combine
+                worker_sync();
+                bool done = true;
+                if (S > 1) {
+                    int* ev = p.ev_ys + m.a * HT + ht;
+                    if (wtid == 0) {
+                        __threadfence();
+                        ctl->flag = (atom_acq_rel_add(ev, 1) == S - 1) ? 1 : 0;
+                    }
+                    worker_sync();
+                    done = ctl->flag != 0;
+                    if (done) {  // last arriver: sum the partials in chunk order
+                        if (wtid == 0) *ev = 0;  // every chunk arrived: reset for the next call
+                        for (int j = wtid; j < rows * kTileM; j += kWorkers) {
+                            const size_t row = static_cast<size_t>(row0 + j / kTileM);
+                            const int c = ht * kTileM + (j % kTileM);
+                            float sum = 0.0f;
+                            for (int s2 = 0; s2 < S; ++s2)
+                                sum += __ldcg(p.partial_s + (static_cast<size_t>(s2) * cap + row) * H + c);
+                            p.ys[row * H + c] = __float2bfloat16_rn(sum);
+                        }
+                        fence_proxy_async_global();
+                        worker_sync();
+                    }
+                }
+                if (done && wtid == 0) {
+                    __threadfence();
+                    red_release_add(&p.hdr->ev_sdone, 1);
+                }
+                continue;
+            }
             if (type == kTaskGateUp) {
                 const int ft = m.b;
                 const int f = ft * kTileM + q * 32 + lane;
@@ -1089,6 +1306,12 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                         (atom_acq_rel_add(&p.hdr->ev_ydone, ntiles) == target - ntiles) ? 1 : 0;
                 }
                 worker_sync();
+                if (ctl->flag && P.MTS > 0) {  // the shared expert's tiles too
+                    if (wtid == 0)
+                        ctl->flag =
+                            ev_wait_geq(wc, &p.hdr->ev_sdone, P.MTS * HT, kWhereY) ? 1 : 0;
+                    worker_sync();
+                }
                 if (ctl->flag) combine_inline(p, P);
             }
         }
@@ -1112,9 +1335,12 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         const int mt = clean ? ld_relaxed(&p.hdr->total_mt) : p.mt_max;
         for (int i = threadIdx.x; i < mt * kSplitMax; i += kThreads) p.ev_h[i] = 0;
         for (int i = threadIdx.x; i < mt * HT; i += kThreads) p.ev_y[i] = 0;
+        const int mts = clean ? P.MTS : p.mts_max;
+        for (int i = threadIdx.x; i < mts * kSplitMax; i += kThreads) p.ev_hs[i] = 0;
         if (!clean) {  // self-resetting counters an aborted launch may have left behind
             for (int i = threadIdx.x; i < p.mt_max * FT; i += kThreads) p.ev_gu[i] = 0;
             for (int i = threadIdx.x; i < p.r_max; i += kThreads) p.ev_tile[i] = 0;
+            for (int i = threadIdx.x; i < p.mts_max * HT; i += kThreads) p.ev_ys[i] = 0;
         }
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -1128,6 +1354,8 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             hd->ev_ydone = 0;
             hd->split = 0;
             hd->gu_split = 0;
+            hd->ev_norm = 0;
+            hd->ev_sdone = 0;
             hd->abort = 0;
             __threadfence();
             hd->exit_count = 0;
@@ -1152,7 +1380,8 @@ cudaError_t launch_moe(const MoeArgs& a, const CUtensorMap* maps, int grid, int 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, moe_megakernel, maps[0], maps[1], maps[2], maps[3], maps[4],
-                              maps[5], maps[6], maps[7], a);
+                              maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], maps[11],
+                              maps[12], a);
 }
 
 cudaError_t prepare_moe(int smem) {

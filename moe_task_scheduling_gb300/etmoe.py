@@ -43,6 +43,9 @@ _SIGNATURES = {
     "et_last_error_string": (ctypes.c_char_p, []),
     "et_moe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "et_moe_layer": (_i, [_vp] * 11 + [_i, _vp] + [_i] * 5 + [_vp, _sz, _vp, _vp]),
+    "et_moe_block_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "et_moe_block": (_i, [_vp, _vp, ctypes.c_float] + [_vp] * 8 + [_i] + [_vp] * 6 + [_i, _vp] +
+                     [_i] * 5 + [_vp, _sz, _vp, _vp]),
     "et_splitk_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "et_splitk_gemm": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _sz, _vp, _vp]),
     "et_splitk_gemm_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
@@ -134,6 +137,10 @@ def et_moe_workspace_bytes(T_max, H, F, E, k) -> int:
     return load().et_moe_workspace_bytes(T_max, H, F, E, k)
 
 
+def et_moe_block_workspace_bytes(T_max, H, F, E, k, Fs) -> int:
+    return load().et_moe_block_workspace_bytes(T_max, H, F, E, k, Fs)
+
+
 def et_splitk_workspace_bytes(M_max, N, K, split) -> int:
     return load().et_splitk_workspace_bytes(M_max, N, K, split)
 
@@ -164,6 +171,27 @@ def et_moe_layer(x, w_router, router_bias, w_gate, w_up, w_down, out, *, k, T=No
     rc = load().et_moe_layer(
         _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
         _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts), _ptr(perm), T, _ptr(d_T),
+        T_max, H, F, E, k, _ptr(workspace), workspace.numel() if hasattr(workspace, "numel") else 0,
+        _opts(timeout_us, fault_mode, fault_arg, trace), _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def et_moe_block(x, gamma, eps, w_router, router_bias, w_gate, w_up, w_down, ws_gate, ws_up,
+                 ws_down, out, *, k, x_hat=None, T=None, d_T=None, T_max=None, topk_idx=None,
+                 topk_w=None, expert_counts=None, perm=None, workspace, stream=None, timeout_us=0,
+                 fault_mode=0, fault_arg=0, trace=None, check=True):
+    H = x.shape[1]
+    E = w_router.shape[1]
+    F = w_gate.shape[1]
+    Fs = 0 if ws_gate is None else ws_gate.shape[0]
+    T_max = T_max if T_max is not None else x.shape[0]
+    T = T if T is not None else x.shape[0]
+    rc = load().et_moe_block(
+        _ptr(x), _ptr(gamma), float(eps), _ptr(w_router), _ptr(router_bias), _ptr(w_gate),
+        _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), Fs, _ptr(out),
+        _ptr(x_hat), _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts), _ptr(perm), T, _ptr(d_T),
         T_max, H, F, E, k, _ptr(workspace), workspace.numel() if hasattr(workspace, "numel") else 0,
         _opts(timeout_us, fault_mode, fault_arg, trace), _stream(stream))
     if check:
