@@ -8,11 +8,14 @@ L2 is flushed (256 MiB write) before every layer call and each call is timed
 with CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload mixtral|fine|mixtral_block|fine_block|splitk|mlp]
+                  [--workload mixtral|fine|mixtral_block|fine_block|mixtral_chain2|
+                              fine_chain2|splitk|mlp]
 
 The *_block workloads run the fused MoE block (RMSNorm, routed experts, a
 shared expert of width 2F on the fine-grained shape, residual add) over the
-same sweep; they print their own line with their own metric.
+same sweep; they print their own line with their own metric.  The *_chain2
+workloads run two such blocks (each with its own weights) chained in one
+launch, and the same two blocks as two launches for comparison.
 
 Prints ONE JSON line on rank 0.  With N > 1 (torchrun, one process per GPU)
 every rank runs an independent replica of the same sweep ("replicas only":
@@ -46,6 +49,10 @@ METRIC_BLOCK = ("Fused MoE-block tokens/s over the token-count sweep (RMSNorm + 
 # workload -> (configuration, shared-expert width; None = the plain layer)
 MOE_WORKLOADS = {"mixtral": (wl.MIXTRAL, None), "fine": (wl.FINE, None),
                  "mixtral_block": (wl.MIXTRAL, 0), "fine_block": (wl.FINE, 2 * wl.FINE.F)}
+METRIC_CHAIN = ("Two chained fused MoE blocks in one launch: tokens/s over the token-count sweep "
+                "(us per two-block call per T; vs the same blocks as two launches)")
+# workload -> (configuration, shared-expert width, layers)
+CHAIN_WORKLOADS = {"mixtral_chain2": (wl.MIXTRAL, 0, 2), "fine_chain2": (wl.FINE, 2 * wl.FINE.F, 2)}
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["et_device.cuh", "et_gemm.cuh", "et_layout.h", "moe_kernel.cu",
                   "splitk_kernel.cu", "mlp_kernel.cu", "etmoe_api.cu"]
@@ -349,6 +356,238 @@ class DenseBench:
         return res
 
 
+class ChainBench:
+    """n fused blocks chained in one launch (et_moe_chain), and the same blocks
+    as n launches (et_moe_block each) on the previous block's output."""
+
+    def __init__(self, cfg, device, Fs, n):
+        import dataclasses
+        from moe_task_scheduling_gb300 import etmoe
+        self.etmoe = etmoe
+        etmoe.load()
+        self.cfg, self.Fs, self.n, self.dev = cfg, Fs, n, device
+        self.inp, self.blk = [], []
+        for j in range(n):
+            c = dataclasses.replace(cfg, index=cfg.index + 100 * j)
+            self.inp.append(wl.moe_inputs(c, device=device))
+            self.blk.append(wl.block_extra_inputs(c, Fs, device=device))
+        T_max = cfg.T_max
+        self.outs = [torch.empty((T_max, cfg.H), dtype=torch.bfloat16, device=device)
+                     for _ in range(n)]
+        self.descs = []
+        for j in range(n):
+            i, b = self.inp[j], self.blk[j]
+            self.descs.append(etmoe.layer_desc(i["wr"], i["bias"], i["wg"], i["wu"], i["wd"],
+                                               self.outs[j], gamma=b["gamma"], eps=b["eps"],
+                                               ws_gate=b["sg"], ws_up=b["su"], ws_down=b["sd"]))
+        self.ws = etmoe.alloc_workspace(etmoe.et_moe_chain_workspace_bytes(
+            self.descs, T_max, cfg.H, cfg.F, cfg.E, cfg.k), device=device)
+        self.ws1 = [etmoe.alloc_workspace(etmoe.et_moe_block_workspace_bytes(
+            T_max, cfg.H, cfg.F, cfg.E, cfg.k, Fs), device=device) for _ in range(n)]
+        self.d_T = torch.zeros(1, dtype=torch.int32, device=device)
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.stream = torch.cuda.current_stream(device)
+
+    def chain(self, x=None):
+        c = self.cfg
+        self.etmoe.et_moe_chain(self.descs, self.inp[0]["x"] if x is None else x, H=c.H, F=c.F,
+                                E=c.E, k=c.k, T=0, d_T=self.d_T, T_max=c.T_max, workspace=self.ws,
+                                stream=self.stream)
+
+    def separate(self):
+        c = self.cfg
+        x = self.inp[0]["x"]
+        for j in range(self.n):
+            i, b = self.inp[j], self.blk[j]
+            self.etmoe.et_moe_block(x, b["gamma"], b["eps"], i["wr"], i["bias"], i["wg"], i["wu"],
+                                    i["wd"], b["sg"], b["su"], b["sd"], self.outs[j], k=c.k, T=0,
+                                    d_T=self.d_T, T_max=c.T_max, workspace=self.ws1[j],
+                                    stream=self.stream)
+            x = self.outs[j]
+
+    def timed(self, fn, T):
+        self.flush.zero_()
+        self.d_T.fill_(T)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(self.stream)
+        fn()
+        e.record(self.stream)
+        return s, e
+
+
+def run_chain(args, world, rank, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cfg, Fs, n = CHAIN_WORKLOADS[args.workload]
+    b = ChainBench(cfg, device, Fs, n)
+    for _ in range(args.warmup):
+        for T in cfg.T_sweep:
+            b.timed(b.chain, T)
+            b.timed(b.separate, T)
+    torch.cuda.synchronize()
+    gpu_index = local
+    barrier(world)
+    torch.cuda.synchronize()
+    pairs = {T: ([], []) for T in cfg.T_sweep}
+    wall0 = time.perf_counter()
+    with ClockSampler(gpu_index) as clk:
+        for _ in range(args.steps):
+            for T in cfg.T_sweep:
+                pairs[T][0].append(b.timed(b.chain, T))
+                pairs[T][1].append(b.timed(b.separate, T))
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - wall0
+    per_T = {T: ([s.elapsed_time(e) / 1e3 for s, e in c], [s.elapsed_time(e) / 1e3 for s, e in d])
+             for T, (c, d) in pairs.items()}
+    code, detail = b.etmoe.et_status(b.ws)
+    assert code == 0, f"device status {code} ({detail})"
+    t_chain = sum(sum(c) for c, _ in per_T.values())
+    t_sep = sum(sum(d) for _, d in per_T.values())
+    tokens = args.steps * sum(cfg.T_sweep)
+    t_max = max_over_ranks(t_chain, world, device)
+    tok_all = sum_over_ranks(tokens, world, device)
+    if rank != 0:
+        return None
+    pk = peaks()
+    sweep, bytes_total = [], 0.0
+    for T in cfg.T_sweep:
+        c, d = per_T[T]
+        tc, td = statistics.median(c), statistics.median(d)
+        b.d_T.fill_(T)
+        cnts = []
+        for j in range(n):  # experts each block touched (from its own run)
+            cnt = torch.zeros(cfg.E, dtype=torch.int32, device=device)
+            i, bb = b.inp[j], b.blk[j]
+            x = b.inp[0]["x"] if j == 0 else b.outs[j - 1]
+            b.etmoe.et_moe_block(x, bb["gamma"], bb["eps"], i["wr"], i["bias"], i["wg"], i["wu"],
+                                 i["wd"], bb["sg"], bb["su"], bb["sd"], b.outs[j], k=cfg.k, T=0,
+                                 d_T=b.d_T, T_max=cfg.T_max, expert_counts=cnt, workspace=b.ws1[j])
+            cnts.append(int((cnt > 0).sum().item()))
+        by = sum(moe_algorithmic_bytes(cfg, T, t, Fs) for t in cnts)
+        bytes_total += by * len(c)
+        sweep.append({"T": T, "us_chain": round(tc * 1e6, 2), "us_two_launches": round(td * 1e6, 2),
+                      "saved_us": round((td - tc) * 1e6, 2), "experts_touched": cnts,
+                      "hbm_frac": round(by / tc / 1e9 / pk["hbm_gbs"], 4)})
+    achieved = bytes_total / t_chain / 1e9
+    return {
+        "metric": METRIC_CHAIN,
+        "value": round(tok_all / t_max, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) bf16 weights and activations)",
+        "config": {"workload": f"{cfg.name}: {n} fused MoE blocks (Fs={Fs}) chained, T sweep "
+                               f"{list(cfg.T_sweep)}",
+                   "H": cfg.H, "F": cfg.F, "E": cfg.E, "k": cfg.k, "Fs": Fs, "layers": n,
+                   "l2": "flushed (256 MiB write) before every call (chain, or the pair)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "two_launches": {"value": round(tokens / t_sep, 1), "unit": "tokens/s",
+                         "kind": "the same blocks, one et_moe_block launch each"},
+        "sweep": sweep,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": pk["source"] + " (hbm copy, burst)",
+                     "kernel": "moe_megakernel"},
+        "gpu_launches": args.steps * len(cfg.T_sweep),
+        "wall_s_timed": round(wall, 3),
+        "clocks": clk.summary(),
+    }
+
+
+WARMUP_CHILD = r"""
+import json, os, sys, time
+sys.path.insert(0, os.environ["ET_ROOT"])
+import torch
+from moe_task_scheduling_gb300 import workloads as wl
+cfg = wl.MIXTRAL
+dev = torch.device("cuda")
+torch.zeros(1, device=dev)
+inp = wl.moe_inputs(cfg, device=dev)
+out = torch.empty((cfg.T_max, cfg.H), dtype=torch.bfloat16, device=dev)
+d_T = torch.ones(1, dtype=torch.int32, device=dev)
+torch.cuda.synchronize()
+def now():
+    torch.cuda.synchronize()
+    return time.perf_counter()
+t0 = now()
+from moe_task_scheduling_gb300 import etmoe
+etmoe.load()
+t_load = now() - t0
+ws = etmoe.alloc_workspace(etmoe.et_moe_workspace_bytes(cfg.T_max, cfg.H, cfg.F, cfg.E, cfg.k))
+torch.cuda.synchronize()
+def call():
+    etmoe.et_moe_layer(inp["x"], inp["wr"], inp["bias"], inp["wg"], inp["wu"], inp["wd"], out,
+                       k=cfg.k, T=0, d_T=d_T, T_max=cfg.T_max, workspace=ws)
+t0 = now(); call(); t_first = now() - t0
+t0 = now(); call(); t_second = now() - t0
+first_T, steady_T = {}, {}
+for T in cfg.T_sweep[1:]:
+    d_T.fill_(T)
+    t0 = now(); call(); first_T[T] = now() - t0
+for T in cfg.T_sweep:
+    d_T.fill_(T)
+    ts = []
+    for _ in range(3):
+        t0 = now(); call(); ts.append(now() - t0)
+    steady_T[T] = sorted(ts)[1]
+assert etmoe.et_status(ws) == (0, 0)
+print(json.dumps({"load_s": t_load, "first_s": t_first, "second_s": t_second,
+                  "first_T": first_T, "steady_T": steady_T}))
+"""
+
+
+def run_warmup(args):
+    """Warm-up cost of one kernel for every token count: the library's full
+    build (timed into a scratch directory) and one translation unit's compile;
+    then, in a fresh process, the first layer call (library load, kernel
+    attributes, tensor maps, module load, launch) and the first call at each
+    new token count against the steady state, host wall clock with a device
+    synchronise on both sides."""
+    import tempfile
+    from moe_task_scheduling_gb300 import build as B
+    with tempfile.TemporaryDirectory() as d:
+        t0 = time.perf_counter()
+        B.build(force=True, out_dir=d)
+        t_build = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        subprocess.run([B.nvcc()] + B.ARCH + B.NVCC_FLAGS +
+                       ["-c", os.path.join(B.CSRC, "moe_kernel.cu"), "-o", os.path.join(d, "m.o")],
+                       check=True, capture_output=True)
+        t_tu = time.perf_counter() - t0
+    env = dict(os.environ, ET_ROOT=ROOT)
+    r = subprocess.run([sys.executable, "-c", WARMUP_CHILD], capture_output=True, text=True,
+                       env=env, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError("warm-up child failed: " + r.stderr[-2000:])
+    c = json.loads(r.stdout.strip().splitlines()[-1])
+    sweep = [{"T": int(T), "first_call_ms": round(c["first_T"].get(T, c["first_s"]) * 1e3, 3),
+              "steady_ms": round(c["steady_T"][T] * 1e3, 3)}
+             for T in sorted(c["steady_T"], key=int)]
+    n_var = 32
+    return {
+        "metric": "MoE layer warm-up: first call in a fresh process, one compiled kernel for "
+                  "every token count (ms)",
+        "value": round(c["first_s"] * 1e3, 3), "unit": "ms", "higher_is_better": False,
+        "n_gpus": 1, "data": "synthetic (seeded N(0,0.02) bf16 weights)",
+        "config": {"workload": "mixtral MoE layer, T = 1 first, then each T of the sweep",
+                   "clock": "host wall clock, device synchronised before and after"},
+        "library_load_ms": round(c["load_s"] * 1e3, 3),
+        "second_call_ms": round(c["second_s"] * 1e3, 3),
+        "sweep": sweep,
+        "build": {"full_library_s": round(t_build, 2), "moe_kernel_unit_s": round(t_tu, 2),
+                  "per_T_variants_analogue_s": round(n_var * t_tu, 1),
+                  "note": f"a build that specialises the kernel per batch size compiles one "
+                          f"variant per size: {n_var} x the measured unit (derived, not run)"},
+    }
+
+
 def run_dense(args, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
@@ -611,8 +850,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(MOE_WORKLOADS) + ["splitk", "mlp"],
-                    default="mixtral")
+    ap.add_argument("--workload", choices=list(MOE_WORKLOADS) + list(CHAIN_WORKLOADS) +
+                    ["splitk", "mlp", "warmup"], default="mixtral")
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -630,6 +869,10 @@ def main(argv=None):
         line = run_single(args, local) if rank == 0 else None
     elif args.impl == "reference":
         line = run_reference(args, world, rank)
+    elif args.workload in CHAIN_WORKLOADS:
+        line = run_chain(args, world, rank, local)
+    elif args.workload == "warmup":
+        line = run_warmup(args) if rank == 0 else None
     elif args.workload in ("splitk", "mlp"):
         line = run_dense(args, local) if rank == 0 else None
     else:

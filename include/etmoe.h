@@ -142,6 +142,56 @@ int et_moe_block(const void* x, const void* gamma, float eps, const void* w_rout
                  size_t workspace_bytes, const et_opts* opts, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Chained MoE layers in one launch.  Megakernels gain by letting the next
+ * layer's work start where the previous layer's tail leaves SMs idle
+ * ("Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
+ * Kernels": events replace kernel boundaries; "Megakernels ch. 5 - Event
+ * Tensor et le dynamisme", section 5.3: one megakernel for the model).
+ *
+ * Layer l + 1 takes layer l's output as its input.  Its first tasks for a
+ * 16-token tile (RMSNorm in a fused block, else the router) wait on a
+ * per-tile counter that layer l's combine raises by the rows it stored; the
+ * layers' task lists are laid end to end in one task index space, so no
+ * kernel boundary separates them.
+ *
+ * Each layer is described by one et_moe_layer_desc: gamma != NULL makes it a
+ * fused MoE block (et_moe_block's definition: RMSNorm, routed experts,
+ * optional shared expert of width Fs, residual), gamma == NULL a plain MoE
+ * layer (et_moe_layer's definition; Fs must be 0).  All layers share
+ * H, F, E, k and the token count.  out (bf16 [T_max, H], required) is the
+ * layer's output; the optional outputs are as in et_moe_layer / et_moe_block.
+ * 1 <= n_layers <= 4.  The workspace holds one region per layer (its size
+ * depends on each layer's kind and Fs).  Errors: as et_moe_layer; the status
+ * word is in the first layer's region (et_status(workspace)).
+ * ---------------------------------------------------------------------- */
+typedef struct et_moe_layer_desc {
+    const void* gamma;         /* bf16 [H], or NULL for a plain MoE layer */
+    float eps;                 /* RMSNorm epsilon (> 0) when gamma != NULL */
+    const void* w_router;      /* bf16 [H, E] */
+    const float* router_bias;  /* fp32 [E] or NULL */
+    const void* w_gate;        /* bf16 [E, F, H] */
+    const void* w_up;          /* bf16 [E, F, H] */
+    const void* w_down;        /* bf16 [E, H, F] */
+    const void* ws_gate;       /* bf16 [Fs, H] (fused block with Fs > 0) */
+    const void* ws_up;         /* bf16 [Fs, H] */
+    const void* ws_down;       /* bf16 [H, Fs] */
+    int Fs;                    /* shared expert width, multiple of 128, or 0 */
+    void* out;                 /* bf16 [T_max, H]: output, the next layer's input */
+    void* x_hat;               /* optional bf16 [T_max, H] (fused block) */
+    int32_t* topk_idx;         /* optional int32 [T_max, k] */
+    float* topk_w;             /* optional fp32 [T_max, k] */
+    int32_t* expert_counts;    /* optional int32 [E] */
+    int32_t* perm;             /* optional int32 [T_max * k] */
+} et_moe_layer_desc;
+
+size_t et_moe_chain_workspace_bytes(int n_layers, const et_moe_layer_desc* layers, int T_max,
+                                    int H, int F, int E, int k);
+
+int et_moe_chain(int n_layers, const et_moe_layer_desc* layers, const void* x, int T,
+                 const int32_t* d_T, int T_max, int H, int F, int E, int k, void* workspace,
+                 size_t workspace_bytes, const et_opts* opts, void* stream);
+
+/* ------------------------------------------------------------------------
  * Split-K GEMM with event-counter reduction:
  *   Y[M,N] = bf16( sum_{s<split} X[:,K_s] Wt[:,K_s]^T ),  K_s = s-th of `split`
  * equal K chunks.  Each (row tile, column tile, split) is one task; the task

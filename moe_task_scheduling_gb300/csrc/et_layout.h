@@ -36,6 +36,8 @@ constexpr int kGuRowsCap = 128;      // K chunks x T*k rows of gate/up partials 
 
 // split-K GEMM and MLP chain: up to 256 token rows per tile
 constexpr int kWideNMax = 256;
+constexpr int kMaxLayers = 4;        // MoE layers chained in one launch
+constexpr int kLayerShift = 28;      // a task's layer, in the type word
 
 // ---------------------------------------------------------------- workspace header
 
@@ -75,7 +77,8 @@ enum WaitWhere {
     kWhereY = 8,
     kWhereNorm = 9,
     kWhereBoundsT = 10,
-    kWhereStage = 11
+    kWhereStage = 11,
+    kWhereInput = 12
 };
 
 // Task descriptor of the dynamic queue: {type, a, b, c}
@@ -133,6 +136,9 @@ struct MoeArgs {
     int32_t* ev_ys;       // [mts_max * H/128]: shared split partials (self-resetting)
     float* partial_s;     // [kSplitMax, split_rows_cap, H]
     int mts_max;
+    // chained layers: this layer's input is the previous layer's output
+    const int32_t* ev_in;  // [r_max] previous layer's rows written per 16-token tile, or null
+    int32_t* ev_tok;       // [r_max] this layer's rows written per 16-token tile, or null (last layer)
     uint64_t* trace;      // optional per-task trace (see et_opts)
     int trace_cap;
     uint64_t timeout_ns;

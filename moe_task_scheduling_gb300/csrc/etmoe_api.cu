@@ -11,7 +11,7 @@
 #include "et_gemm.cuh"
 
 namespace et {
-cudaError_t launch_moe(const MoeArgs&, const CUtensorMap*, int, int, cudaStream_t);
+cudaError_t launch_moe(const MoeArgs*, const CUtensorMap*, int, int, int, cudaStream_t);
 cudaError_t prepare_moe(int);
 int moe_smem_bytes();
 int moe_ring_bytes();
@@ -150,6 +150,7 @@ struct MoeLayout {
     size_t ev_h, ev_y, ev_tile, ev_gu, logits, hist, base, idx, gw, cnt, off, pos, perm, g_expert,
         g_row0, g_rows, g_n, queue, xp, h, y, partial, gu_part;
     size_t xn, hs, ys, ev_hs, ev_ys, partial_s;  // fused block only (block == true)
+    size_t ev_tok;                               // rows released per 16-token tile (chains)
     size_t total;
 };
 
@@ -161,8 +162,9 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k, bool block = false, 
     L.r_max = ceil_div(T_max, kRouterTile);
     L.mt_max = ceil_div(L.Tk, kMoeNMax) + E;
     const int FT = F / kTileM, HT = H / kTileM;
+    L.mts_max = (block && Fs > 0) ? ceil_div(T_max, kWideNMax) : 0;
     L.q_max = L.r_max * kRouterTile * k + L.mt_max * FT * kGuSplitMax +
-              L.mt_max * kSplitMax * HT + T_max;
+              L.mt_max * kSplitMax * HT + T_max + L.mts_max * kSplitMax * HT;
     L.split_cap = L.Tk < kMoeSplitRowsCap ? L.Tk : kMoeSplitRowsCap;
     L.gu_cap = L.Tk * kGuSplitMax < kGuRowsCap ? L.Tk * kGuSplitMax : kGuRowsCap;
     Carve c;
@@ -189,10 +191,10 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k, bool block = false, 
     L.y = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
     L.partial = c.take(sizeof(float) * static_cast<size_t>(kSplitMax) * L.split_cap * H, 1024);
     L.gu_part = c.take(sizeof(float) * 2 * static_cast<size_t>(L.gu_cap) * F, 1024);
+    L.ev_tok = c.take(sizeof(int) * L.r_max);
     if (block) {
         L.xn = c.take(sizeof(uint16_t) * static_cast<size_t>(T_max) * H, 1024);
         if (Fs > 0) {
-            L.mts_max = ceil_div(T_max, kWideNMax);
             L.ev_hs = c.take(sizeof(int) * L.mts_max * kSplitMax);
             L.ev_ys = c.take(sizeof(int) * L.mts_max * HT);
             L.hs = c.take(sizeof(uint16_t) * static_cast<size_t>(T_max) * Fs, 1024);
@@ -308,21 +310,51 @@ size_t et_moe_workspace_bytes(int T_max, int H, int F, int E, int k) {
 
 namespace {
 
-// The plain layer and the fused block share one launch path; `b.on` selects
-// the block (the shapes were validated by the caller).
-int moe_run(const void* x, const BlockIn& b, const void* w_router, const float* router_bias,
-            const void* w_gate, const void* w_up, const void* w_down, void* out, int32_t* topk_idx,
-            float* topk_w, int32_t* expert_counts, int32_t* perm, int T, const int32_t* d_T,
-            int T_max, int H, int F, int E, int k, void* workspace, size_t workspace_bytes,
+// One layer of a launch as the host sees it (a plain layer, or a fused block
+// when b.on).
+struct LayerIn {
+    BlockIn b;
+    const void* w_router;
+    const float* bias;
+    const void *w_gate, *w_up, *w_down;
+    void* out;
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* expert_counts;
+    int32_t* perm;
+};
+
+// Workspace of a launch: one region per layer, each [header | layout].
+size_t chain_bytes(const LayerIn* layers, int nl, int T_max, int H, int F, int E, int k,
+                   size_t* offs) {
+    size_t off = 0;
+    for (int l = 0; l < nl; ++l) {
+        if (offs) offs[l] = off;
+        off += moe_layout(T_max, H, F, E, k, layers[l].b.on, layers[l].b.Fs).total;
+    }
+    return off;
+}
+
+// Every MoE entry point ends here: nl chained layers (shapes validated by the
+// caller), layer l + 1 reading layer l's output, in one launch.
+int moe_run(const void* x, const LayerIn* layers, int nl, int T, const int32_t* d_T, int T_max,
+            int H, int F, int E, int k, void* workspace, size_t workspace_bytes,
             const et_opts* opts, void* stream) {
-    if (!x || !w_router || !w_gate || !w_up || !w_down || !out)
-        return fail(ET_ERR_INVALID, "x, w_router, w_gate, w_up, w_down and out must be non-NULL");
+    if (nl < 1 || nl > kMaxLayers) return fail(ET_ERR_INVALID, "1 to 4 layers per launch");
+    if (!x) return fail(ET_ERR_INVALID, "x must be non-NULL");
+    if (!aligned<void>(x, 16)) return fail(ET_ERR_INVALID, "tensors must be 16-byte aligned");
+    for (int l = 0; l < nl; ++l) {
+        const LayerIn& li = layers[l];
+        if (!li.w_router || !li.w_gate || !li.w_up || !li.w_down || !li.out)
+            return fail(ET_ERR_INVALID, "w_router, w_gate, w_up, w_down and out must be non-NULL");
+        const void* need16[] = {li.w_router, li.w_gate, li.w_up, li.w_down, li.out};
+        for (const void* q : need16)
+            if (!aligned<void>(q, 16)) return fail(ET_ERR_INVALID, "tensors must be 16-byte aligned");
+    }
     if (!d_T && (T < 0 || T > T_max)) return fail(ET_ERR_INVALID, "T must be in [0, T_max]");
-    const void* need16[] = {x, w_router, w_gate, w_up, w_down, out};
-    for (const void* p : need16)
-        if (!aligned<void>(p, 16)) return fail(ET_ERR_INVALID, "tensors must be 16-byte aligned");
-    const MoeLayout L = moe_layout(T_max, H, F, E, k, b.on, b.Fs);
-    int rc = check_ws(workspace, workspace_bytes, L.total);
+    size_t offs[kMaxLayers];
+    const size_t total = chain_bytes(layers, nl, T_max, H, F, E, k, offs);
+    int rc = check_ws(workspace, workspace_bytes, total);
     if (rc) return rc;
     if (!d_T && T == 0) return ET_OK;
 
@@ -334,100 +366,111 @@ int moe_run(const void* x, const BlockIn& b, const void* w_router, const float* 
         if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(moe)");
         st->moe = true;
     }
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    MoeArgs a{};
-    a.x = static_cast<const bf16*>(x);
-    a.wr = static_cast<const bf16*>(w_router);
-    a.bias = router_bias;
-    a.out = static_cast<bf16*>(out);
-    a.idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + L.idx);
-    a.gw = topk_w ? topk_w : reinterpret_cast<float*>(ws + L.gw);
-    a.cnt = expert_counts ? expert_counts : reinterpret_cast<int32_t*>(ws + L.cnt);
-    a.perm = perm ? perm : reinterpret_cast<int32_t*>(ws + L.perm);
-    a.d_T = d_T;
-    a.T_host = T;
-    a.T_max = T_max;
-    a.H = H;
-    a.F = F;
-    a.E = E;
-    a.k = k;
-    a.hdr = reinterpret_cast<EtHeader*>(ws);
-    a.ev_h = reinterpret_cast<int32_t*>(ws + L.ev_h);
-    a.ev_y = reinterpret_cast<int32_t*>(ws + L.ev_y);
-    a.ev_tile = reinterpret_cast<int32_t*>(ws + L.ev_tile);
-    a.logits = reinterpret_cast<float*>(ws + L.logits);
-    a.hist = reinterpret_cast<int32_t*>(ws + L.hist);
-    a.base = reinterpret_cast<int32_t*>(ws + L.base);
-    a.off = reinterpret_cast<int32_t*>(ws + L.off);
-    a.pos = reinterpret_cast<int32_t*>(ws + L.pos);
-    a.g_expert = reinterpret_cast<int32_t*>(ws + L.g_expert);
-    a.g_row0 = reinterpret_cast<int32_t*>(ws + L.g_row0);
-    a.g_rows = reinterpret_cast<int32_t*>(ws + L.g_rows);
-    a.g_n = reinterpret_cast<int32_t*>(ws + L.g_n);
-    a.queue = reinterpret_cast<int4*>(ws + L.queue);
-    a.xp = reinterpret_cast<bf16*>(ws + L.xp);
-    a.h = reinterpret_cast<bf16*>(ws + L.h);
-    a.y = reinterpret_cast<bf16*>(ws + L.y);
-    a.partial = reinterpret_cast<float*>(ws + L.partial);
-    a.gu_part = reinterpret_cast<float*>(ws + L.gu_part);
-    a.ev_gu = reinterpret_cast<int32_t*>(ws + L.ev_gu);
-    a.gu_cap = L.gu_cap;
-    a.mt_max = L.mt_max;
-    a.q_max = L.q_max;
-    a.split_rows_cap = L.split_cap;
-    a.r_max = L.r_max;
-    a.wr_box = E % 8 == 0 ? (H % 256 == 0 ? 256 : 128) : 0;
-    a.num_ctas = st->sms;
-    a.timeout_ns = timeout_ns_of(opts);
-    a.fault_mode = opts ? opts->fault_mode : 0;
-    a.fault_arg = opts ? opts->fault_arg : 0;
-    a.trace = (opts && opts->trace && opts->trace_cap) ? static_cast<uint64_t*>(opts->trace) : nullptr;
-    a.trace_cap = opts ? static_cast<int>(opts->trace_cap) : 0;
-    if (b.on) {
-        a.gamma = static_cast<const bf16*>(b.gamma);
-        a.eps = b.eps;
-        a.Fs = b.Fs;
-        a.xn = b.x_hat ? static_cast<bf16*>(b.x_hat) : reinterpret_cast<bf16*>(ws + L.xn);
-        if (b.Fs > 0) {
-            a.hs = reinterpret_cast<bf16*>(ws + L.hs);
-            a.ys = reinterpret_cast<bf16*>(ws + L.ys);
-            a.ev_hs = reinterpret_cast<int32_t*>(ws + L.ev_hs);
-            a.ev_ys = reinterpret_cast<int32_t*>(ws + L.ev_ys);
-            a.partial_s = reinterpret_cast<float*>(ws + L.partial_s);
-            a.mts_max = L.mts_max;
+    MoeArgs args[kMaxLayers];
+    CUtensorMap maps[13 * kMaxLayers];
+    for (int l = 0; l < nl; ++l) {
+        const LayerIn& li = layers[l];
+        const BlockIn& b = li.b;
+        const MoeLayout L = moe_layout(T_max, H, F, E, k, b.on, b.Fs);
+        uint8_t* ws = static_cast<uint8_t*>(workspace) + offs[l];
+        MoeArgs& a = args[l];
+        a = MoeArgs{};
+        a.x = static_cast<const bf16*>(l == 0 ? x : layers[l - 1].out);
+        a.wr = static_cast<const bf16*>(li.w_router);
+        a.bias = li.bias;
+        a.out = static_cast<bf16*>(li.out);
+        a.idx = li.topk_idx ? li.topk_idx : reinterpret_cast<int32_t*>(ws + L.idx);
+        a.gw = li.topk_w ? li.topk_w : reinterpret_cast<float*>(ws + L.gw);
+        a.cnt = li.expert_counts ? li.expert_counts : reinterpret_cast<int32_t*>(ws + L.cnt);
+        a.perm = li.perm ? li.perm : reinterpret_cast<int32_t*>(ws + L.perm);
+        a.d_T = d_T;
+        a.T_host = T;
+        a.T_max = T_max;
+        a.H = H;
+        a.F = F;
+        a.E = E;
+        a.k = k;
+        a.hdr = reinterpret_cast<EtHeader*>(ws);
+        a.ev_h = reinterpret_cast<int32_t*>(ws + L.ev_h);
+        a.ev_y = reinterpret_cast<int32_t*>(ws + L.ev_y);
+        a.ev_tile = reinterpret_cast<int32_t*>(ws + L.ev_tile);
+        a.logits = reinterpret_cast<float*>(ws + L.logits);
+        a.hist = reinterpret_cast<int32_t*>(ws + L.hist);
+        a.base = reinterpret_cast<int32_t*>(ws + L.base);
+        a.off = reinterpret_cast<int32_t*>(ws + L.off);
+        a.pos = reinterpret_cast<int32_t*>(ws + L.pos);
+        a.g_expert = reinterpret_cast<int32_t*>(ws + L.g_expert);
+        a.g_row0 = reinterpret_cast<int32_t*>(ws + L.g_row0);
+        a.g_rows = reinterpret_cast<int32_t*>(ws + L.g_rows);
+        a.g_n = reinterpret_cast<int32_t*>(ws + L.g_n);
+        a.queue = reinterpret_cast<int4*>(ws + L.queue);
+        a.xp = reinterpret_cast<bf16*>(ws + L.xp);
+        a.h = reinterpret_cast<bf16*>(ws + L.h);
+        a.y = reinterpret_cast<bf16*>(ws + L.y);
+        a.partial = reinterpret_cast<float*>(ws + L.partial);
+        a.gu_part = reinterpret_cast<float*>(ws + L.gu_part);
+        a.ev_gu = reinterpret_cast<int32_t*>(ws + L.ev_gu);
+        a.gu_cap = L.gu_cap;
+        a.mt_max = L.mt_max;
+        a.q_max = L.q_max;
+        a.split_rows_cap = L.split_cap;
+        a.r_max = L.r_max;
+        a.wr_box = E % 8 == 0 ? (H % 256 == 0 ? 256 : 128) : 0;
+        a.num_ctas = st->sms;
+        a.timeout_ns = timeout_ns_of(opts);
+        a.fault_mode = (opts && l == 0) ? opts->fault_mode : 0;
+        a.fault_arg = (opts && l == 0) ? opts->fault_arg : 0;
+        a.trace = (opts && opts->trace && opts->trace_cap) ? static_cast<uint64_t*>(opts->trace)
+                                                           : nullptr;
+        a.trace_cap = opts ? static_cast<int>(opts->trace_cap) : 0;
+        a.ev_in = l > 0 ? args[l - 1].ev_tok : nullptr;
+        a.ev_tok = l + 1 < nl ? reinterpret_cast<int32_t*>(ws + L.ev_tok) : nullptr;
+        if (b.on) {
+            a.gamma = static_cast<const bf16*>(b.gamma);
+            a.eps = b.eps;
+            a.Fs = b.Fs;
+            a.xn = b.x_hat ? static_cast<bf16*>(b.x_hat) : reinterpret_cast<bf16*>(ws + L.xn);
+            if (b.Fs > 0) {
+                a.hs = reinterpret_cast<bf16*>(ws + L.hs);
+                a.ys = reinterpret_cast<bf16*>(ws + L.ys);
+                a.ev_hs = reinterpret_cast<int32_t*>(ws + L.ev_hs);
+                a.ev_ys = reinterpret_cast<int32_t*>(ws + L.ev_ys);
+                a.partial_s = reinterpret_cast<float*>(ws + L.partial_s);
+                a.mts_max = L.mts_max;
+            }
+        }
+
+        CUtensorMap* mp = maps + 13 * l;
+        const uint64_t EF = static_cast<uint64_t>(E) * F, EH = static_cast<uint64_t>(E) * H;
+        if ((rc = make_map(&mp[0], li.w_gate, EF, H, kTileM, "w_gate"))) return rc;
+        if ((rc = make_map(&mp[1], li.w_up, EF, H, kTileM, "w_up"))) return rc;
+        if ((rc = make_map(&mp[2], li.w_down, EH, F, kTileM, "w_down"))) return rc;
+        if ((rc = make_map(&mp[3], a.xp, L.Tk, H, kBBoxRows, "permuted x"))) return rc;
+        if ((rc = make_map(&mp[4], a.h, L.Tk, F, kBBoxRows, "h"))) return rc;
+        if (a.wr_box) {
+            if ((rc = make_map_plain(&mp[5], li.w_router, H, E, 8, a.wr_box, "w_router"))) return rc;
+        } else {
+            mp[5] = mp[0];  // unused: the router weight is read in place
+        }
+        a.b_wide = L.Tk >= kBBoxRowsWide ? 1 : 0;
+        if (a.b_wide) {
+            if ((rc = make_map(&mp[6], a.xp, L.Tk, H, kBBoxRowsWide, "permuted x"))) return rc;
+            if ((rc = make_map(&mp[7], a.h, L.Tk, F, kBBoxRowsWide, "h"))) return rc;
+        } else {
+            mp[6] = mp[3];
+            mp[7] = mp[4];
+        }
+        for (int i = 8; i < 13; ++i) mp[i] = mp[0];  // unused unless the shared expert runs
+        if (b.on && b.Fs > 0) {
+            const uint64_t Fs = static_cast<uint64_t>(b.Fs);
+            if ((rc = make_map(&mp[8], b.ws_gate, Fs, H, kTileM, "ws_gate"))) return rc;
+            if ((rc = make_map(&mp[9], b.ws_up, Fs, H, kTileM, "ws_up"))) return rc;
+            if ((rc = make_map(&mp[10], b.ws_down, H, Fs, kTileM, "ws_down"))) return rc;
+            if ((rc = make_map(&mp[11], a.xn, T_max, H, kBBoxRows, "x_hat"))) return rc;
+            if ((rc = make_map(&mp[12], a.hs, T_max, Fs, kBBoxRows, "shared h"))) return rc;
         }
     }
-
-    CUtensorMap maps[13];
-    const uint64_t EF = static_cast<uint64_t>(E) * F, EH = static_cast<uint64_t>(E) * H;
-    if ((rc = make_map(&maps[0], w_gate, EF, H, kTileM, "w_gate"))) return rc;
-    if ((rc = make_map(&maps[1], w_up, EF, H, kTileM, "w_up"))) return rc;
-    if ((rc = make_map(&maps[2], w_down, EH, F, kTileM, "w_down"))) return rc;
-    if ((rc = make_map(&maps[3], a.xp, L.Tk, H, kBBoxRows, "permuted x"))) return rc;
-    if ((rc = make_map(&maps[4], a.h, L.Tk, F, kBBoxRows, "h"))) return rc;
-    if (a.wr_box) {
-        if ((rc = make_map_plain(&maps[5], w_router, H, E, 8, a.wr_box, "w_router"))) return rc;
-    } else {
-        maps[5] = maps[0];  // unused: the router weight is read in place
-    }
-    a.b_wide = L.Tk >= kBBoxRowsWide ? 1 : 0;
-    if (a.b_wide) {
-        if ((rc = make_map(&maps[6], a.xp, L.Tk, H, kBBoxRowsWide, "permuted x"))) return rc;
-        if ((rc = make_map(&maps[7], a.h, L.Tk, F, kBBoxRowsWide, "h"))) return rc;
-    } else {
-        maps[6] = maps[3];
-        maps[7] = maps[4];
-    }
-    for (int i = 8; i < 13; ++i) maps[i] = maps[0];  // unused unless the shared expert runs
-    if (b.on && b.Fs > 0) {
-        const uint64_t Fs = static_cast<uint64_t>(b.Fs);
-        if ((rc = make_map(&maps[8], b.ws_gate, Fs, H, kTileM, "ws_gate"))) return rc;
-        if ((rc = make_map(&maps[9], b.ws_up, Fs, H, kTileM, "ws_up"))) return rc;
-        if ((rc = make_map(&maps[10], b.ws_down, H, Fs, kTileM, "ws_down"))) return rc;
-        if ((rc = make_map(&maps[11], a.xn, T_max, H, kBBoxRows, "x_hat"))) return rc;
-        if ((rc = make_map(&maps[12], a.hs, T_max, Fs, kBBoxRows, "shared h"))) return rc;
-    }
-    cudaError_t e = launch_moe(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_moe(args, maps, nl, st->sms, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "launch of the MoE megakernel");
     return ET_OK;
 }
@@ -444,10 +487,9 @@ int et_moe_layer(const void* x, const void* w_router, const float* router_bias, 
     g_last_error.clear();
     std::string why;
     if (!moe_shape_ok(T_max, H, F, E, k, &why)) return fail(ET_ERR_UNSUPPORTED, why);
-    BlockIn b{};
-    return moe_run(x, b, w_router, router_bias, w_gate, w_up, w_down, out, topk_idx, topk_w,
-                   expert_counts, perm, T, d_T, T_max, H, F, E, k, workspace, workspace_bytes, opts,
-                   stream);
+    LayerIn li{BlockIn{}, w_router, router_bias, w_gate, w_up, w_down, out, topk_idx, topk_w,
+               expert_counts, perm};
+    return moe_run(x, &li, 1, T, d_T, T_max, H, F, E, k, workspace, workspace_bytes, opts, stream);
 }
 
 size_t et_moe_block_workspace_bytes(int T_max, int H, int F, int E, int k, int Fs) {
@@ -472,9 +514,77 @@ int et_moe_block(const void* x, const void* gamma, float eps, const void* w_rout
     const void* need16[] = {gamma, ws_gate, ws_up, ws_down, x_hat};
     for (const void* q : need16)
         if (q && !aligned<void>(q, 16)) return fail(ET_ERR_INVALID, "tensors must be 16-byte aligned");
-    BlockIn b{true, gamma, eps, Fs, ws_gate, ws_up, ws_down, x_hat};
-    return moe_run(x, b, w_router, router_bias, w_gate, w_up, w_down, out, topk_idx, topk_w,
-                   expert_counts, perm, T, d_T, T_max, H, F, E, k, workspace, workspace_bytes, opts,
+    LayerIn li{BlockIn{true, gamma, eps, Fs, ws_gate, ws_up, ws_down, x_hat}, w_router,
+               router_bias, w_gate, w_up, w_down, out, topk_idx, topk_w, expert_counts, perm};
+    return moe_run(x, &li, 1, T, d_T, T_max, H, F, E, k, workspace, workspace_bytes, opts, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validate a chain's descriptors and turn them into launch layers.
+int chain_layers(int n_layers, const et_moe_layer_desc* d, int T_max, int H, int F, int E, int k,
+                 LayerIn* out, std::string* why) {
+    if (n_layers < 1 || n_layers > kMaxLayers || !d) {
+        *why = "n_layers must be in [1, 4] and layers non-NULL";
+        return ET_ERR_INVALID;
+    }
+    for (int l = 0; l < n_layers; ++l) {
+        const et_moe_layer_desc& q = d[l];
+        const bool block = q.gamma != nullptr;
+        if (block ? !block_shape_ok(T_max, H, F, E, k, q.Fs, why)
+                  : !moe_shape_ok(T_max, H, F, E, k, why))
+            return ET_ERR_UNSUPPORTED;
+        if (!block && q.Fs != 0) {
+            *why = "a layer without gamma has no shared expert (Fs must be 0)";
+            return ET_ERR_INVALID;
+        }
+        if (block) {
+            if (!(q.eps > 0.0f) || !std::isfinite(q.eps)) {
+                *why = "eps must be finite and > 0";
+                return ET_ERR_INVALID;
+            }
+            if (q.Fs > 0 && (!q.ws_gate || !q.ws_up || !q.ws_down)) {
+                *why = "ws_gate, ws_up and ws_down must be non-NULL when Fs > 0";
+                return ET_ERR_INVALID;
+            }
+            const void* need16[] = {q.gamma, q.ws_gate, q.ws_up, q.ws_down, q.x_hat};
+            for (const void* v : need16)
+                if (v && !aligned<void>(v, 16)) {
+                    *why = "tensors must be 16-byte aligned";
+                    return ET_ERR_INVALID;
+                }
+        }
+        out[l] = LayerIn{BlockIn{block, q.gamma, q.eps, block ? q.Fs : 0, q.ws_gate, q.ws_up,
+                                 q.ws_down, q.x_hat},
+                         q.w_router, q.router_bias, q.w_gate, q.w_up, q.w_down, q.out,
+                         q.topk_idx, q.topk_w, q.expert_counts, q.perm};
+    }
+    return ET_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t et_moe_chain_workspace_bytes(int n_layers, const et_moe_layer_desc* layers, int T_max,
+                                    int H, int F, int E, int k) {
+    LayerIn li[kMaxLayers];
+    std::string why;
+    if (chain_layers(n_layers, layers, T_max, H, F, E, k, li, &why) != ET_OK) return 0;
+    return chain_bytes(li, n_layers, T_max, H, F, E, k, nullptr);
+}
+
+int et_moe_chain(int n_layers, const et_moe_layer_desc* layers, const void* x, int T,
+                 const int32_t* d_T, int T_max, int H, int F, int E, int k, void* workspace,
+                 size_t workspace_bytes, const et_opts* opts, void* stream) {
+    g_last_error.clear();
+    LayerIn li[kMaxLayers];
+    std::string why;
+    const int rc = chain_layers(n_layers, layers, T_max, H, F, E, k, li, &why);
+    if (rc != ET_OK) return fail(rc, why);
+    return moe_run(x, li, n_layers, T, d_T, T_max, H, F, E, k, workspace, workspace_bytes, opts,
                    stream);
 }
 

@@ -32,17 +32,27 @@
 // tasks; split-K partials summed through events; symbolic batch size) and
 // "Megakernels ch. 5 - Event Tensor et le dynamisme" section 5.5 (targets
 // computed on the GPU before waiting; online balancing with atomics).
+#include <cstring>
+
 #include "et_gemm.cuh"
 
 namespace et {
 
-struct MoeMaps {
-    const CUtensorMap* wg;
-    const CUtensorMap* wu;
-    const CUtensorMap* wd;
-    const CUtensorMap* xp;
-    const CUtensorMap* h;
+// One layer's tensor maps: its weights and its staging buffers (gate, up,
+// down; permuted x and h in 16- and 64-row boxes; router weight; the fused
+// block's shared expert, x_hat and shared h).
+struct MoeLayerMaps {
+    CUtensorMap wg, wu, wd, xp, h, wr, xp64, h64, sg, su, sd, xn, hs;
 };
+
+// The kernel parameter: nl chained layers; layer l + 1 reads layer l's output.
+struct MoeLaunch {
+    MoeLayerMaps m[kMaxLayers];
+    MoeArgs a[kMaxLayers];
+    int nl;
+};
+
+__device__ __forceinline__ int layer_of(const TaskMsg& m) { return (m.type >> kLayerShift) & 3; }
 
 __device__ __forceinline__ void unpack8(const uint4& raw, float (&v)[8]) {
     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
@@ -73,6 +83,7 @@ constexpr int kMoeScratch = 18432;
 constexpr int kHistOff = kRouterTile * 256 * 4;  // int [256]
 constexpr int kSelOff = kHistOff + 256 * 4;      // int [16 * 8]
 constexpr int kPermOff = 8192;                   // int [128] entries, int [128] rows
+constexpr int kPlanOff = kSelOff + 512;          // MoePlan [kMaxLayers], set once per launch
 
 // ------------------------------------------------------------------ trace
 
@@ -210,11 +221,13 @@ struct MoePlan {
     int CT, NC;    // tokens per combine task; combine tasks
     int NP;        // permute tasks in the queue (0: one router tile, permuted inline)
     bool stage;    // router tiles stage x and their weight chunk in the ring
-    // fused block: norm tasks (16 rows each), shared expert row tiles (256 rows),
-    // F-tiles and down split; the static prefix [norm][router][shared gate/up]
-    // [shared down] precedes the routing-driven queue
+    // fused block: norm tasks (16 rows each; none when the router tiles stage
+    // and normalise their rows), shared expert row tiles (256 rows), F-tiles and
+    // down split; the static prefix [norm][router][shared gate/up] precedes the
+    // routing-driven queue, which holds the shared down tiles
     int NRN, MTS, FTS, SS, NSG, NSD, NS0;
 };
+static_assert(kPlanOff + kMaxLayers * sizeof(MoePlan) <= kMoeScratch, "plans fit the scratch");
 
 __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint32_t ring_bytes) {
     const int E = p.E, k = p.k, H = p.H;
@@ -222,10 +235,10 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     P.T = T;
     P.R = ceil_div(T, kRouterTile);
     // Split the router's experts into chunks when there are few router tiles,
-    // so a small batch still spreads over many CTAs; a chunk keeps at least one
-    // expert per worker warp (or all of E).
+    // so a small batch still spreads over many CTAs; a chunk keeps at least two
+    // experts (or all of E).
     const int want = P.R > 0 ? max(1, G / P.R) : 1;
-    const int ecmin = min(E, kWorkers / 32);
+    const int ecmin = min(E, 2);
     P.C = 1;  // chunk counts are powers of two (a cheap, uniform search)
     for (int d = 2; d <= E; d <<= 1)
         if (E % d == 0 && d <= want && E / d >= ecmin) P.C = d;
@@ -235,10 +248,11 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     if (p.wr_box > 0) {
         const uint32_t xpad = (static_cast<uint32_t>(min(T, kRouterTile) * H * 2) + 1023u) & ~1023u;
         const uint32_t hp = static_cast<uint32_t>(wr_rows_pad(H, p.wr_box));
+        const uint32_t gb = p.gamma ? static_cast<uint32_t>(H) * 2u : 0u;  // gamma, fused norm
         for (int d = P.C; d <= E && !P.stage; d <<= 1) {
             if (E % d) break;
             const int nb = wr_blocks(E / d);
-            if (nb > 0 && xpad + static_cast<uint32_t>(nb) * hp * 16u <= ring_bytes) {
+            if (nb > 0 && xpad + static_cast<uint32_t>(nb) * hp * 16u + gb <= ring_bytes) {
                 P.C = d;
                 P.stage = true;
             }
@@ -254,7 +268,8 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     P.NP = P.R > 1 ? P.R * P.Q : 0;
     const int HT = H / kTileM;
     const bool block = p.gamma != nullptr;
-    P.NRN = block ? P.R : 0;
+    // a staged router tile normalises its own rows; otherwise NORM tasks do
+    P.NRN = (block && !P.stage) ? P.R : 0;
     P.MTS = (block && p.Fs > 0) ? ceil_div(T, kWideNMax) : 0;
     P.FTS = p.Fs / kTileM;
     P.SS = 1;
@@ -268,13 +283,46 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     }
     P.NSG = P.MTS * P.FTS;
     P.NSD = P.MTS * P.SS * HT;
-    P.NS0 = P.NRN + P.R * P.C + P.NSG + P.NSD;
+    P.NS0 = P.NRN + P.R * P.C + P.NSG;  // shared down tiles are queued by the scan
     return P;
 }
 
 __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, uint8_t* smem,
                                           const Ring& ring, Ctl* ctl, const WaitCtx& wc,
                                           uint32_t& sphase, uint32_t& seq);
+
+// ------------------------------------------------------------------ chained layers
+
+// This layer's input rows of router tile r are the previous layer's output:
+// wait (worker thread 0, bounded) until that layer's combine has released
+// them.  Every worker then fences, so the rows can be read by bulk copies.
+__device__ __forceinline__ bool wait_input(const MoeArgs& p, const MoePlan& P, int r, Ctl* ctl,
+                                           const WaitCtx& wc) {
+    if (!p.ev_in) return true;
+    if (wtid_() == 0)
+        ctl->flag = ev_wait_geq(wc, p.ev_in + r, min(kRouterTile, P.T - r * kRouterTile),
+                                kWhereInput) ? 1 : 0;
+    worker_sync();
+    const bool ok = ctl->flag != 0;
+    fence_proxy_async_global();
+    worker_sync();  // the flag is read before any later task writes it
+    return ok;
+}
+
+// Output rows [t0, t0 + nt) are stored: release them to the next layer, one
+// count per row, on the counter of each 16-token tile they fall in.
+__device__ __forceinline__ void release_output(const MoeArgs& p, int t0, int nt) {
+    if (!p.ev_tok || nt <= 0) return;
+    fence_proxy_async_global();  // read back by bulk copies in the next layer
+    worker_sync();
+    if (wtid_() == 0) {
+        __threadfence();
+        for (int r = t0 / kRouterTile; r * kRouterTile < t0 + nt; ++r) {
+            const int lo = max(t0, r * kRouterTile), hi = min(t0 + nt, (r + 1) * kRouterTile);
+            red_release_add(p.ev_tok + r, hi - lo);
+        }
+    }
+}
 
 // ------------------------------------------------------------------ NORM (fused block)
 
@@ -307,6 +355,36 @@ __device__ __forceinline__ void norm_task(const MoeArgs& p, const MoePlan& P, in
     }
 }
 
+// x_hat of a staged router tile in place, the arithmetic of norm_task (gamma
+// staged too); warp w takes rows w, w + 8.  With `store` the rows also go to
+// x_hat in global memory (for the permute and the shared expert).
+__device__ __forceinline__ void norm_rows_staged(const MoeArgs& p, bf16* xs, const bf16* gs,
+                                                 int t0, int nt, bool store) {
+    const int H = p.H, warp = wtid_() >> 5, lane = wtid_() & 31;
+    for (int t = warp; t < nt; t += kWorkers / 32) {
+        bf16* xr = xs + static_cast<size_t>(t) * H;
+        float acc = 0.0f;
+        for (int h = lane; h < H; h += 32) {
+            const float v = bf2f(xr[h]);
+            acc = fmaf(v, v, acc);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) acc = acc + __shfl_down_sync(0xffffffffu, acc, off);
+        float rr = 0.0f;
+        if (lane == 0)
+            rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, static_cast<float>(H)), p.eps)));
+        rr = __shfl_sync(0xffffffffu, rr, 0);
+        for (int h = lane; h < H; h += 32)
+            xr[h] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(bf2f(xr[h]), rr), bf2f(gs[h])));
+        if (store) {
+            __syncwarp();
+            uint4* dst = reinterpret_cast<uint4*>(p.xn + static_cast<size_t>(t0 + t) * H);
+            const uint4* src = reinterpret_cast<const uint4*>(xr);
+            for (int v = lane; v < H / 8; v += 32) dst[v] = src[v];
+        }
+    }
+}
+
 // Logits of router tile r for expert chunk c.  With staging, the token rows
 // (one bulk copy) and the chunk's 8-expert weight blocks (TMA boxes) are
 // copied into the ring, which the workers hold on lease for the task.  With
@@ -324,13 +402,16 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     const int t0 = r * kRouterTile, nt = min(kRouterTile, P.T - t0);
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
     const int e0 = c * P.EC, ec = P.EC;
-    if (p.gamma) {  // fused block: route x_hat, once every norm task is done
+    // fused block: a staged tile normalises its rows itself (NRN == 0);
+    // otherwise it routes x_hat once every norm task is done
+    const bool own_norm = p.gamma && P.NRN == 0;
+    if (p.gamma && !own_norm) {
         if (wtid_() == 0) ctl->flag = ev_wait_geq(wc, &p.hdr->ev_norm, P.NRN, kWhereNorm) ? 1 : 0;
         worker_sync();
         if (!ctl->flag) return false;
         fence_proxy_async_global();  // x_hat rows written by generic stores, read by bulk copies
     }
-    const bf16* xsrc = p.gamma ? p.xn : p.x;
+    const bf16* xsrc = (p.gamma && !own_norm) ? p.xn : p.x;
     const bf16* xb = xsrc + static_cast<size_t>(t0) * H;
     const bf16* wb = p.wr + e0;
     int o = 0, rs = E, blk = 8;
@@ -341,9 +422,13 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
         const int box = p.wr_box, hp = wr_rows_pad(H, box);
         const int eb0 = e0 >> 3, nb = ((e0 + ec + 7) >> 3) - eb0;
         uint8_t* wdst = ring.base + xpad;
+        uint8_t* gdst = wdst + static_cast<size_t>(nb) * hp * 16;  // gamma (own norm)
+        const uint32_t gbytes = own_norm ? static_cast<uint32_t>(H) * 2u : 0u;
         if (wtid_() == 0) {
-            mbar_arrive_expect_tx(&ctl->sbar, xbytes + static_cast<uint32_t>(nb * hp * 16));
+            mbar_arrive_expect_tx(&ctl->sbar,
+                                  xbytes + static_cast<uint32_t>(nb * hp * 16) + gbytes);
             bulk_g2s(ring.base, xb, xbytes, &ctl->sbar);
+            if (own_norm) bulk_g2s(gdst, p.gamma, gbytes, &ctl->sbar);
             const uint64_t pol = policy_evict_last();
             for (int b = 0; b < nb; ++b)
                 for (int h0 = 0; h0 < hp; h0 += box)
@@ -351,6 +436,19 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
                                 (eb0 + b) * 8, h0, pol);
         }
         if (!staging_wait(ctl, sphase, wc, seq)) return false;
+        if (own_norm) {  // x -> x_hat in place; chunk 0 publishes the rows
+            norm_rows_staged(p, reinterpret_cast<bf16*>(ring.base),
+                             reinterpret_cast<const bf16*>(gdst), t0, nt, c == 0);
+            worker_sync();
+            if (c == 0) {
+                fence_proxy_async_global();  // x_hat is read by TMA and bulk copies
+                worker_sync();
+                if (wtid_() == 0) {
+                    __threadfence();
+                    red_release_add(&p.hdr->ev_norm, 1);
+                }
+            }
+        }
         tm = phase_mark(p, 0, tm);
         xb = reinterpret_cast<const bf16*>(ring.base);
         wb = reinterpret_cast<const bf16*>(wdst);
@@ -596,16 +694,19 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     if (wtid_() == 0) {
         const int total_mt = mtb_s[E];
         // split of the down projection: with few output tiles, the smallest
-        // divisor of FT (<= 8) that gives the grid about three tasks a CTA
+        // divisor of FT (<= 8) that gives the grid about four tasks a CTA (the
+        // last wave of long tasks leaves CTAs idle); chunks keep >= 4 k-blocks,
+        // and >= 8 once the grid has three tasks a CTA
         int S = 1;
         if (T * k <= p.split_rows_cap && total_mt > 0 && total_mt * HT < 3 * p.num_ctas) {
             const int down = total_mt * HT;
             int best = 1;
             for (int d = 2; d <= kSplitMax; ++d) {
                 if (FT % d) continue;
-                if (p.F / kBlockK / d < 4) break;  // keep >= 4 k-blocks a chunk
+                const int kbc = p.F / kBlockK / d;
+                if (kbc < 4 || (down * best >= 3 * p.num_ctas && kbc < 8)) break;
                 best = d;
-                if (down * d >= 3 * p.num_ctas) break;
+                if (down * d >= 4 * p.num_ctas) break;
             }
             S = best;
         }
@@ -653,9 +754,9 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     // each expert's h rows are read half as often) when tiles are tall.
     const int wide = (S == 1 && HT % 2 == 0 && T * k >= 64 * total_mt) ? 1 : 0;
     const int u = (FT / S) * KC, d = wide ? HT / 2 : HT, NCH = total_mt * S;
-    const int n_perm = P.NP, n_tiles = NCH * (u + d);
+    const int n_perm = P.NP, n_tiles = NCH * (u + d), n_sd = P.NSD;
     const int n_cb = P.NC > 1 ? P.NC : 0;  // a single combine runs inline (last down tile)
-    const int total = n_perm + n_tiles + n_cb;
+    const int total = n_perm + n_tiles + n_sd + n_cb;
     if (total > p.q_max) {  // cannot happen for a valid workspace; fail loudly
         if (wtid_() == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereQueue);
         return false;
@@ -667,9 +768,17 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         qd[2 * q + 1] = make_int4(0, 0, 0, 0);
     }
     for (int q = wtid_(); q < n_cb; q += kWorkers) {
-        const int qq = n_perm + n_tiles + q;
+        const int qq = n_perm + n_tiles + n_sd + q;
         qd[2 * qq] = make_int4(kTaskCombine, q, 0, 0);
         qd[2 * qq + 1] = make_int4(0, 0, 0, 0);
+    }
+    // fused block: the shared expert's down tiles (row tile, F-chunk, output
+    // tile), after the routed gate/up tiles, by when their inputs are done
+    for (int i = wtid_(); i < n_sd; i += kWorkers) {
+        const int qq = n_perm + NCH * u + i, mt = i / (P.SS * HT);
+        const int row0 = mt * kWideNMax, rows = min(kWideNMax, T - row0);
+        qd[2 * qq] = make_int4(kTaskShDown | (P.SS << 8), mt, (i % (P.SS * HT)) / HT, i % HT);
+        qd[2 * qq + 1] = make_int4(0, row0, rows, (rows + 15) / 16 * 16);
     }
     {  // a warp per chunk, its lanes over the chunk's entries
         const int warp = wtid_() >> 5, lane = wtid_() & 31;
@@ -687,7 +796,7 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
             }
             const int n = n_s[e], mt = g - mtb_s[e];
             const int4 gi = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n), n);
-            const int gu0 = n_perm + c * u, dn0 = n_perm + NCH * u + c * d;
+            const int gu0 = n_perm + c * u, dn0 = n_perm + NCH * u + n_sd + c * d;
             for (int r = lane; r < u; r += 32) {
                 qd[2 * (gu0 + r)] = make_int4(kTaskGateUp | flags, g, sc * (FT / S) + r / KC, r % KC);
                 qd[2 * (gu0 + r) + 1] = gi;
@@ -743,7 +852,7 @@ __device__ __forceinline__ bool permute_rows(const MoeArgs& p, const MoePlan& P,
         bulk_g2s(ring.base, (p.gamma ? p.xn : p.x) + static_cast<size_t>(t0 + tl0 + c0) * H,
                  nc * rowb, &ctl->sbar);
     };
-    if (p.gamma && wtid_() == 0) fence_proxy_async_global();  // x_hat: generic stores
+    if ((p.gamma || p.ev_in) && wtid_() == 0) fence_proxy_async_global();  // generic stores
     if (!x_staged && ntok > 0 && wtid_() == 0) issue(0);
     const int* iv = ie_src;
     if (!iv) {
@@ -877,6 +986,7 @@ __device__ __forceinline__ bool combine_task(const MoeArgs& p, const MoePlan& P,
             mbar_arrive_expect_tx(&ctl->sbar, min(per, nt - b0 - per) * rpt * rowb);
         worker_sync();
     }
+    release_output(p, t0, nt);
     return true;
 }
 
@@ -913,93 +1023,114 @@ __device__ __forceinline__ void combine_inline(const MoeArgs& p, const MoePlan& 
 
 // ------------------------------------------------------------------ queue pop
 
-// Producer thread: next task of this CTA (EXIT when the queue is exhausted or
-// the launch aborted).  `claim` is a queue index taken ahead of time (or -1);
-// the published queue size is read once and kept in `q_total`.
-__device__ __forceinline__ TaskMsg pop_task(const MoeArgs& p, const WaitCtx& wc, const MoePlan& P,
-                                            int claim, int& q_total) {
+// The producer's place in the task index space of the launch: layer l's
+// tasks are [base, base + NS0 + q_total) -- its static prefix, then its queue
+// (size known once its scan has run); the next layer's follow.
+struct QCursor {
+    int layer = 0, base = 0, qt = -1;
+};
+
+// Static-prefix task j of a layer: [norm][router][shared gate/up].
+__device__ __forceinline__ TaskMsg static_task(const MoeArgs& p, const MoePlan& P, int j) {
+    TaskMsg m{};
+    if (j < P.NRN) {  // fused block: RMSNorm of router tile j's rows
+        m.type = kTaskNorm;
+        m.a = j;
+        return m;
+    }
+    j -= P.NRN;
+    const int nr = P.R * P.C;
+    if (j < nr) {
+        m.type = kTaskRouter;
+        m.a = j / P.C;
+        m.b = j % P.C;
+        return m;
+    }
+    j -= nr;  // fused block: shared expert gate/up tiles (no routing needed)
+    m.type = kTaskShGateUp;
+    m.a = j / P.FTS;  // row tile
+    m.b = j % P.FTS;  // F-tile
+    m.row0 = m.a * kWideNMax;
+    m.rows = min(kWideNMax, P.T - m.row0);
+    m.n = (m.rows + 15) / 16 * 16;
+    return m;
+}
+
+// Producer thread: next task of this CTA (EXIT when every layer's tasks are
+// taken or the launch aborted).  `claim` is a task index taken ahead of time
+// (or -1); claims only grow, so the cursor only moves forward.
+template <bool kChain>
+__device__ __forceinline__ TaskMsg pop_task(const MoeLaunch& Lc, const MoePlan* plans,
+                                            const WaitCtx& wc, int claim, QCursor& cur) {
     TaskMsg m{};
     m.type = kTaskExit;
-    if (aborted(wc) || P.R == 0) return m;  // T == 0: no task at all
-    int i = claim >= 0 ? claim : atomicAdd(&p.hdr->q_head, 1);
-    if (i < P.NRN) {  // fused block: RMSNorm of router tile i's rows
-        m.type = kTaskNorm;
-        m.a = i;
-        return m;
-    }
-    i -= P.NRN;
-    const int nr = P.R * P.C;
-    if (i < nr) {
-        m.type = kTaskRouter;
-        m.a = i / P.C;
-        m.b = i % P.C;
-        return m;
-    }
-    i -= nr;
-    if (i < P.NSG + P.NSD) {  // fused block: shared expert tiles (no routing needed)
-        const int HT = p.H / kTileM;
-        if (i < P.NSG) {
-            m.type = kTaskShGateUp;
-            m.a = i / P.FTS;  // row tile
-            m.b = i % P.FTS;  // F-tile
-        } else {
-            i -= P.NSG;
-            m.type = kTaskShDown | (P.SS << 8);
-            m.a = i / (P.SS * HT);
-            m.b = (i % (P.SS * HT)) / HT;  // F-chunk
-            m.c = i % HT;                  // output tile
+    if (aborted(wc) || plans[0].R == 0) return m;  // T == 0: no task at all
+    const int i = claim >= 0 ? claim : atomicAdd(&Lc.a[0].hdr->q_head, 1);
+    for (;;) {
+        const int l = kChain ? cur.layer : 0;
+        const MoeArgs& p = Lc.a[l];
+        const MoePlan& P = plans[l];
+        const int j = i - cur.base;
+        if (j < P.NS0) {
+            m = static_task(p, P, j);
+            break;
         }
-        m.row0 = m.a * kWideNMax;
-        m.rows = min(kWideNMax, P.T - m.row0);
-        m.n = (m.rows + 15) / 16 * 16;
-        return m;
+        if (cur.qt < 0) {
+            if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
+            cur.qt = ld_relaxed(&p.hdr->q_total);
+        }
+        if (j < P.NS0 + cur.qt) {
+            const int q = j - P.NS0;
+            const int4 d0 = __ldcg(p.queue + 2 * q), d1 = __ldcg(p.queue + 2 * q + 1);
+            m.type = d0.x;
+            m.a = d0.y;
+            m.b = d0.z;
+            m.c = d0.w;
+            m.e = d1.x;
+            m.row0 = d1.y;
+            m.rows = d1.z;
+            m.n = d1.w;
+            break;
+        }
+        if (!kChain || cur.layer + 1 >= Lc.nl) return m;  // every layer's tasks are taken
+        cur.base += P.NS0 + cur.qt;
+        ++cur.layer;
+        cur.qt = -1;
     }
-    const int j = i - P.NSG - P.NSD;
-    if (q_total < 0) {
-        if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
-        q_total = ld_relaxed(&p.hdr->q_total);
-    }
-    if (j >= q_total) return m;
-    const int4 d0 = __ldcg(p.queue + 2 * j), d1 = __ldcg(p.queue + 2 * j + 1);
-    m.type = d0.x;
-    m.a = d0.y;
-    m.b = d0.z;
-    m.c = d0.w;
-    m.e = d1.x;
-    m.row0 = d1.y;
-    m.rows = d1.z;
-    m.n = d1.w;
+    if (kChain) m.type |= cur.layer << kLayerShift;
     return m;
 }
 
 // ------------------------------------------------------------------ the kernel
 
-__global__ void __launch_bounds__(kThreads, 1)
-moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
-               const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xp,
-               const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wr,
-               const __grid_constant__ CUtensorMap tm_xp64, const __grid_constant__ CUtensorMap tm_h64,
-               const __grid_constant__ CUtensorMap tm_sg, const __grid_constant__ CUtensorMap tm_su,
-               const __grid_constant__ CUtensorMap tm_sd, const __grid_constant__ CUtensorMap tm_xn,
-               const __grid_constant__ CUtensorMap tm_hs, const __grid_constant__ MoeArgs p) {
+// kChain: more than one layer.  A single layer takes every argument from
+// layer 0 at fixed parameter offsets; a chain indexes the layer per task.
+template <bool kChain>
+__global__ void __launch_bounds__(kThreads, 1) moe_megakernel(const __grid_constant__ MoeLaunch Lc) {
     extern __shared__ uint8_t smem_raw[];
     const uint64_t t_start = globaltimer_ns();
     Ring ring;
     uint8_t* scratch;
     Ctl* ctl = cta_setup(smem_raw, kMoeScratch, ring, &scratch);
-    const WaitCtx wc{p.hdr, p.timeout_ns};
+    const MoeArgs& p0 = Lc.a[0];  // the launch's header: queue head, status, abort, exit count
+    const WaitCtx wc{p0.hdr, p0.timeout_ns};
     const uint32_t tmem = ctl->tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) trace_rec(p, 0, 2, 0, 0, t_start, globaltimer_ns());
+    if (threadIdx.x == 0) trace_rec(p0, 0, 2, 0, 0, t_start, globaltimer_ns());
 
-    int T = p.T_host;
-    if (p.d_T) T = *reinterpret_cast<const volatile int32_t*>(p.d_T);
-    if (T < 0 || T > p.T_max) {
+    int T = p0.T_host;
+    if (p0.d_T) T = *reinterpret_cast<const volatile int32_t*>(p0.d_T);
+    if (T < 0 || T > p0.T_max) {
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereBoundsT);
         T = 0;
     }
-    const MoePlan P = moe_plan(p, T, static_cast<int>(gridDim.x), ring.bytes);
-    const int FT = p.F / kTileM, HT = p.H / kTileM;
+    // every layer's plan, once per CTA (shared memory, read by every role)
+    MoePlan* plans = reinterpret_cast<MoePlan*>(scratch + kPlanOff);
+    if (static_cast<int>(threadIdx.x) < Lc.nl)
+        plans[threadIdx.x] =
+            moe_plan(Lc.a[threadIdx.x], T, static_cast<int>(gridDim.x), ring.bytes);
+    __syncthreads();
+    const int FT = p0.F / kTileM, HT = p0.H / kTileM;  // shapes shared by every layer
 
     auto is_gemm = [](int type) {
         return type == kTaskGateUp || type == kTaskDown || type == kTaskShGateUp ||
@@ -1007,23 +1138,27 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
     };
     auto gemm_of = [&](const TaskMsg& m) {
         const int type = m.type & 0xff, S = (m.type >> 8) & 0xff, KC = (m.type >> 16) & 0xff;
+        const int l = kChain ? layer_of(m) : 0;
+        const MoeArgs& p = Lc.a[l];
+        const MoeLayerMaps& M = Lc.m[l];
+        const MoePlan& P = plans[l];
         if (type == kTaskShGateUp)  // shared expert over the rows of x_hat
-            return GemmTask{&tm_sg, &tm_su, &tm_xn, nullptr, m.b * kTileM, m.row0, 0,
-                            p.H / kBlockK, m.n, m.b, &p.hdr->ev_norm, P.NRN, kWhereNorm};
+            return GemmTask{&M.sg, &M.su, &M.xn, nullptr, m.b * kTileM, m.row0, 0,
+                            p.H / kBlockK, m.n, m.b, &p.hdr->ev_norm, P.R, kWhereNorm};
         if (type == kTaskShDown) {
             const int fch = p.Fs / S;
-            return GemmTask{&tm_sd, nullptr, &tm_hs, nullptr, m.c * kTileM, m.row0,
+            return GemmTask{&M.sd, nullptr, &M.hs, nullptr, m.c * kTileM, m.row0,
                             m.b * (fch / kBlockK), fch / kBlockK, m.n, m.c,
                             &p.ev_hs[m.a * kSplitMax + m.b], P.FTS / S, kWhereH};
         }
         if (type == kTaskGateUp) {
             const int nkb = p.H / kBlockK / KC;
-            return GemmTask{&tm_wg, &tm_wu, &tm_xp, p.b_wide ? &tm_xp64 : nullptr,
+            return GemmTask{&M.wg, &M.wu, &M.xp, p.b_wide ? &M.xp64 : nullptr,
                             m.e * p.F + m.b * kTileM, m.row0, m.c * nkb, nkb, m.n, m.b,
                             &p.hdr->ev_perm, P.NP, kWherePerm};
         }
         const int fchunk = p.F / S, wide = (m.type >> 24) & 1;
-        return GemmTask{&tm_wd, wide ? &tm_wd : nullptr, &tm_h, p.b_wide ? &tm_h64 : nullptr,
+        return GemmTask{&M.wd, wide ? &M.wd : nullptr, &M.h, p.b_wide ? &M.h64 : nullptr,
                         m.e * p.H + m.c * (kTileM << wide), m.row0, m.b * (fchunk / kBlockK),
                         fchunk / kBlockK, m.n, m.c, &p.ev_h[m.a * kSplitMax + m.b], FT / S,
                         kWhereH, wide ? kTileM : 0};
@@ -1033,13 +1168,14 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         if (lane == 0) {  // producer: pop, hand over, load
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
             ProdState ps;
-            int claim = -1, q_total = -1;
+            QCursor cur;
+            int claim = -1;
             for (int i = 0;; ++i) {
                 // a SIMT task still out on lease: take no further task before it
                 // is done, so SIMT work spreads over the CTAs that are free
                 if (!ring_lease_wait(ctl, ps, wc)) break;
                 const uint64_t tp = globaltimer_ns();
-                const TaskMsg m = pop_task(p, wc, P, claim, q_total);
+                const TaskMsg m = pop_task<kChain>(Lc, plans, wc, claim, cur);
                 claim = -1;
                 const int slot = i % kTaskRing;
                 if (!mbar_wait(wc, &ctl->tq_empty[slot], ((i / kTaskRing) & 1) ^ 1, kWhereQueue))
@@ -1050,12 +1186,12 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                 if (type == kTaskExit) break;
                 if (is_gemm(type)) {
                     // claim the next task now: the atomic's latency hides behind the loads
-                    claim = atomicAdd(&p.hdr->q_head, 1);
+                    claim = atomicAdd(&p0.hdr->q_head, 1);
                     if (!produce_task(gemm_of(m), ring, ctl, ps, wc, pol_w, pol_b)) break;
                 } else {
                     ++ps.leases;  // a SIMT task holds the ring until the workers return it
                 }
-                trace_rec(p, type, 0, m.a, m.b, tp, globaltimer_ns());
+                trace_rec(p0, type, 0, m.a, m.b, tp, globaltimer_ns());
             }
         }
         __syncwarp();
@@ -1076,7 +1212,7 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
         __syncwarp();
     } else if (warp >= kEpiWarp0) {  // workers: epilogues and SIMT tasks
         const int q = warp & 3, half = (warp - kEpiWarp0) >> 2, wtid = wtid_();  // TMEM quadrant, column half
-        const int H = p.H, F = p.F;
+        const int H = p0.H, F = p0.F;
         EpiState es;
         uint32_t sphase = 0;
         for (int i = 0;; ++i) {
@@ -1089,20 +1225,28 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
             const int type = m.type & 0xff, S = (m.type >> 8) & 0xff, KC = (m.type >> 16) & 0xff;
             const int wide = (m.type >> 24) & 1;
             if (type == kTaskExit) break;
+            const int l = kChain ? layer_of(m) : 0;
+            const MoeArgs& p = Lc.a[l];
+            const MoePlan& P = plans[l];
             TraceScope trace_scope{p, type, m.a, m.b, p.trace ? globaltimer_ns() : 0ull,
                                    p.trace != nullptr && wtid == 0};
             if (!is_gemm(type)) {  // SIMT task on the leased ring
                 bool ok = true;
                 if (type == kTaskNorm) {
-                    norm_task(p, P, m.a);
-                    fence_proxy_async_global();  // x_hat is read by TMA and bulk copies
-                    worker_sync();
-                    if (wtid == 0) {
-                        __threadfence();
-                        red_release_add(&p.hdr->ev_norm, 1);
+                    ok = wait_input(p, P, m.a, ctl, wc);
+                    if (ok) {
+                        norm_task(p, P, m.a);
+                        fence_proxy_async_global();  // x_hat is read by TMA and bulk copies
+                        worker_sync();
+                        if (wtid == 0) {
+                            __threadfence();
+                            red_release_add(&p.hdr->ev_norm, 1);
+                        }
                     }
                 } else if (type == kTaskRouter)
-                    ok = router_task(p, P, m.a, m.b, scratch, ring, ctl, &tm_wr, wc, sphase, es.seq);
+                    ok = ((p.gamma && P.NRN > 0) || wait_input(p, P, m.a, ctl, wc)) &&
+                         router_task(p, P, m.a, m.b, scratch, ring, ctl, &Lc.m[l].wr, wc, sphase,
+                                     es.seq);
                 else if (type == kTaskPermute)
                     ok = permute_task(p, P, m.a, m.b, scratch, ring, ctl, wc, sphase, es.seq);
                 else
@@ -1312,53 +1456,67 @@ moe_megakernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant_
                             ev_wait_geq(wc, &p.hdr->ev_sdone, P.MTS * HT, kWhereY) ? 1 : 0;
                     worker_sync();
                 }
-                if (ctl->flag) combine_inline(p, P);
+                if (ctl->flag) {
+                    combine_inline(p, P);
+                    release_output(p, 0, P.T);
+                }
             }
         }
     }
 
     const uint64_t t_exit = globaltimer_ns();
-    const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
+    const bool aborted_run = ld_relaxed(&p0.hdr->abort) != 0;
     cta_teardown(ctl, aborted_run);
-    if (threadIdx.x == 0) trace_rec(p, 0, 3, 0, 0, t_exit, globaltimer_ns());
+    if (threadIdx.x == 0) trace_rec(p0, 0, 3, 0, 0, t_exit, globaltimer_ns());
 
     // Exit protocol: the last CTA out returns every counter to zero.
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        ctl->flag = (atomicAdd(&p.hdr->exit_count, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
+        ctl->flag = (atomicAdd(&p0.hdr->exit_count, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
     }
     __syncthreads();
     if (ctl->flag) {
         __threadfence();
-        const bool clean = ld_relaxed(&p.hdr->abort) == 0 && ld_relaxed(&p.hdr->q_ready) != 0;
-        const int mt = clean ? ld_relaxed(&p.hdr->total_mt) : p.mt_max;
-        for (int i = threadIdx.x; i < mt * kSplitMax; i += kThreads) p.ev_h[i] = 0;
-        for (int i = threadIdx.x; i < mt * HT; i += kThreads) p.ev_y[i] = 0;
-        const int mts = clean ? P.MTS : p.mts_max;
-        for (int i = threadIdx.x; i < mts * kSplitMax; i += kThreads) p.ev_hs[i] = 0;
-        if (!clean) {  // self-resetting counters an aborted launch may have left behind
-            for (int i = threadIdx.x; i < p.mt_max * FT; i += kThreads) p.ev_gu[i] = 0;
-            for (int i = threadIdx.x; i < p.r_max; i += kThreads) p.ev_tile[i] = 0;
-            for (int i = threadIdx.x; i < p.mts_max * HT; i += kThreads) p.ev_ys[i] = 0;
+        const bool aborted_all = ld_relaxed(&p0.hdr->abort) != 0;
+        for (int l = 0; l < (kChain ? Lc.nl : 1); ++l) {
+            const MoeArgs& p = Lc.a[l];
+            const MoePlan& P = plans[l];
+            const bool clean = !aborted_all && ld_relaxed(&p.hdr->q_ready) != 0;
+            const int mt = clean ? ld_relaxed(&p.hdr->total_mt) : p.mt_max;
+            for (int i = threadIdx.x; i < mt * kSplitMax; i += kThreads) p.ev_h[i] = 0;
+            for (int i = threadIdx.x; i < mt * HT; i += kThreads) p.ev_y[i] = 0;
+            const int mts = clean ? P.MTS : p.mts_max;
+            for (int i = threadIdx.x; i < mts * kSplitMax; i += kThreads) p.ev_hs[i] = 0;
+            if (p.ev_tok) {
+                const int nr = clean ? P.R : p.r_max;
+                for (int i = threadIdx.x; i < nr; i += kThreads) p.ev_tok[i] = 0;
+            }
+            if (!clean) {  // self-resetting counters an aborted launch may have left behind
+                for (int i = threadIdx.x; i < p.mt_max * FT; i += kThreads) p.ev_gu[i] = 0;
+                for (int i = threadIdx.x; i < p.r_max; i += kThreads) p.ev_tile[i] = 0;
+                for (int i = threadIdx.x; i < p.mts_max * HT; i += kThreads) p.ev_ys[i] = 0;
+            }
         }
         __syncthreads();
         if (threadIdx.x == 0) {
-            EtHeader* hd = p.hdr;
-            hd->q_head = 0;
-            hd->q_ready = 0;
-            hd->q_total = 0;
-            hd->total_mt = 0;
-            hd->ev_router = 0;
-            hd->ev_perm = 0;
-            hd->ev_ydone = 0;
-            hd->split = 0;
-            hd->gu_split = 0;
-            hd->ev_norm = 0;
-            hd->ev_sdone = 0;
-            hd->abort = 0;
+            for (int l = 0; l < (kChain ? Lc.nl : 1); ++l) {
+                EtHeader* hd = Lc.a[l].hdr;
+                hd->q_head = 0;
+                hd->q_ready = 0;
+                hd->q_total = 0;
+                hd->total_mt = 0;
+                hd->ev_router = 0;
+                hd->ev_perm = 0;
+                hd->ev_ydone = 0;
+                hd->split = 0;
+                hd->gu_split = 0;
+                hd->ev_norm = 0;
+                hd->ev_sdone = 0;
+                hd->abort = 0;
+            }
             __threadfence();
-            hd->exit_count = 0;
+            p0.hdr->exit_count = 0;
         }
     }
 }
@@ -1367,8 +1525,17 @@ int moe_smem_bytes() { return smem_bytes_for(kMoeScratch); }
 int moe_ring_bytes() { return ring_bytes_for(kMoeScratch); }
 
 // Host-side launch (called by the C ABI after validation).
-cudaError_t launch_moe(const MoeArgs& a, const CUtensorMap* maps, int grid, int smem,
+cudaError_t launch_moe(const MoeArgs* a, const CUtensorMap* maps, int nl, int grid, int smem,
                        cudaStream_t stream) {
+    static_assert(sizeof(MoeLayerMaps) == 13 * sizeof(CUtensorMap), "13 maps a layer");
+    if (nl < 1 || nl > kMaxLayers) return cudaErrorInvalidValue;
+    MoeLaunch L;
+    memset(&L, 0, sizeof(L));
+    for (int l = 0; l < nl; ++l) {
+        memcpy(&L.m[l], maps + 13 * l, sizeof(MoeLayerMaps));
+        L.a[l] = a[l];
+    }
+    L.nl = nl;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -1379,13 +1546,16 @@ cudaError_t launch_moe(const MoeArgs& a, const CUtensorMap* maps, int grid, int 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_megakernel, maps[0], maps[1], maps[2], maps[3], maps[4],
-                              maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], maps[11],
-                              maps[12], a);
+    return nl > 1 ? cudaLaunchKernelEx(&cfg, moe_megakernel<true>, L)
+                  : cudaLaunchKernelEx(&cfg, moe_megakernel<false>, L);
 }
 
 cudaError_t prepare_moe(int smem) {
-    return cudaFuncSetAttribute(moe_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(moe_megakernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(moe_megakernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem);
 }
 
 }  // namespace et

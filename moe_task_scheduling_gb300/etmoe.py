@@ -27,6 +27,17 @@ class et_opts(ctypes.Structure):
                 ("trace", ctypes.c_void_p)]
 
 
+class et_moe_layer_desc(ctypes.Structure):
+    _fields_ = [("gamma", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("w_router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("ws_gate", ctypes.c_void_p), ("ws_up", ctypes.c_void_p),
+                ("ws_down", ctypes.c_void_p), ("Fs", ctypes.c_int32), ("out", ctypes.c_void_p),
+                ("x_hat", ctypes.c_void_p), ("topk_idx", ctypes.c_void_p),
+                ("topk_w", ctypes.c_void_p), ("expert_counts", ctypes.c_void_p),
+                ("perm", ctypes.c_void_p)]
+
+
 class EtError(RuntimeError):
     def __init__(self, code, msg):
         super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
@@ -46,6 +57,8 @@ _SIGNATURES = {
     "et_moe_block_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "et_moe_block": (_i, [_vp, _vp, ctypes.c_float] + [_vp] * 8 + [_i] + [_vp] * 6 + [_i, _vp] +
                      [_i] * 5 + [_vp, _sz, _vp, _vp]),
+    "et_moe_chain_workspace_bytes": (_sz, [_i, _vp, _i, _i, _i, _i, _i]),
+    "et_moe_chain": (_i, [_i, _vp, _vp, _i, _vp] + [_i] * 5 + [_vp, _sz, _vp, _vp]),
     "et_splitk_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "et_splitk_gemm": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _sz, _vp, _vp]),
     "et_splitk_gemm_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
@@ -194,6 +207,42 @@ def et_moe_block(x, gamma, eps, w_router, router_bias, w_gate, w_up, w_down, ws_
         _ptr(x_hat), _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts), _ptr(perm), T, _ptr(d_T),
         T_max, H, F, E, k, _ptr(workspace), workspace.numel() if hasattr(workspace, "numel") else 0,
         _opts(timeout_us, fault_mode, fault_arg, trace), _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def layer_desc(w_router, router_bias, w_gate, w_up, w_down, out, *, gamma=None, eps=1e-5,
+               ws_gate=None, ws_up=None, ws_down=None, x_hat=None, topk_idx=None, topk_w=None,
+               expert_counts=None, perm=None):
+    """One layer of et_moe_chain (gamma given: a fused block)."""
+    return et_moe_layer_desc(
+        _ptr(gamma), float(eps), _ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up),
+        _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down),
+        0 if ws_gate is None else ws_gate.shape[0], _ptr(out), _ptr(x_hat), _ptr(topk_idx),
+        _ptr(topk_w), _ptr(expert_counts), _ptr(perm))
+
+
+def _desc_array(layers):
+    arr = (et_moe_layer_desc * len(layers))(*layers)
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def et_moe_chain_workspace_bytes(layers, T_max, H, F, E, k) -> int:
+    arr, ptr = _desc_array(layers)
+    return load().et_moe_chain_workspace_bytes(len(layers), ptr, T_max, H, F, E, k)
+
+
+def et_moe_chain(layers, x, *, H, F, E, k, T=None, d_T=None, T_max=None, workspace, stream=None,
+                 timeout_us=0, fault_mode=0, fault_arg=0, trace=None, check=True):
+    """Chained layers in one launch: layers[l + 1] reads layers[l].out."""
+    T_max = T_max if T_max is not None else x.shape[0]
+    T = T if T is not None else x.shape[0]
+    arr, ptr = _desc_array(layers)
+    rc = load().et_moe_chain(len(layers), ptr, _ptr(x), T, _ptr(d_T), T_max, H, F, E, k,
+                             _ptr(workspace),
+                             workspace.numel() if hasattr(workspace, "numel") else 0,
+                             _opts(timeout_us, fault_mode, fault_arg, trace), _stream(stream))
     if check:
         _check(rc)
     return rc
