@@ -216,6 +216,8 @@ class MoeBench:
         self.dev = device
         self.inp = wl.moe_inputs(cfg, device=device)
         self.blk = wl.block_extra_inputs(cfg, Fs, device=device) if Fs is not None else None
+        if self.blk is not None:  # the skew in units of the router input's (x_hat's) logit std
+            self.blk["bias"] = wl.block_router_bias(self.inp["bias"])
         T_max = cfg.T_max
         self.out = torch.empty((T_max, cfg.H), dtype=torch.bfloat16, device=device)
         self.cnt = torch.zeros((cfg.E,), dtype=torch.int32, device=device)
@@ -231,7 +233,7 @@ class MoeBench:
         if self.blk is not None:
             b = self.blk
             self.etmoe.et_moe_block(x if x is not None else i["x"], b["gamma"], b["eps"], i["wr"],
-                                    i["bias"], i["wg"], i["wu"], i["wd"], b["sg"], b["su"], b["sd"],
+                                    b["bias"], i["wg"], i["wu"], i["wd"], b["sg"], b["su"], b["sd"],
                                     out if out is not None else self.out, k=self.cfg.k, T=0,
                                     d_T=self.d_T, T_max=self.cfg.T_max, expert_counts=self.cnt,
                                     workspace=self.ws, stream=self.stream)
@@ -371,13 +373,14 @@ class ChainBench:
             c = dataclasses.replace(cfg, index=cfg.index + 100 * j)
             self.inp.append(wl.moe_inputs(c, device=device))
             self.blk.append(wl.block_extra_inputs(c, Fs, device=device))
+            self.blk[-1]["bias"] = wl.block_router_bias(self.inp[-1]["bias"])
         T_max = cfg.T_max
         self.outs = [torch.empty((T_max, cfg.H), dtype=torch.bfloat16, device=device)
                      for _ in range(n)]
         self.descs = []
         for j in range(n):
             i, b = self.inp[j], self.blk[j]
-            self.descs.append(etmoe.layer_desc(i["wr"], i["bias"], i["wg"], i["wu"], i["wd"],
+            self.descs.append(etmoe.layer_desc(i["wr"], b["bias"], i["wg"], i["wu"], i["wd"],
                                                self.outs[j], gamma=b["gamma"], eps=b["eps"],
                                                ws_gate=b["sg"], ws_up=b["su"], ws_down=b["sd"]))
         self.ws = etmoe.alloc_workspace(etmoe.et_moe_chain_workspace_bytes(
@@ -399,7 +402,7 @@ class ChainBench:
         x = self.inp[0]["x"]
         for j in range(self.n):
             i, b = self.inp[j], self.blk[j]
-            self.etmoe.et_moe_block(x, b["gamma"], b["eps"], i["wr"], i["bias"], i["wg"], i["wu"],
+            self.etmoe.et_moe_block(x, b["gamma"], b["eps"], i["wr"], b["bias"], i["wg"], i["wu"],
                                     i["wd"], b["sg"], b["su"], b["sd"], self.outs[j], k=c.k, T=0,
                                     d_T=self.d_T, T_max=c.T_max, workspace=self.ws1[j],
                                     stream=self.stream)
@@ -460,7 +463,7 @@ def run_chain(args, world, rank, local):
             cnt = torch.zeros(cfg.E, dtype=torch.int32, device=device)
             i, bb = b.inp[j], b.blk[j]
             x = b.inp[0]["x"] if j == 0 else b.outs[j - 1]
-            b.etmoe.et_moe_block(x, bb["gamma"], bb["eps"], i["wr"], i["bias"], i["wg"], i["wu"],
+            b.etmoe.et_moe_block(x, bb["gamma"], bb["eps"], i["wr"], bb["bias"], i["wg"], i["wu"],
                                  i["wd"], bb["sg"], bb["su"], bb["sd"], b.outs[j], k=cfg.k, T=0,
                                  d_T=b.d_T, T_max=cfg.T_max, expert_counts=cnt, workspace=b.ws1[j])
             cnts.append(int((cnt > 0).sum().item()))
@@ -712,8 +715,9 @@ def per_op_layer(inp, cfg, T, blk=None):
         x = (xf * torch.rsqrt(xf.square().mean(-1, keepdim=True) + blk["eps"]) *
              blk["gamma"].float()).to(torch.bfloat16)
     logits = x.float() @ inp["wr"].float()
-    if inp["bias"] is not None:
-        logits = logits + inp["bias"]
+    bias = inp["bias"] if blk is None else blk["bias"]
+    if bias is not None:
+        logits = logits + bias
     w, idx = torch.topk(torch.softmax(logits, dim=-1), cfg.k, dim=-1)
     w = (w / w.sum(dim=-1, keepdim=True)).reshape(-1)
     flat = idx.reshape(-1)
@@ -789,7 +793,9 @@ def cpu_baseline(b, cfg, args):
 def block_bits(blk):
     if blk is None:
         return None
-    return {k: (wl.bits(v) if isinstance(v, torch.Tensor) else v) for k, v in blk.items()}
+    return {k: (wl.bits(v) if isinstance(v, torch.Tensor) and v.dtype == torch.bfloat16 else
+                (v.detach().cpu().numpy() if isinstance(v, torch.Tensor) else v))
+            for k, v in blk.items()}
 
 
 def oracle_call(oracle, hb, bb, cfg, n, threads):
@@ -797,7 +803,7 @@ def oracle_call(oracle, hb, bb, cfg, n, threads):
     if bb is None:
         return lambda: oracle.moe_layer(hb["x"][:n], hb["wr"], hb["bias"], hb["wg"], hb["wu"],
                                         hb["wd"], k=cfg.k, nthreads=threads)
-    return lambda: oracle.moe_block(hb["x"][:n], bb["gamma"], bb["eps"], hb["wr"], hb["bias"],
+    return lambda: oracle.moe_block(hb["x"][:n], bb["gamma"], bb["eps"], hb["wr"], bb["bias"],
                                     hb["wg"], hb["wu"], hb["wd"], bb["sg"], bb["su"], bb["sd"],
                                     k=cfg.k, nthreads=threads)
 
@@ -815,7 +821,11 @@ def run_reference(args, world, rank):
     inp = wl.moe_inputs(cfg, device=dev)
     hb = {k: (wl.bits(v) if v is not None and v.dtype == torch.bfloat16 else
               (None if v is None else v.detach().cpu().numpy())) for k, v in inp.items()}
-    bb = block_bits(wl.block_extra_inputs(cfg, Fs, device=dev)) if Fs is not None else None
+    bb = None
+    if Fs is not None:
+        blk = wl.block_extra_inputs(cfg, Fs, device=dev)
+        blk["bias"] = wl.block_router_bias(inp["bias"])
+        bb = block_bits(blk)
     del inp
     n = args.ref_tokens
     threads = oracle.default_threads()

@@ -339,9 +339,12 @@ __device__ __forceinline__ void norm_task(const MoeArgs& p, const MoePlan& P, in
         if (t >= P.T) break;
         const bf16* xr = p.x + static_cast<size_t>(t) * H;
         float acc = 0.0f;
-        for (int h = lane; h < H; h += 32) {
-            const float v = bf2f(xr[h]);
-            acc = fmaf(v, v, acc);  // v * v is exact: fma == add of the square
+        for (int h0 = lane; h0 < H; h0 += 128) {  // H % 128 == 0; loads issue ahead
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = bf2f(xr[h0 + 32 * u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc = fmaf(v[u], v[u], acc);  // v * v exact in fp32
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) acc = acc + __shfl_down_sync(0xffffffffu, acc, off);
@@ -350,6 +353,7 @@ __device__ __forceinline__ void norm_task(const MoeArgs& p, const MoePlan& P, in
             rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, static_cast<float>(H)), p.eps)));
         rr = __shfl_sync(0xffffffffu, rr, 0);
         bf16* on = p.xn + static_cast<size_t>(t) * H;
+#pragma unroll 4
         for (int h = lane; h < H; h += 32)
             on[h] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(bf2f(xr[h]), rr), bf2f(p.gamma[h])));
     }
@@ -364,9 +368,14 @@ __device__ __forceinline__ void norm_rows_staged(const MoeArgs& p, bf16* xs, con
     for (int t = warp; t < nt; t += kWorkers / 32) {
         bf16* xr = xs + static_cast<size_t>(t) * H;
         float acc = 0.0f;
-        for (int h = lane; h < H; h += 32) {
-            const float v = bf2f(xr[h]);
-            acc = fmaf(v, v, acc);
+        // H is a multiple of 128: blocks of 4 strided loads issue ahead of the
+        // (ordered) accumulation
+        for (int h0 = lane; h0 < H; h0 += 128) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = bf2f(xr[h0 + 32 * u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc = fmaf(v[u], v[u], acc);
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) acc = acc + __shfl_down_sync(0xffffffffu, acc, off);
@@ -374,6 +383,7 @@ __device__ __forceinline__ void norm_rows_staged(const MoeArgs& p, bf16* xs, con
         if (lane == 0)
             rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, static_cast<float>(H)), p.eps)));
         rr = __shfl_sync(0xffffffffu, rr, 0);
+#pragma unroll 4
         for (int h = lane; h < H; h += 32)
             xr[h] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(bf2f(xr[h]), rr), bf2f(gs[h])));
         if (store) {
@@ -607,6 +617,8 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     int* off_s = cnt_s + 256;                   // [257]
     int* n_s = off_s + 264;                     // [256]
     int* mtb_s = n_s + 256;                     // [257]
+    // [mt_max <= 2304]: expert of row tile g (ends below kHistOff; dead before the permute)
+    int* ge_s = mtb_s + 264;
     const int RE = R * E;
     const bool staged = R > 1 && static_cast<size_t>(RE) * 4 <= ring.bytes;
     int* hs = reinterpret_cast<int*>(ring.base);
@@ -730,6 +742,7 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         if (e == E - 1) p.off[E] = off_s[E];
         const int n = n_s[e];
         for (int g = mtb_s[e], mt = 0; g < mtb_s[e + 1]; ++g, ++mt) {
+            ge_s[g] = e;
             p.g_expert[g] = e;
             p.g_row0[g] = off_s[e] + mt * n;
             p.g_rows[g] = min(n, cnt_s[e] - mt * n);
@@ -744,8 +757,9 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         for (int i = wtid_(); i < RE; i += kWorkers) p.base[i] += off_s[i % E];
     }
     tm = phase_mark(p, 7, tm);
-    // Queue: [permute parts][gate/up tiles, by chunk][down tiles, by chunk]
-    // [combine tasks].  A chunk c = (row tile g, F-chunk s) has u gate/up and
+    worker_sync();  // the tile -> expert table is complete
+    // Queue: [permute parts][gate/up tiles, by chunk][shared down tiles (fused
+    // block)][down tiles, by chunk][combine tasks].  A chunk c = (row tile g, F-chunk s) has u gate/up and
     // d down tasks; every down task comes after the gate/up tasks it waits for.
     // (Down tiles placed right behind their chunk's gate/up tiles were
     // measured slower on decode and large batches: popped early, they stall
@@ -780,31 +794,19 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         qd[2 * qq] = make_int4(kTaskShDown | (P.SS << 8), mt, (i % (P.SS * HT)) / HT, i % HT);
         qd[2 * qq + 1] = make_int4(0, row0, rows, (rows + 15) / 16 * 16);
     }
-    {  // a warp per chunk, its lanes over the chunk's entries
-        const int warp = wtid_() >> 5, lane = wtid_() & 31;
-        for (int c = warp; c < NCH; c += kWorkers / 32) {
-            const int g = c / S, sc = c % S;
-            int e = 0;  // the expert of row tile g: mtb_s[e] <= g < mtb_s[e + 1]
-            for (int lo = 0, hi = E - 1; lo <= hi;) {
-                const int mid = (lo + hi) >> 1;
-                if (mtb_s[mid] <= g) {
-                    e = mid;
-                    lo = mid + 1;
-                } else {
-                    hi = mid - 1;
-                }
-            }
+    {  // a thread per entry: chunk c = (row tile g, F-chunk sc) has u gate/up and d down
+        const int dn_base = n_perm + NCH * u + n_sd;
+        for (int q = wtid_(); q < NCH * u; q += kWorkers) {
+            const int c = q / u, r = q % u, g = c / S, sc = c % S, e = ge_s[g];
             const int n = n_s[e], mt = g - mtb_s[e];
-            const int4 gi = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n), n);
-            const int gu0 = n_perm + c * u, dn0 = n_perm + NCH * u + n_sd + c * d;
-            for (int r = lane; r < u; r += 32) {
-                qd[2 * (gu0 + r)] = make_int4(kTaskGateUp | flags, g, sc * (FT / S) + r / KC, r % KC);
-                qd[2 * (gu0 + r) + 1] = gi;
-            }
-            for (int r = lane; r < d; r += 32) {  // r: output tile (of 128, or 256 if wide)
-                qd[2 * (dn0 + r)] = make_int4(kTaskDown | flags, g, sc, r);
-                qd[2 * (dn0 + r) + 1] = gi;
-            }
+            qd[2 * (n_perm + q)] = make_int4(kTaskGateUp | flags, g, sc * (FT / S) + r / KC, r % KC);
+            qd[2 * (n_perm + q) + 1] = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n), n);
+        }
+        for (int q = wtid_(); q < NCH * d; q += kWorkers) {  // r: output tile (of 128, or 256 if wide)
+            const int c = q / d, r = q % d, g = c / S, sc = c % S, e = ge_s[g];
+            const int n = n_s[e], mt = g - mtb_s[e];
+            qd[2 * (dn_base + q)] = make_int4(kTaskDown | flags, g, sc, r);
+            qd[2 * (dn_base + q) + 1] = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n), n);
         }
     }
     worker_sync();

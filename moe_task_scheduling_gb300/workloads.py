@@ -166,6 +166,15 @@ def block_extra_inputs(cfg: MoEConfig, Fs: int, device="cpu", unit_scale=False):
     return dict(gamma=gamma, sg=sg, su=su, sd=sd, eps=1e-5)
 
 
+def block_router_bias(layer_bias, unit_scale=False):
+    """The skewed router bias for a fused block, whose router sees x_hat (unit
+    RMS, gamma ~ 1) instead of x: the same bias in units of the Gaussian logit
+    std of x_hat, i.e. scaled by 1 / x_std (None stays None)."""
+    if layer_bias is None:
+        return None
+    return layer_bias * (1.0 if unit_scale else 1.0 / WEIGHT_STD)
+
+
 def splitk_inputs(cfg: SplitKConfig, device="cpu", M_max: Optional[int] = None, unit_scale=False):
     """X [M_max,K], Wt [N,K] (the weight stored transposed, K contiguous), bf16."""
     M_max = M_max or cfg.M_max
