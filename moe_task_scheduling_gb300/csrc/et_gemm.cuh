@@ -401,9 +401,9 @@ __device__ __forceinline__ void ring_return(Ctl* ctl) {
 // bf16(sum over s in order 0, 1, .. of part[s][r][col]) for r in [r0, r1).
 // part + s * sstride + r * ld + col addresses partial s (fp32); the worker
 // group reads float4 columns with every split's load in flight at once.
+template <int kMaxSplit = 16>
 __device__ __forceinline__ void reduce_slice(const float* part, size_t sstride, int ld, int split,
                                              int r0, int r1, int col0, bf16* Y, int ldy) {
-    constexpr int kMaxSplit = 16;
     const int nv = (r1 - r0) * (kTileM / 4);
     for (int v = static_cast<int>(threadIdx.x) - kEpiWarp0 * 32; v < nv; v += kWorkers) {
         const int row = r0 + v / (kTileM / 4), col = col0 + (v % (kTileM / 4)) * 4;
@@ -421,6 +421,41 @@ __device__ __forceinline__ void reduce_slice(const float* part, size_t sstride, 
                 acc.z = acc.z + q[s].z;
                 acc.w = acc.w + q[s].w;
             }
+        __nv_bfloat162 o[2] = {__floats2bfloat162_rn(acc.x, acc.y), __floats2bfloat162_rn(acc.z, acc.w)};
+        *reinterpret_cast<uint2*>(Y + static_cast<size_t>(row) * ldy + col) =
+            *reinterpret_cast<const uint2*>(o);
+    }
+}
+
+// reduce_slice with at most four splits' loads in flight at a time, and not
+// inlined: callers inside register-tight loops pay a register save only on
+// this (rare) path.  The same sum order.
+static __device__ __noinline__ void reduce_slice4(const float* part, size_t sstride, int ld,
+                                                  int split, int r0, int r1, int col0, bf16* Y,
+                                                  int ldy) {
+    const int nv = (r1 - r0) * (kTileM / 4);
+    for (int v = static_cast<int>(threadIdx.x) - kEpiWarp0 * 32; v < nv; v += kWorkers) {
+        const int row = r0 + v / (kTileM / 4), col = col0 + (v % (kTileM / 4)) * 4;
+        const float* src = part + static_cast<size_t>(row) * ld + col;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int s0 = 0; s0 < split; s0 += 4) {
+            float4 q[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (s0 + i < split) q[i] = __ldcg(reinterpret_cast<const float4*>(src + (s0 + i) * sstride));
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (s0 + i < split) {
+                    if (s0 + i == 0) {
+                        acc = q[0];
+                    } else {
+                        acc.x = acc.x + q[i].x;
+                        acc.y = acc.y + q[i].y;
+                        acc.z = acc.z + q[i].z;
+                        acc.w = acc.w + q[i].w;
+                    }
+                }
+        }
         __nv_bfloat162 o[2] = {__floats2bfloat162_rn(acc.x, acc.y), __floats2bfloat162_rn(acc.z, acc.w)};
         *reinterpret_cast<uint2*>(Y + static_cast<size_t>(row) * ldy + col) =
             *reinterpret_cast<const uint2*>(o);

@@ -272,13 +272,15 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     P.NRN = (block && !P.stage) ? P.R : 0;
     P.MTS = (block && p.Fs > 0) ? ceil_div(T, kWideNMax) : 0;
     P.FTS = p.Fs / kTileM;
+    // the shared down tiles run beside the routed ones: split over F only for
+    // small batches (short tiles, cheap reductions), to about half a task a CTA
     P.SS = 1;
-    if (P.MTS > 0 && T <= p.split_rows_cap && P.MTS * HT < 3 * G) {
+    if (P.MTS > 0 && T <= 128 && T <= p.split_rows_cap && 2 * P.MTS * HT < G) {
         for (int d = 2; d <= kSplitMax; ++d) {
             if (P.FTS % d) continue;
             if (p.Fs / kBlockK / d < 4) break;  // keep >= 4 k-blocks a chunk
             P.SS = d;
-            if (P.MTS * HT * d >= 3 * G) break;
+            if (2 * P.MTS * HT * d >= G) break;
         }
     }
     P.NSG = P.MTS * P.FTS;
@@ -1316,14 +1318,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(const __grid_const
                     done = ctl->flag != 0;
                     if (done) {  // last arriver: sum the partials in chunk order
                         if (wtid == 0) *ev = 0;  // every chunk arrived: reset for the next call
-                        for (int j = wtid; j < rows * kTileM; j += kWorkers) {
-                            const size_t row = static_cast<size_t>(row0 + j / kTileM);
-                            const int c = ht * kTileM + (j % kTileM);
-                            float sum = 0.0f;
-                            for (int s2 = 0; s2 < S; ++s2)
-                                sum += __ldcg(p.partial_s + (static_cast<size_t>(s2) * cap + row) * H + c);
-                            p.ys[row * H + c] = __float2bfloat16_rn(sum);
-                        }
+                        reduce_slice4(p.partial_s, static_cast<size_t>(cap) * H, H, S, row0,
+                                      row0 + rows, ht * kTileM, p.ys, H);
                         fence_proxy_async_global();
                         worker_sync();
                     }
@@ -1426,14 +1422,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(const __grid_const
                 worker_sync();
                 done = ctl->flag != 0;
                 if (done) {  // last arriver: sum the partials in chunk order
-                    for (int j = wtid; j < rows * kTileM; j += kWorkers) {
-                        const size_t row = static_cast<size_t>(row0 + j / kTileM);
-                        const int c = ht * kTileM + (j % kTileM);
-                        float sum = 0.0f;
-                        for (int s2 = 0; s2 < S; ++s2)
-                            sum += __ldcg(p.partial + (static_cast<size_t>(s2) * cap + row) * H + c);
-                        p.y[row * H + c] = __float2bfloat16_rn(sum);
-                    }
+                    reduce_slice4(p.partial, static_cast<size_t>(cap) * H, H, S, row0, row0 + rows,
+                                  ht * kTileM, p.y, H);
                     fence_proxy_async_global();
                     worker_sync();
                 }
