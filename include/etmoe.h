@@ -207,6 +207,23 @@ int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t*
                    const et_opts* opts, void* stream);
 
 /* ------------------------------------------------------------------------
+ * The same split-K GEMM with Blackwell's Cluster Launch Control as the work
+ * queue ("Megakernels ch. 5 - Event Tensor et le dynamisme", section 5.5: a
+ * running CTA can take over the work of a CTA that has not started).
+ *
+ * One CTA per tile task (ceil(M_max/256) * N/128 * split CTAs); each running
+ * CTA cancels not-yet-launched CTAs (clusterlaunchcontrol.try_cancel) and
+ * runs their tasks itself, so the hardware balances the work and no
+ * cooperative launch is needed.  The task that completes a tile's counter
+ * sums the tile's partials in split order (the last arriver).  Arguments,
+ * workspace (et_splitk_workspace_bytes), results and errors as et_splitk_gemm;
+ * the two calls may share a workspace, not concurrently.
+ * ---------------------------------------------------------------------- */
+int et_splitk_gemm_clc(const void* X, const void* Wt, void* Y, int M, const int32_t* d_M,
+                       int M_max, int N, int K, int split, void* workspace,
+                       size_t workspace_bytes, const et_opts* opts, void* stream);
+
+/* ------------------------------------------------------------------------
  * Split-K GEMM that allocates nothing (the source paper has no counterpart;
  * this entry point exists for callers that cannot allocate).
  *

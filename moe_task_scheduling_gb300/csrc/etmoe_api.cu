@@ -18,6 +18,9 @@ int moe_ring_bytes();
 cudaError_t launch_splitk(const SplitKArgs&, const CUtensorMap*, int, int, cudaStream_t);
 cudaError_t prepare_splitk(int);
 int splitk_smem_bytes();
+cudaError_t launch_splitk_clc(const SplitKArgs&, const CUtensorMap*, int, int, cudaStream_t);
+cudaError_t prepare_splitk_clc(int);
+int splitk_clc_smem_bytes();
 cudaError_t launch_mlp(const MlpArgs&, const CUtensorMap*, int, int, cudaStream_t);
 cudaError_t prepare_mlp(int);
 int mlp_smem_bytes();
@@ -43,7 +46,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     bool ready = false;
     int sms = 0;
-    bool moe = false, splitk = false, mlp = false;
+    bool moe = false, splitk = false, splitk_clc = false, mlp = false;
 };
 
 std::mutex g_mu;
@@ -594,10 +597,15 @@ size_t et_splitk_workspace_bytes(int M_max, int N, int K, int split) {
     return splitk_layout(M_max, N, K, split).total;
 }
 
-int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t* d_M, int M_max,
-                   int N, int K, int split, void* workspace, size_t workspace_bytes,
-                   const et_opts* opts, void* stream) {
-    g_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+// The split-K GEMM: the static, cooperative schedule (clc == false) or the
+// Cluster Launch Control work queue (clc == true).
+int splitk_run(const void* X, const void* Wt, void* Y, int M, const int32_t* d_M, int M_max, int N,
+               int K, int split, void* workspace, size_t workspace_bytes, const et_opts* opts,
+               void* stream, bool clc) {
     if (M_max < 1 || M_max > (1 << 20)) return fail(ET_ERR_INVALID, "M_max must be in [1, 2^20]");
     if (N < 128 || N % 128 || N > (1 << 20))
         return fail(ET_ERR_UNSUPPORTED, "N must be a positive multiple of 128");
@@ -614,11 +622,12 @@ int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t*
     if (!d_M && M == 0) return ET_OK;
     DeviceState* st = nullptr;
     if ((rc = device_state(&st, nullptr))) return rc;
-    const int smem = splitk_smem_bytes();
-    if (!st->splitk) {
-        cudaError_t e = prepare_splitk(smem);
+    const int smem = clc ? splitk_clc_smem_bytes() : splitk_smem_bytes();
+    bool& prepared = clc ? st->splitk_clc : st->splitk;
+    if (!prepared) {
+        cudaError_t e = clc ? prepare_splitk_clc(smem) : prepare_splitk(smem);
         if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(splitk)");
-        st->splitk = true;
+        prepared = true;
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     SplitKArgs a{};
@@ -645,9 +654,33 @@ int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t*
     } else {
         maps[2] = maps[1];
     }
-    cudaError_t e = launch_splitk(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
+    // the hardware queue's grid: one CTA per tile task of every M tile up to M_max
+    const long long tasks = static_cast<long long>(ceil_div(M_max, kWideNMax)) * (N / kTileM) * split;
+    cudaError_t e = clc ? launch_splitk_clc(a, maps, static_cast<int>(tasks), smem,
+                                            static_cast<cudaStream_t>(stream))
+                        : launch_splitk(a, maps, st->sms, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "launch of the split-K kernel");
     return ET_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int et_splitk_gemm(const void* X, const void* Wt, void* Y, int M, const int32_t* d_M, int M_max,
+                   int N, int K, int split, void* workspace, size_t workspace_bytes,
+                   const et_opts* opts, void* stream) {
+    g_last_error.clear();
+    return splitk_run(X, Wt, Y, M, d_M, M_max, N, K, split, workspace, workspace_bytes, opts,
+                      stream, false);
+}
+
+int et_splitk_gemm_clc(const void* X, const void* Wt, void* Y, int M, const int32_t* d_M,
+                       int M_max, int N, int K, int split, void* workspace,
+                       size_t workspace_bytes, const et_opts* opts, void* stream) {
+    g_last_error.clear();
+    return splitk_run(X, Wt, Y, M, d_M, M_max, N, K, split, workspace, workspace_bytes, opts,
+                      stream, true);
 }
 
 size_t et_mlp_workspace_bytes(int B_max, int H, int F) {

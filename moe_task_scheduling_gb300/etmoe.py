@@ -62,6 +62,7 @@ _SIGNATURES = {
     "et_splitk_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "et_splitk_gemm": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _sz, _vp, _vp]),
     "et_splitk_gemm_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "et_splitk_gemm_clc": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _sz, _vp, _vp]),
     "et_mlp_workspace_bytes": (_sz, [_i, _i, _i]),
     "et_mlp_chain": (_i, [_vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _vp,
                           _sz, _vp, _vp]),
@@ -257,6 +258,21 @@ def et_splitk_gemm(X, Wt, Y, *, split, M=None, d_M=None, M_max=None, workspace, 
     rc = load().et_splitk_gemm(_ptr(X), _ptr(Wt), _ptr(Y), M, _ptr(d_M), M_max, N, K, split,
                                _ptr(workspace), workspace.numel(), _opts(timeout_us),
                                _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def et_splitk_gemm_clc(X, Wt, Y, *, split, M=None, d_M=None, M_max=None, workspace, stream=None,
+                       timeout_us=0, check=True):
+    """Split-K GEMM with the Cluster Launch Control work queue (same results)."""
+    K = X.shape[1]
+    N = Wt.shape[0]
+    M_max = M_max if M_max is not None else X.shape[0]
+    M = M if M is not None else X.shape[0]
+    rc = load().et_splitk_gemm_clc(_ptr(X), _ptr(Wt), _ptr(Y), M, _ptr(d_M), M_max, N, K, split,
+                                   _ptr(workspace), workspace.numel(), _opts(timeout_us),
+                                   _stream(stream))
     if check:
         _check(rc)
     return rc
