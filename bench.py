@@ -695,6 +695,11 @@ def run_ours(args, world, rank, local):
     }
     if world == 1 and not args.no_per_op:
         line["per_op_baseline"] = per_op_baseline(b, cfg)
+        # torch._grouped_mm is not run: on the GPU machine's torch build it failed with an
+        # unspecified launch failure on this GPU
+        line["per_op_grouped_baseline"] = {
+            "unavailable": "torch._grouped_mm failed with an unspecified launch failure on this "
+                           "GPU (GPU box torch build); not run"}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(b, cfg, args)
     return line

@@ -85,7 +85,6 @@ struct GemmTask {
     int b_row;               // first activation row
     int kb0, nkb;            // k-blocks [kb0, kb0 + nkb), 64 elements each
     int n;                   // UMMA N: multiple of 16, <= 256
-    int rot;                 // the k loop starts at fill rot % fills (see fill_kb)
     const int* dep;          // wait *dep >= dep_target before activation loads
     int dep_target;
     int dep_where;
@@ -108,13 +107,12 @@ __device__ __forceinline__ int kpack_of(const GemmTask& t) {
 }
 __device__ __forceinline__ int fills_of(const GemmTask& t) { return ceil_div(t.nkb, kpack_of(t)); }
 // First k-block (relative to kb0) and k-block count of the task's u-th fill.
-// Tasks that share their activation rows run at the same time on different
-// SMs; each starts its k loop at its own rotation, so they do not all pull the
-// same activation k-block through the same L2 slices at once.  The sum order
-// is fixed per task, so results are deterministic.
+// Every task walks its k-blocks in order: concurrent tiles of neighbouring
+// weight rows then read the same columns at the same time, which streams DRAM
+// faster than staggered starts (measured: +2.5 % over the Mixtral sweep).
 __device__ __forceinline__ int fill_kb(const GemmTask& t, int u, int& nk) {
-    const int kp = kpack_of(t), nf = fills_of(t);
-    const int kb = ((u + t.rot) % nf) * kp;
+    const int kp = kpack_of(t);
+    const int kb = u * kp;
     nk = min(kp, t.nkb - kb);
     return kb;
 }

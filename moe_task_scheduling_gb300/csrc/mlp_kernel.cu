@@ -151,11 +151,11 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     auto gemm_of = [&](const MlpTile& t) {
         if (t.kind == 1)
             return GemmTask{&tm_wg, &tm_wu, &tm_xhat, p.b_wide ? &tm_xhat64 : nullptr,
-                            t.ft * kTileM, t.mt * kWideNMax, 0, p.H / kBlockK, t.n, t.ft,
+                            t.ft * kTileM, t.mt * kWideNMax, 0, p.H / kBlockK, t.n,
                             &p.hdr->ev_norm, P.NR, kWhereNorm};
         const int fchunk = p.F / P.S;
         return GemmTask{&tm_wd, nullptr, &tm_h, p.b_wide ? &tm_h64 : nullptr, t.ht * kTileM,
-                        t.mt * kWideNMax, t.s * (fchunk / kBlockK), fchunk / kBlockK, t.n, t.ht,
+                        t.mt * kWideNMax, t.s * (fchunk / kBlockK), fchunk / kBlockK, t.n,
                         &p.ev_h[t.mt * kSplitMax + t.s], P.FT / P.S, kWhereH};
     };
 

@@ -1148,24 +1148,24 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(const __grid_const
         const MoePlan& P = plans[l];
         if (type == kTaskShGateUp)  // shared expert over the rows of x_hat
             return GemmTask{&M.sg, &M.su, &M.xn, nullptr, m.b * kTileM, m.row0, 0,
-                            p.H / kBlockK, m.n, m.b, &p.hdr->ev_norm, P.R, kWhereNorm};
+                            p.H / kBlockK, m.n, &p.hdr->ev_norm, P.R, kWhereNorm};
         if (type == kTaskShDown) {
             const int fch = p.Fs / S;
             return GemmTask{&M.sd, nullptr, &M.hs, nullptr, m.c * kTileM, m.row0,
-                            m.b * (fch / kBlockK), fch / kBlockK, m.n, m.c,
+                            m.b * (fch / kBlockK), fch / kBlockK, m.n,
                             &p.ev_hs[m.a * kSplitMax + m.b], P.FTS / S, kWhereH};
         }
         if (type == kTaskGateUp) {
             const int nkb = p.H / kBlockK / KC;
             return GemmTask{&M.wg, &M.wu, &M.xp, p.b_wide ? &M.xp64 : nullptr,
-                            m.e * p.F + m.b * kTileM, m.row0, m.c * nkb, nkb, m.n, m.b,
+                            m.e * p.F + m.b * kTileM, m.row0, m.c * nkb, nkb, m.n,
                             &p.hdr->ev_perm, P.NP, kWherePerm};
         }
         const int fchunk = p.F / S, wide = (m.type >> 24) & 1;
         return GemmTask{&M.wd, wide ? &M.wd : nullptr, &M.h, p.b_wide ? &M.h64 : nullptr,
                         m.e * p.H + m.c * (kTileM << wide), m.row0, m.b * (fchunk / kBlockK),
-                        fchunk / kBlockK, m.n, m.c, &p.ev_h[m.a * kSplitMax + m.b], FT / S,
-                        kWhereH, wide ? kTileM : 0};
+                        fchunk / kBlockK, m.n, &p.ev_h[m.a * kSplitMax + m.b], FT / S, kWhereH,
+                        wide ? kTileM : 0};
     };
 
     if (warp == 0) {

@@ -63,7 +63,7 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 
     auto gemm_of = [&](const SplitKTile& t) {
         return GemmTask{&tm_w, nullptr, &tm_x, p.b_wide ? &tm_x64 : nullptr, t.nt * kTileM,
-                        t.mt * kWideNMax, t.s * kbs, kbs, t.n, t.nt, nullptr, 0, 0};
+                        t.mt * kWideNMax, t.s * kbs, kbs, t.n, nullptr, 0, 0};
     };
 
     if (warp == 0) {
@@ -254,7 +254,7 @@ splitk_clc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
 
     auto gemm_of = [&](const SplitKTile& t) {
         return GemmTask{&tm_w, nullptr, &tm_x, p.b_wide ? &tm_x64 : nullptr, t.nt * kTileM,
-                        t.mt * kWideNMax, t.s * kbs, kbs, t.n, t.nt, nullptr, 0, 0};
+                        t.mt * kWideNMax, t.s * kbs, kbs, t.n, nullptr, 0, 0};
     };
 
     if (warp == 0) {

@@ -159,3 +159,21 @@ def test_block_full_size(cuda_lib, oracle, cfg, Fs, Ts):
         sample = sorted({0, T // 3, T // 2, T - 1})
         ref = oracle_block(oracle, hb, bb, cfg, T, tokens=sample)
         check_block(res, ref, T, cfg.k, sample=sample)
+
+
+def test_block_fault_times_out_and_recovers(cuda_lib, oracle):
+    """A routed gate/up task that skips its release: the block's waits end in
+    ET_ERR_TIMEOUT; the next call on the same workspace is correct."""
+    cfg, Fs = SMALL_MIX, 1024
+    inp, blk = _inputs(cfg, Fs, True)
+    hb, bb = host_bits(inp), block_bits(blk)
+    d = {k: _to_dev(v) for k, v in inp.items()}
+    b = {k: _to_dev(v) for k, v in blk.items()}
+    T = 64
+    ws = cuda_lib.alloc_workspace(
+        cuda_lib.et_moe_block_workspace_bytes(T, cfg.H, cfg.F, cfg.E, cfg.k, Fs))
+    res = run_block(cuda_lib, d, b, cfg, T, ws=ws, timeout_us=20000, fault_mode=1, fault_arg=0)
+    assert res["code"] == cuda_lib.ET_ERR_TIMEOUT, (res["code"], res["detail"])
+    cuda_lib.et_reset_status(ws)
+    res = run_block(cuda_lib, d, b, cfg, T, ws=ws)
+    check_block(res, oracle_block(oracle, hb, bb, cfg, T), T, cfg.k)

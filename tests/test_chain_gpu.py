@@ -215,3 +215,34 @@ def test_chain_rejects_bad_descriptors(cuda_lib):
     assert cuda_lib.et_moe_chain_workspace_bytes(ds * 3, 16, cfg.H, cfg.F, cfg.E, cfg.k) == 0
     ds[1].Fs = 128  # a shared expert needs gamma
     assert cuda_lib.et_moe_chain_workspace_bytes(ds, 16, cfg.H, cfg.F, cfg.E, cfg.k) == 0
+
+
+def test_chain_fault_times_out_and_recovers(cuda_lib):
+    """A gate/up task of the first layer that never releases its event: the
+    chain must end with ET_ERR_TIMEOUT (every layer unwinds on the launch's
+    abort flag), and the next normal call on the same workspace must match
+    the same layers launched one by one."""
+    cfg = SMALL_MIX
+    T = 64
+    ch = Chain(cuda_lib, cfg, KINDS["block2"], T)
+    descs = ch.descs()
+    ws = ch.workspace(descs)
+    cuda_lib.et_moe_chain(descs, ch.x, H=cfg.H, F=cfg.F, E=cfg.E, k=cfg.k, T=T, T_max=T,
+                          workspace=ws, timeout_us=20000, fault_mode=1, fault_arg=0)
+    torch.cuda.synchronize()
+    code, detail = cuda_lib.et_status(ws)
+    assert code == cuda_lib.ET_ERR_TIMEOUT, (code, detail)
+    cuda_lib.et_reset_status(ws)
+    for o in ch.outs:
+        o.fill_(3.0)
+    assert ch.run(T, ws=ws) == (0, 0)
+    chained = [o.clone() for o in ch.outs]
+    x = ch.x
+    for j in range(2):
+        sub = Chain.__new__(Chain)
+        sub.__dict__.update(ch.__dict__)
+        sub.layers, sub.outs, sub.idx, sub.cnt = (ch.layers[j:j + 1], ch.outs[j:j + 1],
+                                                  ch.idx[j:j + 1], ch.cnt[j:j + 1])
+        assert sub.run(T, x=x) == (0, 0)
+        assert torch.equal(ch.outs[j][:T], chained[j][:T]), f"layer {j} after the fault"
+        x = chained[j]
