@@ -171,11 +171,15 @@ struct MlpArgs {
     int32_t* ev_h;        // [mt_max * kSplitMax]
     int32_t* ev_y;        // [mt_max * H/128], self-resetting
     float* partial;       // [kSplitMax, B_max, H]
+    float* gu_part;       // [2][gu_cap, F]: gate then up fp32 partials of K-split tiles
+    int32_t* ev_gu;       // [mt_max * F/128]: K chunks done per gate/up tile (self-resetting)
+    int gu_cap;           // rows of each gu_part half (K chunks x batch rows)
     int mt_max;
     int b_wide;
     int num_ctas;
     uint64_t timeout_ns;
     int fault_mode, fault_arg;
 };
+constexpr int kMlpGuRowsCap = 256;   // MLP: K chunks x B rows of gate/up partials at most
 
 }  // namespace et

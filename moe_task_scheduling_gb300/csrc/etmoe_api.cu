@@ -269,8 +269,8 @@ SplitKLayout splitk_layout(int M_max, int N, int K, int split) {
 // ---------------------------------------------------------------- MLP layout
 
 struct MlpLayout {
-    int mt_max;
-    size_t xhat, h, ev_h, ev_y, partial, total;
+    int mt_max, gu_cap;
+    size_t xhat, h, ev_h, ev_y, ev_gu, partial, gu_part, total;
 };
 
 MlpLayout mlp_layout(int B_max, int H, int F) {
@@ -282,6 +282,9 @@ MlpLayout mlp_layout(int B_max, int H, int F) {
     L.xhat = c.take(sizeof(uint16_t) * static_cast<size_t>(B_max) * H, 1024);
     L.h = c.take(sizeof(uint16_t) * static_cast<size_t>(B_max) * F, 1024);
     L.partial = c.take(sizeof(float) * static_cast<size_t>(kSplitMax) * B_max * H, 1024);
+    L.gu_cap = B_max * kGuSplitMax < kMlpGuRowsCap ? B_max * kGuSplitMax : kMlpGuRowsCap;
+    L.ev_gu = c.take(sizeof(int) * L.mt_max * (F / kTileM));
+    L.gu_part = c.take(sizeof(float) * 2 * static_cast<size_t>(L.gu_cap) * F, 1024);
     L.total = round_up(c.off, 256);
     return L;
 }
@@ -731,6 +734,9 @@ int et_mlp_chain(const void* x, const void* gamma, float eps, const void* w_gate
     a.ev_h = reinterpret_cast<int32_t*>(ws + L.ev_h);
     a.ev_y = reinterpret_cast<int32_t*>(ws + L.ev_y);
     a.partial = reinterpret_cast<float*>(ws + L.partial);
+    a.gu_part = reinterpret_cast<float*>(ws + L.gu_part);
+    a.ev_gu = reinterpret_cast<int32_t*>(ws + L.ev_gu);
+    a.gu_cap = L.gu_cap;
     a.mt_max = L.mt_max;
     a.num_ctas = st->sms;
     a.timeout_ns = timeout_ns_of(opts);

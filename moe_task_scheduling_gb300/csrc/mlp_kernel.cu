@@ -5,7 +5,10 @@
 // Tasks are bound to CTAs by index (task i runs on CTA i mod grid, in index
 // order) -- no queue, no atomics for distribution.  Index order is
 //   [0, NR)                 NORM i      8 rows each;      releases ev_norm
-//   [NR, NR + MT*FT)        GATEUP m,f  waits ev_norm >= NR; releases ev_h[m][chunk(f)]
+//   [NR, NR + MT*FT*KC)     GATEUP m,f,c waits ev_norm >= NR; with a K split (small
+//                                       batches: K chunks c) stores fp32 partials, and
+//                                       the chunk that completes ev_gu[m][f] sums them;
+//                                       then releases ev_h[m][chunk(f)]
 //   [.., + MT*S*HT)         DOWN m,s,n  waits ev_h[m][s] >= F-tiles per chunk;
 //                                       with a split, stores an fp32 partial and
 //                                       releases ev_y[m][n]
@@ -28,12 +31,12 @@ constexpr int kNormRows = 8;  // one row per worker warp
 constexpr int kRedRows = 32;  // rows per REDUCE task
 
 struct MlpPlan {
-    int B, NR, MT, FT, HT, S, n_gu, n_dn, n_red, total;
+    int B, NR, MT, FT, HT, S, KC, n_gu, n_dn, n_red, total;
 };
 
 struct MlpTile {
     int kind;  // 0 norm, 1 gate/up, 2 down, 3 reduce
-    int i, mt, ft, s, ht, rows, n;
+    int i, mt, ft, kc, s, ht, rows, n;
 };
 
 __device__ __forceinline__ MlpTile mlp_tile(const MlpPlan& P, int task) {
@@ -53,8 +56,9 @@ __device__ __forceinline__ MlpTile mlp_tile(const MlpPlan& P, int task) {
     if (task < P.NR + P.n_gu) {
         t.kind = 1;
         t.i = task - P.NR;
-        t.mt = t.i / P.FT;
-        t.ft = t.i % P.FT;
+        t.kc = t.i % P.KC;  // the K chunks of one tile run on neighbouring CTAs
+        t.mt = (t.i / P.KC) / P.FT;
+        t.ft = (t.i / P.KC) % P.FT;
     } else {
         t.kind = 2;
         t.i = task - P.NR - P.n_gu;
@@ -143,16 +147,32 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             if (P.MT * P.HT * d >= static_cast<int>(gridDim.x)) break;
         }
     }
-    P.n_gu = P.MT * P.FT;
+    // K split of the gate/up tiles: with one row tile, F/128 tiles can leave
+    // CTAs idle; the smallest split that gives the grid >= 2.5 tasks a CTA (K
+    // chunks of >= 8 k-blocks, partial rows within gu_cap), else none
+    P.KC = 1;
+    {
+        const int nkb = p.H / kBlockK, G = static_cast<int>(gridDim.x);
+        for (int kc = 2; kc <= kGuSplitMax && P.MT * P.FT < (5 * G) / 2; kc *= 2) {
+            if (nkb % kc || nkb / kc < 8 || P.B * kc > p.gu_cap) break;
+            if (2 * P.MT * P.FT * kc >= 5 * G) {
+                P.KC = kc;
+                break;
+            }
+        }
+    }
+    P.n_gu = P.MT * P.FT * P.KC;
     P.n_dn = P.MT * P.S * P.HT;
     P.n_red = P.S > 1 ? ceil_div(P.B, kRedRows) * P.HT : 0;
     P.total = P.NR + P.n_gu + P.n_dn + P.n_red;
 
     auto gemm_of = [&](const MlpTile& t) {
-        if (t.kind == 1)
+        if (t.kind == 1) {
+            const int nkb = p.H / kBlockK / P.KC;
             return GemmTask{&tm_wg, &tm_wu, &tm_xhat, p.b_wide ? &tm_xhat64 : nullptr,
-                            t.ft * kTileM, t.mt * kWideNMax, 0, p.H / kBlockK, t.n,
+                            t.ft * kTileM, t.mt * kWideNMax, t.kc * nkb, nkb, t.n,
                             &p.hdr->ev_norm, P.NR, kWhereNorm};
+        }
         const int fchunk = p.F / P.S;
         return GemmTask{&tm_wd, nullptr, &tm_h, p.b_wide ? &tm_h64 : nullptr, t.ht * kTileM,
                         t.mt * kWideNMax, t.s * (fchunk / kBlockK), fchunk / kBlockK, t.n,
@@ -217,22 +237,65 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const size_t m0 = static_cast<size_t>(t.mt) * kWideNMax;
             if (t.kind == 1) {
                 const int f = t.ft * kTileM + q * 32 + lane;
+                // K-split tile: fp32 partials of chunk kc, rows of this call
+                float* gpart = p.gu_part + (static_cast<size_t>(t.kc) * P.B) * F;
+                float* upart = gpart + static_cast<size_t>(p.gu_cap) * F;
                 for (int c0 = half * 16; c0 < t.n; c0 += 32) {
                     float gv[16], uv[16];
                     tmem_ld16(lane_base + c0, gv);
                     tmem_ld16(acc1 + lane_off + c0, uv);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        if (c0 + c < t.rows)
-                            p.h[(m0 + c0 + c) * F + f] =
+                    for (int c = 0; c < 16; ++c) {
+                        if (c0 + c >= t.rows) continue;
+                        const size_t r = m0 + c0 + c;
+                        if (P.KC == 1) {
+                            p.h[r * F + f] =
                                 __float2bfloat16_rn(gv[c] / (1.0f + __expf(-gv[c])) * uv[c]);
+                        } else {
+                            gpart[r * F + f] = gv[c];
+                            upart[r * F + f] = uv[c];
+                        }
+                    }
                 }
                 epi_release(ctl, es, true, t.n);
+                if (P.KC > 1) {  // the chunk that completes the tile sums the partials
+                    int* ev = p.ev_gu + t.mt * P.FT + t.ft;
+                    worker_sync();
+                    if (wtid == 0) {
+                        __threadfence();
+                        ctl->flag = (atom_acq_rel_add(ev, 1) == P.KC - 1) ? 1 : 0;
+                    }
+                    worker_sync();
+                    if (!ctl->flag) continue;
+                    if (wtid == 0) *ev = 0;  // every chunk arrived: reset for the next call
+                    const float* g0 = p.gu_part;
+                    const float* u0 = p.gu_part + static_cast<size_t>(p.gu_cap) * F;
+                    for (int j = wtid; j < t.rows * (kTileM / 4); j += kWorkers) {
+                        const size_t r = m0 + j / (kTileM / 4);
+                        const int ff = t.ft * kTileM + (j % (kTileM / 4)) * 4;
+                        float gs[4] = {0.0f, 0.0f, 0.0f, 0.0f}, us[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        for (int kc = 0; kc < P.KC; ++kc) {  // chunk order kc = 0 .. KC-1
+                            const size_t o = (static_cast<size_t>(kc) * P.B + r) * F + ff;
+                            const float4 gq = __ldcg(reinterpret_cast<const float4*>(g0 + o));
+                            const float4 uq = __ldcg(reinterpret_cast<const float4*>(u0 + o));
+                            gs[0] += gq.x; gs[1] += gq.y; gs[2] += gq.z; gs[3] += gq.w;
+                            us[0] += uq.x; us[1] += uq.y; us[2] += uq.z; us[3] += uq.w;
+                        }
+                        __nv_bfloat162 o2[2];
+#pragma unroll
+                        for (int i2 = 0; i2 < 2; ++i2) {
+                            const float a = gs[2 * i2], b2 = gs[2 * i2 + 1];
+                            o2[i2] = __floats2bfloat162_rn(a / (1.0f + __expf(-a)) * us[2 * i2],
+                                                           b2 / (1.0f + __expf(-b2)) * us[2 * i2 + 1]);
+                        }
+                        *reinterpret_cast<uint2*>(p.h + r * F + ff) = *reinterpret_cast<const uint2*>(o2);
+                    }
+                }
                 fence_proxy_async_global();  // h is read back by TMA
                 worker_sync();
                 if (wtid == 0) {
-                    const bool skip = p.fault_mode == 1 && t.i == p.fault_arg;
+                    const bool skip = p.fault_mode == 1 && t.mt * P.FT + t.ft == p.fault_arg;
                     __threadfence();
                     if (!skip) red_release_add(&p.ev_h[t.mt * kSplitMax + t.ft / (P.FT / P.S)], 1);
                 }
@@ -280,6 +343,8 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         for (int j = threadIdx.x; j < mt_clear * kSplitMax; j += kThreads) p.ev_h[j] = 0;
         const int y_clear = ab ? p.mt_max : (P.S > 1 ? P.MT : 0);
         for (int j = threadIdx.x; j < y_clear * P.HT; j += kThreads) p.ev_y[j] = 0;
+        if (ab)  // the K-split counters reset themselves unless the launch aborted
+            for (int j = threadIdx.x; j < p.mt_max * P.FT; j += kThreads) p.ev_gu[j] = 0;
         __syncthreads();
         if (threadIdx.x == 0) {
             p.hdr->ev_norm = 0;

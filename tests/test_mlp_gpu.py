@@ -88,3 +88,24 @@ def test_full_size_sweep(cuda_lib, oracle):
         rows = sorted({0, B // 2, B - 1})
         ref = oracle.mlp_chain(hb["x"], hb["gamma"], cfg.eps, hb["wg"], hb["wu"], hb["wd"], rows=rows)
         assert_close_bf16(wl.bits(out)[rows], ref, f"MLP B={B}")
+
+
+def test_ksplit_gate_up_every_row(cuda_lib, oracle):
+    """A shape whose gate/up tiles are split along K at small batches (95 F-tiles
+    cannot fill the grid): every row against the oracle, one workspace, B read
+    from device memory, the counters clean between calls."""
+    B_max, H, F = 64, 2048, 95 * 128
+    cfg, inp = small_inputs(B_max, H, F, 50)
+    hb = {k: wl.bits(v) for k, v in inp.items()}
+    d = {k: v.cuda() for k, v in inp.items()}
+    ws = cuda_lib.alloc_workspace(cuda_lib.et_mlp_workspace_bytes(B_max, H, F))
+    d_B = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for B in (1, 17, 64, 33):
+        d_B.fill_(B)
+        out, code, detail, _ = run_chain(cuda_lib, d, cfg.eps, B, B_max=B_max, ws=ws, d_B=d_B)
+        assert code == 0, (code, detail)
+        ref = oracle.mlp_chain(hb["x"][:B], hb["gamma"], cfg.eps, hb["wg"], hb["wu"], hb["wd"])
+        assert_close_bf16(wl.bits(out)[:B], ref, f"MLP K-split B={B}")
+        assert torch.all(out[B:].float() == 3.0)
+    hdr = ws[:256].view(torch.int32).cpu().numpy()
+    assert np.all(hdr[2:] == 0)
