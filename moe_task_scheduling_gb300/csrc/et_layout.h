@@ -59,7 +59,8 @@ struct EtHeader {
     int32_t split;          // split of the down projection chosen this call
     int32_t gu_split;       // K chunks of a gate/up tile chosen this call
     int32_t ev_sdone;       // shared-expert output tiles complete (fused block)
-    int32_t reserved[49];
+    int32_t q_wide;         // the down tiles are 256 columns wide this call
+    int32_t reserved[48];
 };
 static_assert(sizeof(EtHeader) == 256, "header is 256 bytes");
 
@@ -108,11 +109,7 @@ struct MoeArgs {
     int32_t* base;        // [r_max * E]: first permuted row of each (tile, expert)
     int32_t* off;         // [E + 1]
     int32_t* pos;         // [T_max * k]: permuted row of (t, j)
-    int32_t* g_expert;    // [mt_max]: expert of row tile g
-    int32_t* g_row0;      // [mt_max]: first permuted row of tile g
-    int32_t* g_rows;      // [mt_max]: valid rows of tile g
-    int32_t* g_n;         // [mt_max]: UMMA N of tile g
-    int4* queue;          // [q_max][2]: {type|split<<8|K chunks<<16, a, b, c}, {e, row0, rows, n}
+    int4* g_info;         // [mt_max]: row tile g's {expert, first permuted row, rows, UMMA N}
     bf16* xp;             // [T_max*k, H]: x rows in permuted order
     bf16* h;              // [T_max*k, F]
     bf16* y;              // [T_max*k, H]
@@ -120,7 +117,7 @@ struct MoeArgs {
     float* gu_part;       // [2][gu_cap, F]: gate then up fp32 partials of K-split tiles
     int32_t* ev_gu;       // [mt_max * F/128]: K chunks done per gate/up tile (self-resetting)
     int gu_cap;           // rows of each gu_part half
-    int mt_max, q_max, split_rows_cap, r_max;
+    int mt_max, split_rows_cap, r_max;
     int wr_box;           // router-weight TMA box height (0: the weight is read in place)
     int b_wide;           // the 64-row activation maps are valid (enough rows)
     int num_ctas;

@@ -149,9 +149,9 @@ struct Carve {
 // ---------------------------------------------------------------- MoE layout
 
 struct MoeLayout {
-    int Tk, r_max, mt_max, q_max, split_cap, gu_cap, mts_max;
-    size_t ev_h, ev_y, ev_tile, ev_gu, logits, hist, base, idx, gw, cnt, off, pos, perm, g_expert,
-        g_row0, g_rows, g_n, queue, xp, h, y, partial, gu_part;
+    int Tk, r_max, mt_max, split_cap, gu_cap, mts_max;
+    size_t ev_h, ev_y, ev_tile, ev_gu, logits, hist, base, idx, gw, cnt, off, pos, perm, g_info,
+        xp, h, y, partial, gu_part;
     size_t xn, hs, ys, ev_hs, ev_ys, partial_s;  // fused block only (block == true)
     size_t ev_tok;                               // rows released per 16-token tile (chains)
     size_t total;
@@ -166,8 +166,6 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k, bool block = false, 
     L.mt_max = ceil_div(L.Tk, kMoeNMax) + E;
     const int FT = F / kTileM, HT = H / kTileM;
     L.mts_max = (block && Fs > 0) ? ceil_div(T_max, kWideNMax) : 0;
-    L.q_max = L.r_max * kRouterTile * k + L.mt_max * FT * kGuSplitMax +
-              L.mt_max * kSplitMax * HT + T_max + L.mts_max * kSplitMax * HT;
     L.split_cap = L.Tk < kMoeSplitRowsCap ? L.Tk : kMoeSplitRowsCap;
     L.gu_cap = L.Tk * kGuSplitMax < kGuRowsCap ? L.Tk * kGuSplitMax : kGuRowsCap;
     Carve c;
@@ -184,11 +182,7 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k, bool block = false, 
     L.off = c.take(sizeof(int) * (E + 1));
     L.pos = c.take(sizeof(int) * L.Tk);
     L.perm = c.take(sizeof(int) * L.Tk);
-    L.g_expert = c.take(sizeof(int) * L.mt_max);
-    L.g_row0 = c.take(sizeof(int) * L.mt_max);
-    L.g_rows = c.take(sizeof(int) * L.mt_max);
-    L.g_n = c.take(sizeof(int) * L.mt_max);
-    L.queue = c.take(sizeof(int4) * 2 * static_cast<size_t>(L.q_max));
+    L.g_info = c.take(sizeof(int4) * L.mt_max);
     L.xp = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
     L.h = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * F, 1024);
     L.y = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
@@ -405,11 +399,7 @@ int moe_run(const void* x, const LayerIn* layers, int nl, int T, const int32_t* 
         a.base = reinterpret_cast<int32_t*>(ws + L.base);
         a.off = reinterpret_cast<int32_t*>(ws + L.off);
         a.pos = reinterpret_cast<int32_t*>(ws + L.pos);
-        a.g_expert = reinterpret_cast<int32_t*>(ws + L.g_expert);
-        a.g_row0 = reinterpret_cast<int32_t*>(ws + L.g_row0);
-        a.g_rows = reinterpret_cast<int32_t*>(ws + L.g_rows);
-        a.g_n = reinterpret_cast<int32_t*>(ws + L.g_n);
-        a.queue = reinterpret_cast<int4*>(ws + L.queue);
+        a.g_info = reinterpret_cast<int4*>(ws + L.g_info);
         a.xp = reinterpret_cast<bf16*>(ws + L.xp);
         a.h = reinterpret_cast<bf16*>(ws + L.h);
         a.y = reinterpret_cast<bf16*>(ws + L.y);
@@ -418,7 +408,6 @@ int moe_run(const void* x, const LayerIn* layers, int nl, int T, const int32_t* 
         a.ev_gu = reinterpret_cast<int32_t*>(ws + L.ev_gu);
         a.gu_cap = L.gu_cap;
         a.mt_max = L.mt_max;
-        a.q_max = L.q_max;
         a.split_rows_cap = L.split_cap;
         a.r_max = L.r_max;
         a.wr_box = E % 8 == 0 ? (H % 256 == 0 ? 256 : 128) : 0;

@@ -220,6 +220,7 @@ struct MoePlan {
     int Q;         // permute parts per router tile
     int CT, NC;    // tokens per combine task; combine tasks
     int NP;        // permute tasks in the queue (0: one router tile, permuted inline)
+    int NPW;       // permute releases the gate/up tiles wait for (the inline permute: 1)
     bool stage;    // router tiles stage x and their weight chunk in the ring
     // fused block: norm tasks (16 rows each; none when the router tiles stage
     // and normalise their rows), shared expert row tiles (256 rows), F-tiles and
@@ -266,6 +267,7 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     P.CT = min(min(kCombineTile, per_batch), max(1, ceil_div(T, G)));
     P.NC = ceil_div(T, P.CT);
     P.NP = P.R > 1 ? P.R * P.Q : 0;
+    P.NPW = P.R > 1 ? P.NP : 1;
     const int HT = H / kTileM;
     const bool block = p.gamma != nullptr;
     // a staged router tile normalises its own rows; otherwise NORM tasks do
@@ -619,8 +621,6 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     int* off_s = cnt_s + 256;                   // [257]
     int* n_s = off_s + 264;                     // [256]
     int* mtb_s = n_s + 256;                     // [257]
-    // [mt_max <= 2304]: expert of row tile g (ends below kHistOff; dead before the permute)
-    int* ge_s = mtb_s + 264;
     const int RE = R * E;
     const bool staged = R > 1 && static_cast<size_t>(RE) * 4 <= ring.bytes;
     int* hs = reinterpret_cast<int*>(ring.base);
@@ -743,13 +743,8 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         p.off[e] = off_s[e];
         if (e == E - 1) p.off[E] = off_s[E];
         const int n = n_s[e];
-        for (int g = mtb_s[e], mt = 0; g < mtb_s[e + 1]; ++g, ++mt) {
-            ge_s[g] = e;
-            p.g_expert[g] = e;
-            p.g_row0[g] = off_s[e] + mt * n;
-            p.g_rows[g] = min(n, cnt_s[e] - mt * n);
-            p.g_n[g] = n;
-        }
+        for (int g = mtb_s[e], mt = 0; g < mtb_s[e + 1]; ++g, ++mt)
+            p.g_info[g] = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n), n);
     }
     if (R == 1) {
         for (int e = wtid_(); e < E; e += kWorkers) p.base[e] = off_s[e];
@@ -759,74 +754,41 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         for (int i = wtid_(); i < RE; i += kWorkers) p.base[i] += off_s[i % E];
     }
     tm = phase_mark(p, 7, tm);
-    worker_sync();  // the tile -> expert table is complete
-    // Queue: [permute parts][gate/up tiles, by chunk][shared down tiles (fused
-    // block)][down tiles, by chunk][combine tasks].  A chunk c = (row tile g, F-chunk s) has u gate/up and
-    // d down tasks; every down task comes after the gate/up tasks it waits for.
-    // (Down tiles placed right behind their chunk's gate/up tiles were
-    // measured slower on decode and large batches: popped early, they stall
-    // their CTA on the dependency.)
+    // The queue is implicit: every entry follows from the row tiles, S, KC and
+    // the down-tile width, so the scan publishes those (and the row-tile table)
+    // and each producer decodes the indices it claims (queue_task); nothing is
+    // written per entry.  Order: [permute parts][gate/up tiles, by chunk]
+    // [shared down tiles (fused block)][down tiles, by chunk][combine tasks].
+    // A chunk c = (row tile g, F-chunk s) has u gate/up and d down tasks; every
+    // down task comes after the gate/up tasks it waits for.  (Down tiles placed
+    // right behind their chunk's gate/up tiles were measured slower on decode
+    // and large batches: popped early, they stall their CTA on the dependency.)
     // Wide down tiles (256 output columns: two weight boxes share one h tile, so
     // each expert's h rows are read half as often) when tiles are tall.
     const int wide = (S == 1 && HT % 2 == 0 && T * k >= 64 * total_mt) ? 1 : 0;
     const int u = (FT / S) * KC, d = wide ? HT / 2 : HT, NCH = total_mt * S;
-    const int n_perm = P.NP, n_tiles = NCH * (u + d), n_sd = P.NSD;
-    const int n_cb = P.NC > 1 ? P.NC : 0;  // a single combine runs inline (last down tile)
-    const int total = n_perm + n_tiles + n_sd + n_cb;
-    if (total > p.q_max) {  // cannot happen for a valid workspace; fail loudly
-        if (wtid_() == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereQueue);
-        return false;
-    }
-    const int flags = (S << 8) | (KC << 16) | (wide << 24);
-    int4* qd = p.queue;  // two int4 per entry: {type|flags, a, b, c}, {e, row0, rows, n}
-    for (int q = wtid_(); q < n_perm; q += kWorkers) {
-        qd[2 * q] = make_int4(kTaskPermute, q / P.Q, q % P.Q, 0);
-        qd[2 * q + 1] = make_int4(0, 0, 0, 0);
-    }
-    for (int q = wtid_(); q < n_cb; q += kWorkers) {
-        const int qq = n_perm + n_tiles + n_sd + q;
-        qd[2 * qq] = make_int4(kTaskCombine, q, 0, 0);
-        qd[2 * qq + 1] = make_int4(0, 0, 0, 0);
-    }
-    // fused block: the shared expert's down tiles (row tile, F-chunk, output
-    // tile), after the routed gate/up tiles, by when their inputs are done
-    for (int i = wtid_(); i < n_sd; i += kWorkers) {
-        const int qq = n_perm + NCH * u + i, mt = i / (P.SS * HT);
-        const int row0 = mt * kWideNMax, rows = min(kWideNMax, T - row0);
-        qd[2 * qq] = make_int4(kTaskShDown | (P.SS << 8), mt, (i % (P.SS * HT)) / HT, i % HT);
-        qd[2 * qq + 1] = make_int4(0, row0, rows, (rows + 15) / 16 * 16);
-    }
-    {  // a thread per entry: chunk c = (row tile g, F-chunk sc) has u gate/up and d down
-        const int dn_base = n_perm + NCH * u + n_sd;
-        for (int q = wtid_(); q < NCH * u; q += kWorkers) {
-            const int c = q / u, r = q % u, g = c / S, sc = c % S, e = ge_s[g];
-            const int n = n_s[e], mt = g - mtb_s[e];
-            qd[2 * (n_perm + q)] = make_int4(kTaskGateUp | flags, g, sc * (FT / S) + r / KC, r % KC);
-            qd[2 * (n_perm + q) + 1] = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n), n);
-        }
-        for (int q = wtid_(); q < NCH * d; q += kWorkers) {  // r: output tile (of 128, or 256 if wide)
-            const int c = q / d, r = q % d, g = c / S, sc = c % S, e = ge_s[g];
-            const int n = n_s[e], mt = g - mtb_s[e];
-            qd[2 * (dn_base + q)] = make_int4(kTaskDown | flags, g, sc, r);
-            qd[2 * (dn_base + q) + 1] = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n), n);
-        }
-    }
-    worker_sync();
-    tm = phase_mark(p, 8, tm);
-    if (R == 1) {  // permute inline: base = off, x rows already staged if the router staged them
-        const int* sel = reinterpret_cast<const int*>(smem + kSelOff);
-        if (!permute_rows(p, P, 0, 0, T * k, smem, ring, ctl, wc, sphase, seq, sel, off_s, P.stage))
-            return false;
-    }
-    tm = phase_mark(p, 9, tm);
+    const int total = P.NP + NCH * (u + d) + P.NSD + (P.NC > 1 ? P.NC : 0);
+    worker_sync();  // the row-tile table and the permute bases are written
     if (wtid_() == 0) {
         p.hdr->total_mt = total_mt;
         p.hdr->split = S;
         p.hdr->gu_split = KC;
+        p.hdr->q_wide = wide;
         p.hdr->q_total = total;
         __threadfence();
         st_release(&p.hdr->q_ready, 1);
     }
+    if (R == 1) {  // permute inline (x rows already staged if the router staged them), after
+                   // the publish: the gate/up tiles wait on its ev_perm release
+        const int* sel = reinterpret_cast<const int*>(smem + kSelOff);
+        if (!permute_rows(p, P, 0, 0, T * k, smem, ring, ctl, wc, sphase, seq, sel, off_s, P.stage))
+            return false;
+        if (wtid_() == 0) {
+            __threadfence();
+            red_release_add(&p.hdr->ev_perm, 1);
+        }
+    }
+    tm = phase_mark(p, 8, tm);
     return true;
 }
 
@@ -1032,7 +994,60 @@ __device__ __forceinline__ void combine_inline(const MoeArgs& p, const MoePlan& 
 // (size known once its scan has run); the next layer's follow.
 struct QCursor {
     int layer = 0, base = 0, qt = -1;
+    int mt = 0, S = 1, KC = 1, wide = 0;  // the layer's published queue parameters
 };
+
+// Entry q of a layer's implicit queue (see scan_task for the order).
+__device__ __forceinline__ TaskMsg queue_task(const MoeArgs& p, const MoePlan& P,
+                                              const QCursor& cur, int q) {
+    TaskMsg m{};
+    if (q < P.NP) {  // permute part q % Q of router tile q / Q
+        m.type = kTaskPermute;
+        m.a = q / P.Q;
+        m.b = q % P.Q;
+        return m;
+    }
+    q -= P.NP;
+    const int FT = p.F / kTileM, HT = p.H / kTileM, S = cur.S, KC = cur.KC;
+    const int u = (FT / S) * KC, d = cur.wide ? HT / 2 : HT, NCH = cur.mt * S;
+    const int flags = (S << 8) | (KC << 16) | (cur.wide << 24);
+    if (q < NCH * u) {  // gate/up: row tile g, F-tile, K chunk
+        const int c = q / u, r = q % u, g = c / S;
+        m.type = kTaskGateUp | flags;
+        m.a = g;
+        m.b = (c % S) * (FT / S) + r / KC;
+        m.c = r % KC;
+        const int4 gi = __ldcg(p.g_info + g);
+        m.e = gi.x, m.row0 = gi.y, m.rows = gi.z, m.n = gi.w;
+        return m;
+    }
+    q -= NCH * u;
+    if (q < P.NSD) {  // fused block: shared down tile (row tile, F-chunk, output tile)
+        const int mt = q / (P.SS * HT);
+        m.type = kTaskShDown | (P.SS << 8);
+        m.a = mt;
+        m.b = (q % (P.SS * HT)) / HT;
+        m.c = q % HT;
+        m.row0 = mt * kWideNMax;
+        m.rows = min(kWideNMax, P.T - m.row0);
+        m.n = (m.rows + 15) / 16 * 16;
+        return m;
+    }
+    q -= P.NSD;
+    if (q < NCH * d) {  // down: row tile g, F-chunk, output tile (of 128, or 256 if wide)
+        const int c = q / d, g = c / S;
+        m.type = kTaskDown | flags;
+        m.a = g;
+        m.b = c % S;
+        m.c = q % d;
+        const int4 gi = __ldcg(p.g_info + g);
+        m.e = gi.x, m.row0 = gi.y, m.rows = gi.z, m.n = gi.w;
+        return m;
+    }
+    m.type = kTaskCombine;
+    m.a = q - NCH * d;
+    return m;
+}
 
 // Static-prefix task j of a layer: [norm][router][shared gate/up].
 __device__ __forceinline__ TaskMsg static_task(const MoeArgs& p, const MoePlan& P, int j) {
@@ -1082,18 +1097,13 @@ __device__ __forceinline__ TaskMsg pop_task(const MoeLaunch& Lc, const MoePlan* 
         if (cur.qt < 0) {
             if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
             cur.qt = ld_relaxed(&p.hdr->q_total);
+            cur.mt = ld_relaxed(&p.hdr->total_mt);
+            cur.S = ld_relaxed(&p.hdr->split);
+            cur.KC = ld_relaxed(&p.hdr->gu_split);
+            cur.wide = ld_relaxed(&p.hdr->q_wide);
         }
         if (j < P.NS0 + cur.qt) {
-            const int q = j - P.NS0;
-            const int4 d0 = __ldcg(p.queue + 2 * q), d1 = __ldcg(p.queue + 2 * q + 1);
-            m.type = d0.x;
-            m.a = d0.y;
-            m.b = d0.z;
-            m.c = d0.w;
-            m.e = d1.x;
-            m.row0 = d1.y;
-            m.rows = d1.z;
-            m.n = d1.w;
+            m = queue_task(p, P, cur, j - P.NS0);
             break;
         }
         if (!kChain || cur.layer + 1 >= Lc.nl) return m;  // every layer's tasks are taken
@@ -1159,7 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(const __grid_const
             const int nkb = p.H / kBlockK / KC;
             return GemmTask{&M.wg, &M.wu, &M.xp, p.b_wide ? &M.xp64 : nullptr,
                             m.e * p.F + m.b * kTileM, m.row0, m.c * nkb, nkb, m.n,
-                            &p.hdr->ev_perm, P.NP, kWherePerm};
+                            &p.hdr->ev_perm, P.NPW, kWherePerm};
         }
         const int fchunk = p.F / S, wide = (m.type >> 24) & 1;
         return GemmTask{&M.wd, wide ? &M.wd : nullptr, &M.h, p.b_wide ? &M.h64 : nullptr,
@@ -1503,6 +1513,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(const __grid_const
                 hd->ev_ydone = 0;
                 hd->split = 0;
                 hd->gu_split = 0;
+                hd->q_wide = 0;
                 hd->ev_norm = 0;
                 hd->ev_sdone = 0;
                 hd->abort = 0;
