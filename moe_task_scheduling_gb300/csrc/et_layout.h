@@ -110,6 +110,9 @@ struct MoeArgs {
     int32_t* off;         // [E + 1]
     int32_t* pos;         // [T_max * k]: permuted row of (t, j)
     int4* g_info;         // [mt_max]: row tile g's {expert, first permuted row, rows, UMMA N}
+    int4* e_tile;         // [E]: expert e's {first row tile, UMMA N, first permuted row, 0}
+    int32_t* gpos;        // [T_max * k]: row tile of the permuted row of (t, j)
+    int32_t* ev_gdone;    // [mt_max]: 128-column output tiles of row tile g complete
     bf16* xp;             // [T_max*k, H]: x rows in permuted order
     bf16* h;              // [T_max*k, F]
     bf16* y;              // [T_max*k, H]

@@ -151,7 +151,7 @@ struct Carve {
 struct MoeLayout {
     int Tk, r_max, mt_max, split_cap, gu_cap, mts_max;
     size_t ev_h, ev_y, ev_tile, ev_gu, logits, hist, base, idx, gw, cnt, off, pos, perm, g_info,
-        xp, h, y, partial, gu_part;
+        e_tile, gpos, ev_gdone, xp, h, y, partial, gu_part;
     size_t xn, hs, ys, ev_hs, ev_ys, partial_s;  // fused block only (block == true)
     size_t ev_tok;                               // rows released per 16-token tile (chains)
     size_t total;
@@ -183,6 +183,9 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k, bool block = false, 
     L.pos = c.take(sizeof(int) * L.Tk);
     L.perm = c.take(sizeof(int) * L.Tk);
     L.g_info = c.take(sizeof(int4) * L.mt_max);
+    L.e_tile = c.take(sizeof(int4) * E);
+    L.gpos = c.take(sizeof(int) * L.Tk);
+    L.ev_gdone = c.take(sizeof(int) * L.mt_max);
     L.xp = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
     L.h = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * F, 1024);
     L.y = c.take(sizeof(uint16_t) * static_cast<size_t>(L.Tk) * H, 1024);
@@ -400,6 +403,9 @@ int moe_run(const void* x, const LayerIn* layers, int nl, int T, const int32_t* 
         a.off = reinterpret_cast<int32_t*>(ws + L.off);
         a.pos = reinterpret_cast<int32_t*>(ws + L.pos);
         a.g_info = reinterpret_cast<int4*>(ws + L.g_info);
+        a.e_tile = reinterpret_cast<int4*>(ws + L.e_tile);
+        a.gpos = reinterpret_cast<int32_t*>(ws + L.gpos);
+        a.ev_gdone = reinterpret_cast<int32_t*>(ws + L.ev_gdone);
         a.xp = reinterpret_cast<bf16*>(ws + L.xp);
         a.h = reinterpret_cast<bf16*>(ws + L.h);
         a.y = reinterpret_cast<bf16*>(ws + L.y);
