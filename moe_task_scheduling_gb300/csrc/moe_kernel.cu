@@ -385,6 +385,14 @@ __device__ __forceinline__ void norm_task(const MoeArgs& p, const MoePlan& P, in
     }
 }
 
+// The router weight chunk (and gamma) a CTA staged last stays in the ring for
+// its next router task with the same chunk; any other use of the ring drops
+// it.  The key (ctl->scratch[8..9]) is the chunk's global address, 0 = none.
+constexpr int kWrKey = 8;
+__device__ __forceinline__ void wr_cache_drop(Ctl* ctl) {
+    if (wtid_() == 0) ctl->scratch[kWrKey] = ctl->scratch[kWrKey + 1] = 0;
+}
+
 // x_hat of a staged router tile in place, the arithmetic of norm_task (gamma
 // staged too); warp w takes rows w, w + 8.  With `store` the rows also go to
 // x_hat in global memory (for the permute and the shared expert).
@@ -454,22 +462,31 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     uint64_t tm = p.trace ? globaltimer_ns() : 0;
     if (P.stage) {
         const uint32_t xbytes = static_cast<uint32_t>(nt * H * 2);
-        const uint32_t xpad = (xbytes + 1023u) & ~1023u;
+        // the weight chunk sits after room for a full tile, at the same place for every tile
+        const uint32_t xpad = (static_cast<uint32_t>(min(P.T, kRouterTile) * H * 2) + 1023u) & ~1023u;
         const int box = p.wr_box, hp = wr_rows_pad(H, box);
         const int eb0 = e0 >> 3, nb = ((e0 + ec + 7) >> 3) - eb0;
         uint8_t* wdst = ring.base + xpad;
         uint8_t* gdst = wdst + static_cast<size_t>(nb) * hp * 16;  // gamma (own norm)
         const uint32_t gbytes = own_norm ? static_cast<uint32_t>(H) * 2u : 0u;
+        const uint64_t key = reinterpret_cast<uint64_t>(wb);
+        const bool cached = static_cast<uint32_t>(ctl->scratch[kWrKey]) == static_cast<uint32_t>(key) &&
+                            static_cast<uint32_t>(ctl->scratch[kWrKey + 1]) ==
+                                static_cast<uint32_t>(key >> 32);
+        worker_sync();  // every worker has read the key before it changes
         if (wtid_() == 0) {
-            mbar_arrive_expect_tx(&ctl->sbar,
-                                  xbytes + static_cast<uint32_t>(nb * hp * 16) + gbytes);
+            mbar_arrive_expect_tx(&ctl->sbar, xbytes + (cached ? 0u : static_cast<uint32_t>(nb * hp * 16) + gbytes));
             bulk_g2s(ring.base, xb, xbytes, &ctl->sbar);
-            if (own_norm) bulk_g2s(gdst, p.gamma, gbytes, &ctl->sbar);
-            const uint64_t pol = policy_evict_last();
-            for (int b = 0; b < nb; ++b)
-                for (int h0 = 0; h0 < hp; h0 += box)
-                    tma_load_2d(wdst + static_cast<size_t>(b * hp + h0) * 16, tm_wr, &ctl->sbar,
-                                (eb0 + b) * 8, h0, pol);
+            if (!cached) {
+                if (own_norm) bulk_g2s(gdst, p.gamma, gbytes, &ctl->sbar);
+                const uint64_t pol = policy_evict_last();
+                for (int b = 0; b < nb; ++b)
+                    for (int h0 = 0; h0 < hp; h0 += box)
+                        tma_load_2d(wdst + static_cast<size_t>(b * hp + h0) * 16, tm_wr, &ctl->sbar,
+                                    (eb0 + b) * 8, h0, pol);
+                ctl->scratch[kWrKey] = static_cast<int>(static_cast<uint32_t>(key));
+                ctl->scratch[kWrKey + 1] = static_cast<int>(static_cast<uint32_t>(key >> 32));
+            }
         }
         if (!staging_wait(ctl, sphase, wc, seq)) return false;
         if (own_norm) {  // x -> x_hat in place; chunk 0 publishes the rows
@@ -638,6 +655,7 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
                                           uint32_t& sphase, uint32_t& seq) {
     const int E = p.E, k = p.k, R = P.R, T = P.T;
     uint64_t tm = p.trace ? globaltimer_ns() : 0;
+    wr_cache_drop(ctl);  // the scan and the inline permute stage into the ring
     const int* hs1 = reinterpret_cast<const int*>(smem + kHistOff);  // R == 1: the counts
     int* cnt_s = reinterpret_cast<int*>(smem);  // [256]
     int* off_s = cnt_s + 256;                   // [257]
@@ -889,6 +907,7 @@ __device__ __forceinline__ bool permute_task(const MoeArgs& p, const MoePlan& P,
                                              uint8_t* smem, const Ring& ring, Ctl* ctl,
                                              const WaitCtx& wc, uint32_t& sphase, uint32_t& seq) {
     const int t0 = r * kRouterTile, nent = min(kRouterTile, P.T - t0) * p.k;
+    wr_cache_drop(ctl);
     if (!permute_rows(p, P, r, part * nent / P.Q, (part + 1) * nent / P.Q, smem, ring, ctl, wc,
                       sphase, seq, nullptr, nullptr, false))
         return false;
@@ -940,6 +959,7 @@ __device__ __forceinline__ bool combine_task(const MoeArgs& p, const MoePlan& P,
                                              const WaitCtx& wc, uint32_t& sphase, uint32_t& seq) {
     const int H = p.H, k = p.k;
     const int t0 = c * P.CT, nt = min(P.CT, P.T - t0), vpr = H / 8;
+    wr_cache_drop(ctl);
     if (!combine_wait_rows(p, P, t0, nt, ctl, wc)) return false;
     fence_proxy_async_global();  // y rows written by other CTAs' generic stores
     const int rpt = combine_rows_per_token(p, P), hx = p.gamma ? 1 : 0, hs = P.MTS > 0 ? 1 : 0;
@@ -1099,10 +1119,10 @@ __device__ __forceinline__ TaskMsg static_task(const MoeArgs& p, const MoePlan& 
     }
     j -= P.NRN;
     const int nr = P.R * P.C;
-    if (j < nr) {
+    if (j < nr) {  // chunk-major: a CTA's next router task often reuses its staged chunk
         m.type = kTaskRouter;
-        m.a = j / P.C;
-        m.b = j % P.C;
+        m.a = j % P.R;
+        m.b = j / P.R;
         return m;
     }
     j -= nr;  // fused block: shared expert gate/up tiles (no routing needed)
@@ -1180,6 +1200,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(const __grid_const
     }
     // every layer's plan, once per CTA (shared memory, read by every role)
     MoePlan* plans = reinterpret_cast<MoePlan*>(scratch + kPlanOff);
+    if (threadIdx.x == 0) ctl->scratch[kWrKey] = ctl->scratch[kWrKey + 1] = 0;
     if (static_cast<int>(threadIdx.x) < Lc.nl)
         plans[threadIdx.x] =
             moe_plan(Lc.a[threadIdx.x], T, static_cast<int>(gridDim.x), ring.bytes);
@@ -1310,6 +1331,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(const __grid_const
                 continue;
             }
             const bool two = type == kTaskGateUp || type == kTaskShGateUp || wide;
+            wr_cache_drop(ctl);  // the tile's fills went through the ring
             uint32_t acc, acc1;
             if (!epi_acquire(ctl, es, two, m.n, tmem, wc, acc, acc1)) break;
             const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
