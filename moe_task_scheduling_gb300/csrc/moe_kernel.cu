@@ -144,7 +144,7 @@ __device__ __forceinline__ void load_w(const bf16* wrow, float (&w)[EBW]) {
 }
 
 // Fixed-order logits of nt (<= 16) tokens x `ec` experts (global experts
-// e0 .. e0+ec).  A job is 4 tokens x EBW experts on one warp: lane l owns
+// e0 .. e0+ec).  A job is TB tokens x EBW experts on one warp: lane l owns
 // partial sum l and accumulates h = l, l+32, ... in ascending order with fp32
 // fma (a bf16 x bf16 product is exact in fp32, so fma == mul + add); the
 // halving shuffle tree (16, 8, 4, 2, 1) then adds p[l] + p[l + off].
@@ -169,9 +169,9 @@ __device__ __forceinline__ void fma2(float& c0, float& c1, float x, float w0, fl
 }
 
 template <int EBW, int TB>
-__device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, const bf16* wb,
-                                              int o, int rs, int blk, int nt, int e0, int ec,
-                                              float* out) {
+__device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16* xb,
+                                                   const bf16* wb, int o, int rs, int blk, int nt,
+                                                   int e0, int ec, float* out) {
     const int H = p.H, E = p.E;
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
     const int neb = ec / EBW, ntb = ceil_div(nt, TB);
@@ -185,12 +185,14 @@ __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, 
             for (int b = 0; b < EBW; ++b) acc[a][b] = 0.0f;
         const bf16* xr = xb + static_cast<size_t>(tb * TB) * H;
         const bf16* wj = wb + static_cast<size_t>((o + j0) >> 3) * blk + ((o + j0) & 7);
-        // A plain loop, unrolled (the compiler hoists the loads of later steps):
-        // measured faster than explicit software pipelining here.  Pairs of
-        // experts go through one packed fma.rn.f32x2 (two independent IEEE
-        // fmas: the same sums, half the instructions; 2 % on the fine-grained
-        // sweep).
-#pragma unroll 2
+        // A plain loop, unrolled so the compiler keeps several steps' loads in
+        // flight (each lane's sum is one dependent chain of H/32 fmas, so a
+        // narrow job is latency-bound: unrolling 8 steps instead of 2 took a
+        // 1-token job from 7.1K to 4.5K SM cycles on GB300; the 4x8 job, with
+        // many jobs a CTA on large batches, keeps 2).  Pairs of experts go
+        // through one packed fma.rn.f32x2 (two independent IEEE fmas: the same
+        // sums, half the instructions).
+#pragma unroll(TB * EBW >= 32 ? 2 : 8)
         for (int h = lane; h < H; h += 32) {  // h ascending per lane
             float wv[EBW];
             load_w<EBW>(wj + static_cast<size_t>(h) * rs, wv);
@@ -223,6 +225,25 @@ __device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, 
                 }
         }
     }
+}
+
+// Narrow jobs (up to 16 accumulators, their loop unrolled 8 steps) run out of
+// line, so their registers do not add to the kernel's; the 4x8 job (many to a
+// CTA on large batches) stays inline, which measured faster there.
+template <int EBW, int TB>
+static __device__ __noinline__ void router_logits_narrow(const MoeArgs& p, const bf16* xb,
+                                                         const bf16* wb, int o, int rs, int blk,
+                                                         int nt, int e0, int ec, float* out) {
+    router_logits_body<EBW, TB>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+}
+template <int EBW, int TB>
+__device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, const bf16* wb,
+                                              int o, int rs, int blk, int nt, int e0, int ec,
+                                              float* out) {
+    if constexpr (TB * EBW >= 32)
+        router_logits_body<EBW, TB>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    else
+        router_logits_narrow<EBW, TB>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
 }
 
 // Router-weight staging geometry: 8-expert column blocks, rows padded to the
@@ -510,34 +531,24 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
         blk = hp * 8;
     }
     float* out = P.C == 1 ? lg : p.logits + static_cast<size_t>(t0) * E;
-    // the widest expert block (<= 8) that divides the chunk (and E when the
-    // weight is read in place, for aligned vector loads) and still gives every
-    // worker warp a job, else one expert per job
-    // A job is TB tokens x EBW experts on one warp.  Shapes in order of FMAs per
-    // shared-memory wavefront (TB x EBW / (TB + 4)): 4x8, 8x4, 4x4, 8x2, 4x2,
-    // 8x1, 4x1 (8x8 measured no faster than 4x8 and would need 64 accumulators);
-    // the first that gives every worker warp a job wins (8-token jobs only when
-    // the tile has more than 4 tokens).  EBW divides the chunk (and E when the
-    // weight is read in place, for aligned vector loads).
+    // A job is TB tokens x EBW experts on one warp.  The loop is latency-bound
+    // rather than issue-bound, so few wide jobs beat one job per warp: EBW is
+    // the widest block (<= 8) that divides the chunk (and E when the weight is
+    // read in place, for aligned vector loads), TB is 4 tokens, or 1 when the
+    // tile holds a single token.  Measured on GB300: 16 tokens x 2 experts as
+    // four 4x2 jobs take 55 % of the time of eight 4x1 jobs; 1 token x 2
+    // experts as one 1x2 job 60 % of the time of one 4x2 job.
     const int ew = P.stage ? ec : (ec | E);
-    int tb = 4, ebw = 1;
-    {
-        const int cand[7][2] = {{4, 8}, {8, 4}, {4, 4}, {8, 2}, {4, 2}, {8, 1}, {4, 1}};
-        for (int i = 0; i < 7; ++i) {
-            const int ct = cand[i][0], ce = cand[i][1];
-            if ((ct == 8 && nt <= 4) || ew % ce != 0) continue;
-            tb = ct;
-            ebw = ce;
-            if ((ec / ce) * ceil_div(nt, ct) >= kWorkers / 32) break;
-        }
-    }
-    if (tb == 8) {
-        if (ebw == 4)
-            router_logits<4, 8>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    const int ebw = ew % 8 == 0 ? 8 : (ew % 4 == 0 ? 4 : (ew % 2 == 0 ? 2 : 1));
+    if (nt == 1) {
+        if (ebw == 8)
+            router_logits<8, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+        else if (ebw == 4)
+            router_logits<4, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else if (ebw == 2)
-            router_logits<2, 8>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<2, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else
-            router_logits<1, 8>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<1, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
     } else {
         if (ebw == 8)
             router_logits<8, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
