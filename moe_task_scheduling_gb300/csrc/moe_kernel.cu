@@ -270,6 +270,7 @@ struct MoePlan {
     int NP;        // permute tasks in the queue (0: one router tile, permuted inline)
     int NPW;       // permute releases the gate/up tiles wait for (the inline permute: 1)
     bool stage;    // router tiles stage x and their weight chunk in the ring
+    bool wr_whole; // ... the whole router weight [H, E] with one bulk copy, as laid out
     // fused block: norm tasks (16 rows each; none when the router tiles stage
     // and normalise their rows), shared expert row tiles (256 rows), F-tiles and
     // down split; the static prefix [norm][router][shared gate/up] precedes the
@@ -308,6 +309,18 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
         }
     }
     P.EC = E / P.C;
+    // A router weight small enough to sit next to a full token tile is staged
+    // whole by one bulk copy (and reused by every later router task of the
+    // CTA): 16-byte-wide TMA boxes of an 8-expert block move its rows far
+    // below the bulk copy's rate.
+    {
+        const uint32_t xpad = (static_cast<uint32_t>(min(T, kRouterTile) * H * 2) + 1023u) & ~1023u;
+        const uint32_t gb = p.gamma ? static_cast<uint32_t>(H) * 2u : 0u;
+        const uint32_t wfull = static_cast<uint32_t>(H) * static_cast<uint32_t>(E) * 2u;
+        P.wr_whole = P.stage && wfull % 16u == 0 &&
+                     (reinterpret_cast<uintptr_t>(p.wr) & 15u) == 0 &&
+                     xpad + wfull + gb <= ring_bytes;
+    }
     P.Q = P.R > 0 ? min(max(1, G / P.R), kRouterTile * k) : 1;
     // a combine task's k rows per token fit the ring in one staging batch
     const int rpt = k + (p.gamma ? 1 : 0) + (p.gamma && p.Fs > 0 ? 1 : 0);  // rows per token
@@ -493,23 +506,29 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
         const int box = p.wr_box, hp = wr_rows_pad(H, box);
         const int eb0 = e0 >> 3, nb = ((e0 + ec + 7) >> 3) - eb0;
         uint8_t* wdst = ring.base + xpad;
-        uint8_t* gdst = wdst + static_cast<size_t>(nb) * hp * 16;  // gamma (own norm)
+        const uint32_t wbytes = P.wr_whole ? static_cast<uint32_t>(H) * static_cast<uint32_t>(E) * 2u
+                                           : static_cast<uint32_t>(nb * hp * 16);
+        uint8_t* gdst = wdst + wbytes;  // gamma (own norm)
         const uint32_t gbytes = own_norm ? static_cast<uint32_t>(H) * 2u : 0u;
-        const uint64_t key = reinterpret_cast<uint64_t>(wb);
+        const uint64_t key = reinterpret_cast<uint64_t>(P.wr_whole ? p.wr : wb);
         const bool cached = static_cast<uint32_t>(ctl->scratch[kWrKey]) == static_cast<uint32_t>(key) &&
                             static_cast<uint32_t>(ctl->scratch[kWrKey + 1]) ==
                                 static_cast<uint32_t>(key >> 32);
         worker_sync();  // every worker has read the key before it changes
         if (wtid_() == 0) {
-            mbar_arrive_expect_tx(&ctl->sbar, xbytes + (cached ? 0u : static_cast<uint32_t>(nb * hp * 16) + gbytes));
+            mbar_arrive_expect_tx(&ctl->sbar, xbytes + (cached ? 0u : wbytes + gbytes));
             bulk_g2s(ring.base, xb, xbytes, &ctl->sbar);
             if (!cached) {
                 if (own_norm) bulk_g2s(gdst, p.gamma, gbytes, &ctl->sbar);
-                const uint64_t pol = policy_evict_last();
-                for (int b = 0; b < nb; ++b)
-                    for (int h0 = 0; h0 < hp; h0 += box)
-                        tma_load_2d(wdst + static_cast<size_t>(b * hp + h0) * 16, tm_wr, &ctl->sbar,
-                                    (eb0 + b) * 8, h0, pol);
+                if (P.wr_whole) {
+                    bulk_g2s(wdst, p.wr, wbytes, &ctl->sbar);
+                } else {
+                    const uint64_t pol = policy_evict_last();
+                    for (int b = 0; b < nb; ++b)
+                        for (int h0 = 0; h0 < hp; h0 += box)
+                            tma_load_2d(wdst + static_cast<size_t>(b * hp + h0) * 16, tm_wr,
+                                        &ctl->sbar, (eb0 + b) * 8, h0, pol);
+                }
                 ctl->scratch[kWrKey] = static_cast<int>(static_cast<uint32_t>(key));
                 ctl->scratch[kWrKey + 1] = static_cast<int>(static_cast<uint32_t>(key >> 32));
             }
@@ -531,9 +550,15 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
         tm = phase_mark(p, 0, tm);
         xb = reinterpret_cast<const bf16*>(ring.base);
         wb = reinterpret_cast<const bf16*>(wdst);
-        o = e0 & 7;
-        rs = 8;
-        blk = hp * 8;
+        if (P.wr_whole) {  // [H, E] as in global memory
+            o = e0;
+            rs = E;
+            blk = 8;
+        } else {
+            o = e0 & 7;
+            rs = 8;
+            blk = hp * 8;
+        }
     }
     float* out = P.C == 1 ? lg : p.logits + static_cast<size_t>(t0) * E;
     // A job is TB tokens x EBW experts on one warp.  The loop is latency-bound
@@ -543,7 +568,7 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     // tile holds a single token.  Measured on GB300: 16 tokens x 2 experts as
     // four 4x2 jobs take 55 % of the time of eight 4x1 jobs; 1 token x 2
     // experts as one 1x2 job 60 % of the time of one 4x2 job.
-    const int ew = P.stage ? ec : (ec | E);
+    const int ew = (P.stage && !P.wr_whole) ? ec : (ec | E);
     const int ebw = ew % 8 == 0 ? 8 : (ew % 4 == 0 ? 4 : (ew % 2 == 0 ? 2 : 1));
     if (nt == 1) {
         if (ebw == 8)
