@@ -229,20 +229,22 @@ class MoeBench:
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
         self.stream = torch.cuda.current_stream(device)
 
-    def call(self, x=None, out=None):
+    def call(self, x=None, out=None, T=None):
+        """One layer call; T from device memory (d_T), or the host count T."""
         i = self.inp
+        tkw = dict(T=0, d_T=self.d_T) if T is None else dict(T=T, d_T=None)
         if self.blk is not None:
             b = self.blk
             self.etmoe.et_moe_block(x if x is not None else i["x"], b["gamma"], b["eps"], i["wr"],
                                     b["bias"], i["wg"], i["wu"], i["wd"], b["sg"], b["su"], b["sd"],
-                                    out if out is not None else self.out, k=self.cfg.k, T=0,
-                                    d_T=self.d_T, T_max=self.cfg.T_max, expert_counts=self.cnt,
-                                    workspace=self.ws, stream=self.stream)
+                                    out if out is not None else self.out, k=self.cfg.k,
+                                    T_max=self.cfg.T_max, expert_counts=self.cnt,
+                                    workspace=self.ws, stream=self.stream, **tkw)
             return
         self.etmoe.et_moe_layer(x if x is not None else i["x"], i["wr"], i["bias"], i["wg"], i["wu"],
-                                i["wd"], out if out is not None else self.out, k=self.cfg.k, T=0,
-                                d_T=self.d_T, T_max=self.cfg.T_max, expert_counts=self.cnt,
-                                workspace=self.ws, stream=self.stream)
+                                i["wd"], out if out is not None else self.out, k=self.cfg.k,
+                                T_max=self.cfg.T_max, expert_counts=self.cnt,
+                                workspace=self.ws, stream=self.stream, **tkw)
 
     def step(self, events=None):
         """One pass over the sweep; returns per-T event pairs if asked."""
@@ -271,7 +273,8 @@ class MoeBench:
 
     def e2e(self, steps):
         """Through the public call with host buffers: per T, pinned x -> device,
-        the layer, out -> pinned host; all copies inside the timed region."""
+        the layer (the token count passed from the host, as a caller holding host
+        buffers would), out -> pinned host; all copies inside the timed region."""
         cfg = self.cfg
         xh = {T: self.inp["x"][:T].cpu().pin_memory() for T in cfg.T_sweep}
         oh = {T: torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory() for T in cfg.T_sweep}
@@ -283,8 +286,7 @@ class MoeBench:
             s.record(self.stream)
             for T in cfg.T_sweep:
                 xd[:T].copy_(xh[T], non_blocking=True)
-                self.d_T.fill_(T)
-                self.call(x=xd)
+                self.call(x=xd, T=T)
                 oh[T].copy_(self.out[:T], non_blocking=True)
             e.record(self.stream)
             e.synchronize()

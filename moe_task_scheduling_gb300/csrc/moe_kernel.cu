@@ -662,14 +662,19 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     }
     tm = phase_mark(p, 11, tm);
     worker_sync();
-    for (int e = wtid_(); e < E; e += kWorkers) p.hist[static_cast<size_t>(r) * E + e] = hs[e];
-    worker_sync();
     tm = phase_mark(p, 3, tm);
-    // the last router tile to finish runs the scan: no task waits for it
-    if (wtid_() == 0) {
-        __threadfence();
-        ctl->flag = (atom_acq_rel_add(&p.hdr->ev_router, 1) == P.R - 1) ? 1 : 0;
+    // the last router tile to finish runs the scan: no task waits for it.  A
+    // single tile is its own last (its counts stay in smem for the scan).
+    if (P.R > 1) {
+        for (int e = wtid_(); e < E; e += kWorkers) p.hist[static_cast<size_t>(r) * E + e] = hs[e];
+        worker_sync();
+        if (wtid_() == 0) {
+            __threadfence();
+            ctl->flag = (atom_acq_rel_add(&p.hdr->ev_router, 1) == P.R - 1) ? 1 : 0;
+        }
+        worker_sync();
     }
+    if (P.R == 1 && wtid_() == 0) ctl->flag = 1;
     worker_sync();
     tm = phase_mark(p, 4, tm);
     if (!ctl->flag) return true;
