@@ -4,8 +4,9 @@ Default workload: the Mixtral-shaped MoE layer (H 4096, 8 experts, top-2,
 SwiGLU FFN 14336, bf16 weights ~N(0, 0.02), synthetic seeded inputs).  One
 step is one pass over the token sweep T = 1, 2, 4, ..., 512 -- every token
 count served by the same compiled kernel, the count read from device memory.
-L2 is flushed (256 MiB write) before every layer call and each call is timed
-with CUDA events on the launching stream.
+L2 is flushed before every layer call (a 256 MiB write, then a 256 MiB read,
+so the call starts from a cold L2 holding clean lines only) and each call is
+timed with CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload mixtral|fine|mixtral_block|fine_block|mixtral_chain2|
@@ -54,6 +55,25 @@ METRIC_CHAIN = ("Two chained fused MoE blocks in one launch: tokens/s over the t
 # workload -> (configuration, shared-expert width, layers)
 CHAIN_WORKLOADS = {"mixtral_chain2": (wl.MIXTRAL, 0, 2), "fine_chain2": (wl.FINE, 2 * wl.FINE.F, 2)}
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Run before each timed call: write a buffer twice the size of L2 (every
+    line of the previous call is evicted), then read another one, so the call
+    starts from a cold L2 that holds clean lines only.  With the write alone
+    L2 is left full of the flush buffer's dirty lines, and writing those back
+    to HBM lands inside the next timed call (measured on GB300: 2.5 % of the
+    Mixtral sweep's time)."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        # fp32, so the sum reads the buffer in place (an integer sum would first cast it)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 # the sources the MoE megakernel is compiled from: a committed ncu traffic
 # figure stands for the kernel only while these hash to its recorded value
 KERNEL_SOURCES = ["et_device.cuh", "et_gemm.cuh", "et_layout.h", "moe_kernel.cu"]
@@ -226,7 +246,7 @@ class MoeBench:
                   etmoe.et_moe_block_workspace_bytes(T_max, cfg.H, cfg.F, cfg.E, cfg.k, Fs))
         self.ws = etmoe.alloc_workspace(nbytes, device=device)
         self.d_T = torch.zeros(1, dtype=torch.int32, device=device)
-        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.flush = L2Flush(device)
         self.stream = torch.cuda.current_stream(device)
 
     def call(self, x=None, out=None, T=None):
@@ -250,7 +270,7 @@ class MoeBench:
         """One pass over the sweep; returns per-T event pairs if asked."""
         pairs = []
         for T in self.cfg.T_sweep:
-            self.flush.zero_()
+            self.flush()
             self.d_T.fill_(T)
             if events:
                 s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -304,7 +324,7 @@ class DenseBench:
         self.kind = kind
         self.dev = device
         self.stream = torch.cuda.current_stream(device)
-        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.flush = L2Flush(device)
         self.d_n = torch.zeros(1, dtype=torch.int32, device=device)
         if kind == "splitk":
             c = self.cfg = wl.SPLITK
@@ -348,11 +368,11 @@ class DenseBench:
             times = {}
             for clc in variants:
                 for _ in range(warmup):
-                    self.flush.zero_()
+                    self.flush()
                     self.call(clc)
                 ts = []
                 for _ in range(steps):
-                    self.flush.zero_()
+                    self.flush()
                     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     s.record(self.stream)
                     self.call(clc)
@@ -404,7 +424,7 @@ class ChainBench:
         self.ws1 = [etmoe.alloc_workspace(etmoe.et_moe_block_workspace_bytes(
             T_max, cfg.H, cfg.F, cfg.E, cfg.k, Fs), device=device) for _ in range(n)]
         self.d_T = torch.zeros(1, dtype=torch.int32, device=device)
-        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.flush = L2Flush(device)
         self.stream = torch.cuda.current_stream(device)
 
     def chain(self, x=None):
@@ -425,7 +445,7 @@ class ChainBench:
             x = self.outs[j]
 
     def timed(self, fn, T):
-        self.flush.zero_()
+        self.flush()
         self.d_T.fill_(T)
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(self.stream)
@@ -505,7 +525,7 @@ def run_chain(args, world, rank, local):
         "config": {"workload": f"{cfg.name}: {n} fused MoE blocks (Fs={Fs}) chained, T sweep "
                                f"{list(cfg.T_sweep)}",
                    "H": cfg.H, "F": cfg.F, "E": cfg.E, "k": cfg.k, "Fs": Fs, "layers": n,
-                   "l2": "flushed (256 MiB write) before every call (chain, or the pair)",
+                   "l2": "flushed before every call (chain, or the pair): 256 MiB write, then 256 MiB read",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "two_launches": {"value": round(tokens / t_sep, 1), "unit": "tokens/s",
                          "kind": "the same blocks, one et_moe_block launch each"},
@@ -681,7 +701,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": f"{cfg.name} {what}, T sweep {list(cfg.T_sweep)}",
                    "H": cfg.H, "F": cfg.F, "E": cfg.E, "k": cfg.k,
                    **({} if Fs is None else {"Fs": Fs, "eps": 1e-5}),
-                   "l2": "flushed (256 MiB write) before every layer call",
+                   "l2": "flushed before every layer call: 256 MiB write, then 256 MiB read (cold, clean L2)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "symbolic_T": "one compiled kernel, T read from device memory"},
         "sweep": sweep,
@@ -716,7 +736,7 @@ def run_single(args, local):
     b = MoeBench(cfg, device, Fs)
     b.d_T.fill_(args.single)
     for _ in range(args.warmup + 1):
-        b.flush.zero_()
+        b.flush()
         b.call()
     torch.cuda.synchronize()
     code, detail = b.etmoe.et_status(b.ws)
@@ -771,7 +791,7 @@ def per_op_baseline(b, cfg, reps=3):
     for T in cfg.T_sweep:
         ts = []
         for i in range(reps + 1):
-            b.flush.zero_()
+            b.flush()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(b.stream)
             _, touched = per_op_layer(b.inp, cfg, T, b.blk)
