@@ -793,15 +793,22 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     worker_sync();
     if (wtid_() == 0) {
         const int total_mt = mtb_s[E];
+        // Wide down tiles (256 output columns: two weight boxes share one h
+        // tile, so each expert's h rows are read half as often) when the row
+        // tiles are tall.
+        const int wide = (HT % 2 == 0 && T * k >= 64 * total_mt) ? 1 : 0;
         // split of the down projection: with few output tiles, the smallest
         // divisor of FT (<= 8) that gives the grid about four tasks a CTA (the
         // last wave of long tasks leaves CTAs idle); chunks keep >= 4 k-blocks,
-        // and >= 8 once the grid has three tasks a CTA
+        // and >= 8 once the grid has three tasks a CTA.  Wide tiles split in
+        // two at most: measured on the Mixtral shape at T = 256, wide tiles in
+        // 2 F-chunks take 494 us against 528 us for 128-column tiles in 4 and
+        // 500 us for wide ones in 4 (their partials are twice the bytes).
         int S = 1;
-        if (T * k <= p.split_rows_cap && total_mt > 0 && total_mt * HT < 3 * p.num_ctas) {
-            const int down = total_mt * HT;
+        const int down = total_mt * (wide ? HT / 2 : HT);
+        if (T * k <= p.split_rows_cap && total_mt > 0 && down < 3 * p.num_ctas) {
             int best = 1;
-            for (int d = 2; d <= kSplitMax; ++d) {
+            for (int d = 2; d <= (wide ? 2 : kSplitMax); ++d) {
                 if (FT % d) continue;
                 const int kbc = p.F / kBlockK / d;
                 if (kbc < 4 || (down * best >= 3 * p.num_ctas && kbc < 8)) break;
@@ -820,10 +827,12 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         ctl->scratch[0] = total_mt;
         ctl->scratch[1] = S;
         ctl->scratch[2] = KC;
+        ctl->scratch[3] = wide;
     }
     worker_sync();
     tm = phase_mark(p, 6, tm);
     const int total_mt = ctl->scratch[0], S = ctl->scratch[1], KC = ctl->scratch[2];
+    const int wide = ctl->scratch[3];
     for (int e = wtid_(); e < E; e += kWorkers) {
         p.cnt[e] = cnt_s[e];
         p.off[e] = off_s[e];
@@ -850,9 +859,6 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     // down task comes after the gate/up tasks it waits for.  (Down tiles placed
     // right behind their chunk's gate/up tiles were measured slower on decode
     // and large batches: popped early, they stall their CTA on the dependency.)
-    // Wide down tiles (256 output columns: two weight boxes share one h tile, so
-    // each expert's h rows are read half as often) when tiles are tall.
-    const int wide = (S == 1 && HT % 2 == 0 && T * k >= 64 * total_mt) ? 1 : 0;
     const int u = (FT / S) * KC, d = wide ? HT / 2 : HT, NCH = total_mt * S;
     const int total = P.NP + NCH * (u + d) + P.NSD + (P.NC > 1 ? P.NC : 0);
     worker_sync();  // the row-tile table and the permute bases are written
@@ -1507,10 +1513,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
                 }
                 continue;
             }
-            // DOWN: y (S == 1) or an fp32 partial of F-chunk s; a wide tile holds
-            // output columns [256 ht, +128) in acc and [256 ht + 128, +128) in acc1
+            // DOWN: y (S == 1) or an fp32 partial of F-chunk s (partials [row][S]);
+            // a wide tile holds output columns [256 ht, +128) in acc and
+            // [256 ht + 128, +128) in acc1
             const int s = m.b, ht = m.c;
-            const int cap = p.split_rows_cap;
             for (int w = 0; w <= wide; ++w) {
                 const int hh = ht * (kTileM << wide) + w * kTileM + q * 32 + lane;
                 const uint32_t ab = (w ? acc1 : acc) + lane_off;
@@ -1525,7 +1531,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
                         if (S == 1)
                             p.y[row * H + hh] = __float2bfloat16_rn(v[c]);
                         else
-                            p.partial[(static_cast<size_t>(s) * cap + row) * H + hh] = v[c];
+                            p.partial[(row * S + s) * H + hh] = v[c];
                     }
                 }
             }
@@ -1541,8 +1547,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
                 worker_sync();
                 done = ctl->flag != 0;
                 if (done) {  // last arriver: sum the partials in chunk order
-                    reduce_slice4(p.partial, static_cast<size_t>(cap) * H, H, S, row0, row0 + rows,
-                                  ht * kTileM, p.y, H);
+                    for (int w = 0; w <= wide; ++w)
+                        reduce_slice4(p.partial, static_cast<size_t>(H), S * H, S, row0,
+                                      row0 + rows, ht * (kTileM << wide) + w * kTileM, p.y, H);
                     fence_proxy_async_global();
                     worker_sync();
                 }

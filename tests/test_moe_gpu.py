@@ -73,9 +73,13 @@ SMALL_FINE = wl.MoEConfig("fine_small", 4, H=256, F=256, E=128, k=8, T_sweep=(1,
 ODD = wl.MoEConfig("odd_experts", 5, H=128, F=640, E=12, k=3, T_sweep=(1, 2, 31, 77))
 # tall expert tiles, no down split: the 256-column (two weight box) down tiles
 WIDE = wl.MoEConfig("wide_down", 6, H=512, F=256, E=4, k=2, T_sweep=(300, 520))
+# tall expert tiles with few output tiles: 256-column down tiles split in two
+# F-chunks, their partials summed by the last arriver
+WIDE_SPLIT = wl.MoEConfig("wide_split", 7, H=512, F=512, E=4, k=2, T_sweep=(130, 200, 256))
 
 
-@pytest.mark.parametrize("cfg", [SMALL_MIX, SMALL_FINE, ODD, WIDE], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [SMALL_MIX, SMALL_FINE, ODD, WIDE, WIDE_SPLIT],
+                         ids=lambda c: c.name)
 @pytest.mark.parametrize("unit", [True, False])
 def test_small_shapes(cuda_lib, oracle, cfg, unit):
     inp = wl.moe_inputs(cfg, device="cpu", unit_scale=unit)
@@ -155,7 +159,7 @@ def test_fault_injection_times_out_cleanly(cuda_lib, oracle):
     check(res, oracle_layer(oracle, hb, cfg, 64), 64, cfg.k)
 
 
-@pytest.mark.parametrize("cfg,Ts", [(wl.MIXTRAL, (1, 2, 16, 128, 512)),
+@pytest.mark.parametrize("cfg,Ts", [(wl.MIXTRAL, (1, 2, 16, 128, 256, 512)),
                                     (wl.FINE, (1, 8, 64, 1024, 4096))], ids=["mixtral", "fine"])
 def test_full_size(cuda_lib, oracle, cfg, Ts):
     """The configured shapes, one workspace, T from device memory.  Routing is
