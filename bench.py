@@ -91,10 +91,37 @@ def peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def _code_only(text):
+    """C++ source without its comments and with whitespace runs collapsed, so
+    that a comment-only edit leaves the hash of the compiled code unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, copied whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash():
+    """Hash of the megakernel's code (comments and layout excluded)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, "moe_task_scheduling_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "moe_task_scheduling_gb300", "csrc", f), encoding="utf-8").read()
+        h.update(_code_only(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,9 +1,9 @@
 // moe_kernel.cu -- the MoE layer as one persistent megakernel whose tiled
 // tasks are ordered by device-resident event counters, not kernel boundaries.
 //
-// Task graph (one dynamic queue, popped with an atomic head by each CTA's
-// producer thread and handed to its MMA thread and worker warps through a
-// small shared-memory ring; index order is a topological order and every
+// Task graph (one task index space, claimed with an atomic head by each
+// CTA's producer thread and handed to its MMA thread and worker warps through
+// a small shared-memory ring; index order is a topological order and every
 // role of a CTA walks its tasks in that order, so every wait is on a task
 // that a resident CTA already holds -- the launch is cooperative):
 //   [0, R*C)    ROUTER r,c fixed-order fp32 logits of router tile r for expert
@@ -11,21 +11,25 @@
 //                          ev_tile[r]) takes the top-k, gate weights and the
 //                          tile's expert histogram; the tile that completes
 //                          ev_router (count R, computed from the device token
-//                          count) runs the SCAN: counts, offsets, the expert
-//                          row tiles and the split of the down projection,
-//                          then it fills the queue (and, with a single router
-//                          tile, permutes it inline):
+//                          count; a single tile is its own last) runs the
+//                          SCAN: counts, offsets, the expert row tiles, the
+//                          splits and the down-tile width, which it publishes
+//                          -- the queue below is implicit, each producer
+//                          decodes the index it claims -- and, with a single
+//                          router tile, it then permutes inline:
 //   queue:      PERMUTE r,q stable scatter of part q of router tile r's rows;
 //                          releases ev_perm
 //               GATEUP g,f SwiGLU tile of expert row-tile g, F-tile f (waits
 //                          ev_perm >= permute parts); releases ev_h[g][chunk(f)]
-//               DOWN g,s,n down-projection tile, F-chunk s (waits
-//                          ev_h[g][s] >= F-tiles per chunk); with a split the
-//                          last arriver on ev_y[g][n] sums the fp32 partials
-//                          in chunk order; counts ev_ydone
-//               COMBINE c  waits ev_ydone >= tiles, out = sum_j w * y; a
-//                          single combine is run inline by the output tile
-//                          that completes ev_ydone.
+//               DOWN g,s,n down-projection tile (128 output columns, or 256
+//                          for tall row tiles), F-chunk s (waits ev_h[g][s] >=
+//                          F-tiles per chunk); with a split the last arriver on
+//                          ev_y[g][n] sums the fp32 partials in chunk order;
+//                          a finished output tile adds to ev_gdone[g]
+//               COMBINE c  waits for ev_gdone of every row tile that holds one
+//                          of its tokens' rows, out = sum_j w * y; a single
+//                          combine is run inline by the output tile that
+//                          completes ev_ydone.
 //
 // Sources: "Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
 // Kernels" (MoE routing gives data-dependent event counters that trigger
