@@ -321,23 +321,60 @@ class MoeBench:
     def e2e(self, steps):
         """Through the public call with host buffers: per T, pinned x -> device,
         the layer (the token count passed from the host, as a caller holding host
-        buffers would), out -> pinned host; all copies inside the timed region."""
+        buffers would), out -> pinned host; every copy is inside the timed region.
+        As a serving loop would, the copies run on a second stream with double
+        buffers, so the next call's upload and the last call's download overlap
+        the current layer.  The host outputs of the last step are then checked
+        bit for bit against a plain call per T."""
+        import torch
         cfg = self.cfg
-        xh = {T: self.inp["x"][:T].cpu().pin_memory() for T in cfg.T_sweep}
-        oh = {T: torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory() for T in cfg.T_sweep}
-        xd = torch.empty_like(self.inp["x"])
-        h2d = sum(T * cfg.H * 2 for T in cfg.T_sweep)
+        dev = self.inp["x"].device
+        Ts = list(cfg.T_sweep)
+        xh = {T: self.inp["x"][:T].cpu().pin_memory() for T in Ts}
+        oh = {T: torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory() for T in Ts}
+        xd = [torch.empty_like(self.inp["x"]) for _ in range(2)]
+        od = [torch.empty_like(self.out) for _ in range(2)]
+        ms, cs = self.stream, torch.cuda.Stream(device=dev)
+        h2d = sum(T * cfg.H * 2 for T in Ts)
         total = 0.0
         for _ in range(steps):
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record(self.stream)
-            for T in cfg.T_sweep:
-                xd[:T].copy_(xh[T], non_blocking=True)
-                self.call(x=xd, T=T)
-                oh[T].copy_(self.out[:T], non_blocking=True)
-            e.record(self.stream)
+            s.record(ms)
+            cs.wait_event(s)
+            up, done, down = [None] * len(Ts), [None] * len(Ts), [None] * len(Ts)
+
+            def upload(i):
+                with torch.cuda.stream(cs):
+                    if i >= 2:
+                        cs.wait_event(done[i - 2])  # layer i - 2 has read this x buffer
+                    xd[i % 2][:Ts[i]].copy_(xh[Ts[i]], non_blocking=True)
+                    up[i] = torch.cuda.Event()
+                    up[i].record(cs)
+
+            upload(0)
+            for i, T in enumerate(Ts):
+                if i + 1 < len(Ts):
+                    upload(i + 1)
+                ms.wait_event(up[i])
+                if i >= 2:
+                    ms.wait_event(down[i - 2])  # this out buffer has been read back
+                self.call(x=xd[i % 2], out=od[i % 2], T=T)
+                done[i] = torch.cuda.Event()
+                done[i].record(ms)
+                with torch.cuda.stream(cs):
+                    cs.wait_event(done[i])
+                    oh[T].copy_(od[i % 2][:T], non_blocking=True)
+                    down[i] = torch.cuda.Event()
+                    down[i].record(cs)
+            ms.wait_event(down[-1])
+            e.record(ms)
             e.synchronize()
             total += s.elapsed_time(e) / 1e3
+        for T in Ts:  # the pipelined results are the plain call's
+            self.call(x=self.inp["x"], out=od[0], T=T)
+            torch.cuda.synchronize()
+            if not torch.equal(od[0][:T].cpu(), oh[T]):
+                raise RuntimeError(f"e2e: host output at T={T} differs from a plain call")
         return total, h2d, h2d
 
 
