@@ -84,6 +84,14 @@ typedef struct et_opts {
  * MoE layer: router top-k -> per-expert counts -> SwiGLU expert FFN ->
  * weighted combine, in one persistent cooperative launch.
  *
+ * Source: "Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
+ * Kernels", the MoE discussion: routing yields data-dependent per-expert
+ * counters on the device, and those counters trigger the expert tasks from
+ * the router's output within one megakernel; "Megakernels ch. 5 - Event
+ * Tensor et le dynamisme", section 5.1 (MoE routing as a source of data
+ * dependence) and section 5.5, obstacles 1 and 3 (counter targets computed
+ * on the GPU from this call's routing; an online atomic work queue).
+ *
  *   logits[t,e] = sum_h x[t,h] * w_router[h,e] (+ router_bias[e]), fp32 in a
  *                 fixed order (32 strided partial sums, then a halving tree),
  *                 so routing is reproducible bit for bit;
@@ -97,6 +105,12 @@ typedef struct et_opts {
  * Optional outputs (NULL to skip): topk_idx int32 [T,k], topk_w fp32 [T,k],
  * expert_counts int32 [E], perm int32 [T*k] (perm[off[e]+r] = t*k+j for the
  * r-th token, ascending, routed to e; off = exclusive prefix sum of counts).
+ * T is the token count (used when d_T is NULL); d_T an optional device int32
+ * read by the kernel at run time (0 <= *d_T <= T_max; above that the kernel
+ * records ET_ERR_BOUNDS and does nothing); T_max sizes the workspace and the
+ * row buffers.  opts may be NULL.  Errors: ET_ERR_INVALID (a NULL or
+ * misaligned tensor, T outside [0, T_max]), ET_ERR_UNSUPPORTED (shape),
+ * ET_ERR_WORKSPACE, ET_ERR_CUDA; nothing is launched on any of them.
  * ---------------------------------------------------------------------- */
 size_t et_moe_workspace_bytes(int T_max, int H, int F, int E, int k);
 
@@ -194,11 +208,21 @@ int et_moe_chain(int n_layers, const et_moe_layer_desc* layers, const void* x, i
 /* ------------------------------------------------------------------------
  * Split-K GEMM with event-counter reduction:
  *   Y[M,N] = bf16( sum_{s<split} X[:,K_s] Wt[:,K_s]^T ),  K_s = s-th of `split`
- * equal K chunks.  Each (row tile, column tile, split) is one task; the task
- * that brings a tile's counter to `split` sums the fp32 partials in split
- * order and stores Y.  X bf16 [M_max,K] (rows >= M are never read into Y);
- * Wt bf16 [N,K]; Y bf16 [M,N].  N % 128 == 0, K % (64*split) == 0,
- * 1 <= split <= 16.
+ * equal K chunks.
+ *
+ * Source: "Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
+ * Kernels", the split-K example: the tiles of each K chunk produce partial
+ * sums, and the reduction of a tile starts when an event over its producing
+ * tiles completes, not at a kernel boundary; the batch size M stays
+ * symbolic, so one compiled kernel serves every M.
+ *
+ * Each (row tile, column tile, split) is one task; REDUCE tasks wait until a
+ * tile's counter reaches `split`, then sum its fp32 partials in split order
+ * and store Y.  X bf16 [M_max,K] (rows >= M are never read into Y); Wt bf16
+ * [N,K] (the weight transposed, K contiguous); Y bf16 [M_max,N], rows >= M
+ * untouched.  N % 128 == 0, K % (64*split) == 0, 1 <= split <= 16.  M is used
+ * when d_M is NULL, else the device int32 *d_M (0 <= *d_M <= M_max, else
+ * ET_ERR_BOUNDS on the device).  Errors as et_moe_layer.
  * ---------------------------------------------------------------------- */
 size_t et_splitk_workspace_bytes(int M_max, int N, int K, int split);
 
@@ -238,7 +262,9 @@ int et_splitk_gemm_clc(const void* X, const void* Wt, void* Y, int M, const int3
  *  - No cudaMalloc, cudaFree or other allocating call is made.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process, like the library's other per-device state: after
+ *    cudaDeviceReset the process must be restarted.
  *  - Each call first clears the status word and tile counters of the array
  *    on `stream` (cudaMemsetAsync), then runs the split-K kernel.
  *  - Every call shares the one array: calls that overlap on the GPU (other
@@ -246,20 +272,37 @@ int et_splitk_gemm_clc(const void* X, const void* Wt, void* Y, int M, const int3
  *  - Shapes whose scratch (et_splitk_workspace_bytes(M, N, K, split)) exceeds
  *    the array are rejected with ET_ERR_WORKSPACE before anything is
  *    launched; other argument rules are those of et_splitk_gemm.
- *  - Device-side errors are not observable through et_status here.
+ *  - A device-side error of the last call (a bounded wait that ran out) is
+ *    read with et_splitk_noalloc_status before the next call clears it.
  * ---------------------------------------------------------------------- */
 #define ET_SPLITK_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 int et_splitk_gemm_noalloc(const void* X, const void* Wt, void* Y, int M, int N, int K, int split,
                            void* stream);
 
+/* Device status of the last et_splitk_gemm_noalloc call on the current
+ * device: synchronises `stream` (cudaStream_t as void*), then copies the
+ * status word of the built-in scratch array to *code_out / *detail_out (host
+ * pointers; detail_out may be NULL).  Allocates nothing.  Returns ET_OK, or
+ * ET_ERR_INVALID / ET_ERR_CUDA when the status could not be read. */
+int et_splitk_noalloc_status(void* stream, int32_t* code_out, int32_t* detail_out);
+
 /* ------------------------------------------------------------------------
  * Dense dependent MLP chain, statically scheduled (tasks bound to CTAs):
  *   xhat = bf16( x / sqrt(mean(x^2) + eps) * gamma )
  *   out  = bf16( bf16( silu(xhat Wg^T) * (xhat Wu^T) ) Wd^T )
- * x bf16 [B,H]; gamma bf16 [H]; w_gate, w_up bf16 [F,H]; w_down bf16 [H,F];
- * out bf16 [B,H].  Down tiles wait on per-chunk event counters of the
- * gate/up tiles, not on a kernel boundary.
+ *
+ * Source: "Prompt Boundary-Aware Scheduling with Event Tensors for Dynamic
+ * Kernels", static versus dynamic scheduling: for dense, predictable work a
+ * static assignment of tasks to SMs is the better choice (no queue), while
+ * events still order the dependent tiles in place of kernel boundaries.
+ *
+ * x bf16 [B_max,H]; gamma bf16 [H]; eps >= 0; w_gate, w_up bf16 [F,H];
+ * w_down bf16 [H,F]; out bf16 [B_max,H] (rows >= B untouched).  RMSNorm
+ * tasks release an event the gate/up tiles wait on; down tiles wait on
+ * per-chunk event counters of the gate/up tiles.  B is used when d_B is
+ * NULL, else the device int32 *d_B (0 <= *d_B <= B_max).  H and F multiples
+ * of 128.  Errors as et_moe_layer.
  * ---------------------------------------------------------------------- */
 size_t et_mlp_workspace_bytes(int B_max, int H, int F);
 

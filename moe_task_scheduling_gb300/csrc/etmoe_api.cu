@@ -798,7 +798,9 @@ void* g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  In host code the
 // array's name is only a host-side stand-in, so the real address is looked up
-// once per device, with that device current.
+// once per device, with that device current.  Like the library's other
+// per-device state (kernel attributes), the address is kept for the life of
+// the process: after cudaDeviceReset the process must be restarted.
 int noalloc_scratch(int dev, void** out) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_noalloc_ptr[dev]) {
@@ -842,4 +844,19 @@ extern "C" int et_splitk_gemm_noalloc(const void* X, const void* Wt, void* Y, in
     cudaError_t e = cudaMemsetAsync(scratch, 0, L.partial, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(split-K scratch counters)");
     return et_splitk_gemm(X, Wt, Y, M, nullptr, M, N, K, split, scratch, need, nullptr, stream);
+}
+
+// The device status of the last et_splitk_gemm_noalloc call on the current
+// device: synchronises `stream`, then reads the status word at the start of
+// the built-in scratch array (cleared again by the next call).
+extern "C" int et_splitk_noalloc_status(void* stream, int32_t* code_out, int32_t* detail_out) {
+    g_last_error.clear();
+    if (!code_out) return fail(ET_ERR_INVALID, "code_out must be non-NULL");
+    DeviceState* st = nullptr;
+    int dev = 0;
+    int rc = device_state(&st, &dev);
+    if (rc) return rc;
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch(dev, &scratch))) return rc;
+    return et_status(scratch, stream, code_out, detail_out);
 }

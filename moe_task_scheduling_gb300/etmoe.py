@@ -66,6 +66,8 @@ _SIGNATURES = {
     "et_mlp_workspace_bytes": (_sz, [_i, _i, _i]),
     "et_mlp_chain": (_i, [_vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _vp,
                           _sz, _vp, _vp]),
+    "et_splitk_noalloc_status": (_i, [_vp, ctypes.POINTER(ctypes.c_int32),
+                                      ctypes.POINTER(ctypes.c_int32)]),
     "et_status": (_i, [_vp, _vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
     "et_reset_status": (_i, [_vp, _vp]),
 }
@@ -287,6 +289,15 @@ def et_splitk_gemm_noalloc(X, Wt, Y, *, split, M=None, stream=None, check=True):
     if check:
         _check(rc)
     return rc
+
+
+def et_splitk_noalloc_status(stream=None):
+    """(code, detail) of the last no-alloc split-K call on this device (synchronises)."""
+    code = ctypes.c_int32(0)
+    detail = ctypes.c_int32(0)
+    _check(load().et_splitk_noalloc_status(_stream(stream), ctypes.byref(code),
+                                           ctypes.byref(detail)))
+    return code.value, detail.value
 
 
 def et_mlp_chain(x, gamma, eps, w_gate, w_up, w_down, out, *, B=None, d_B=None, B_max=None,

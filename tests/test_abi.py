@@ -34,6 +34,35 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(etmoe.exported_symbols())
 
 
+SOURCES = ("Prompt Boundary-Aware Scheduling with Event Tensors", "Megakernels ch. 5",
+           "has no counterpart")
+
+
+def declaration_blocks():
+    """Each exported entry point's comment block: the last section comment
+    ("/* ----") before its first declaration in etmoe.h, with everything up to
+    the declaration (a block may cover several calls)."""
+    text = open(HEADER).read()
+    out = {}
+    for name in declared_functions():
+        m = re.search(r"\b" + name + r"\s*\(", text)
+        before = text[:m.start()]
+        block = before[before.rfind("/* ---"):]
+        out[name] = " ".join(re.sub(r"^\s*\*", " ", block, flags=re.M).split())
+    return out
+
+
+def test_every_compute_entry_point_cites_its_source():
+    """Each declaration of a compute call (and the calls the hot path consists
+    of) carries, in its own comment block, the passage that defines it."""
+    blocks = declaration_blocks()
+    compute = [n for n in blocks if not n.endswith(("_workspace_bytes", "status", "_string",
+                                                    "version"))]
+    assert {"et_moe_layer", "et_splitk_gemm", "et_mlp_chain"} <= set(compute)
+    for name in compute:
+        assert any(src in blocks[name] for src in SOURCES), f"{name}: no source named"
+
+
 def test_version_and_error_string(lib):
     assert lib.et_version() >= 100
     assert isinstance(lib.et_last_error_string(), bytes)

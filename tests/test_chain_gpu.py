@@ -181,8 +181,8 @@ def test_chain_vs_oracle(cuda_lib, oracle, kinds):
 
 def test_chain_mixtral_full_size(cuda_lib, oracle):
     """Two Mixtral-shaped fused blocks (no shared expert) in one launch against
-    the two blocks called one after another, T from device memory; the first
-    block's sampled outputs against the oracle."""
+    the two blocks called one after another, T from device memory; every output
+    row of the first block against the oracle."""
     cfg = wl.MIXTRAL
     T_max = cfg.T_max
     ch = Chain(cuda_lib, cfg, [(True, 0), (True, 0)], T_max, unit=False, device="cuda")
@@ -202,10 +202,9 @@ def test_chain_mixtral_full_size(cuda_lib, oracle):
             assert torch.equal(ch.outs[j][:T], chained[j]), f"layer {j}, T={T}"
             x = ch.outs[j]
         hb, bb = ch.layers[0][2], ch.layers[0][3]
-        sample = sorted({0, T // 2, T - 1})
         ref = oracle.moe_block(hb["x"][:T], bb["gamma"], bb["eps"], hb["wr"], hb["bias"],
-                               hb["wg"], hb["wu"], hb["wd"], k=cfg.k, tokens=sample)
-        assert_close_bf16(wl.bits(chained[0])[sample], ref["out"], f"layer 0 T={T}")
+                               hb["wg"], hb["wu"], hb["wd"], k=cfg.k)
+        assert_close_bf16(wl.bits(chained[0]), ref["out"], f"layer 0 T={T}")
 
 
 def test_chain_rejects_bad_descriptors(cuda_lib):
