@@ -155,7 +155,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.gpu)],
+                 "-lms", "20", "-i", str(self.gpu)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -195,6 +195,14 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def smi_index(local):
+    """nvidia-smi's index of this process's GPU (CUDA_VISIBLE_DEVICES respected)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis.replace(",", "").isdigit():
+        return int(vis.split(",")[local if local < len(vis.split(",")) else 0])
+    return local
 
 
 def dist_setup():
@@ -605,23 +613,24 @@ def run_chain(args, world, rank, local):
 
 
 WARMUP_CHILD = r"""
-import json, os, sys, time
+import hashlib, json, os, sys, time
 sys.path.insert(0, os.environ["ET_ROOT"])
 import torch
 from moe_task_scheduling_gb300 import workloads as wl
 cfg = wl.MIXTRAL
+Ts = [int(t) for t in os.environ.get("ET_TS", "").split(",") if t] or list(cfg.T_sweep)
 dev = torch.device("cuda")
 torch.zeros(1, device=dev)
 inp = wl.moe_inputs(cfg, device=dev)
 out = torch.empty((cfg.T_max, cfg.H), dtype=torch.bfloat16, device=dev)
-d_T = torch.ones(1, dtype=torch.int32, device=dev)
+d_T = torch.full((1,), Ts[0], dtype=torch.int32, device=dev)
 torch.cuda.synchronize()
 def now():
     torch.cuda.synchronize()
     return time.perf_counter()
 t0 = now()
 from moe_task_scheduling_gb300 import etmoe
-etmoe.load()
+etmoe.load(os.environ.get("ET_LIB") or None)
 t_load = now() - t0
 ws = etmoe.alloc_workspace(etmoe.et_moe_workspace_bytes(cfg.T_max, cfg.H, cfg.F, cfg.E, cfg.k))
 torch.cuda.synchronize()
@@ -630,50 +639,71 @@ def call():
                        k=cfg.k, T=0, d_T=d_T, T_max=cfg.T_max, workspace=ws)
 t0 = now(); call(); t_first = now() - t0
 t0 = now(); call(); t_second = now() - t0
-first_T, steady_T = {}, {}
-for T in cfg.T_sweep[1:]:
+first_T, steady_T, sha = {}, {}, {}
+for T in Ts[1:]:
     d_T.fill_(T)
     t0 = now(); call(); first_T[T] = now() - t0
-for T in cfg.T_sweep:
+for T in Ts:
     d_T.fill_(T)
     ts = []
     for _ in range(3):
         t0 = now(); call(); ts.append(now() - t0)
     steady_T[T] = sorted(ts)[1]
+    sha[T] = hashlib.sha256(out[:T].cpu().view(torch.int16).numpy().tobytes()).hexdigest()[:16]
 assert etmoe.et_status(ws) == (0, 0)
 print(json.dumps({"load_s": t_load, "first_s": t_first, "second_s": t_second,
-                  "first_T": first_T, "steady_T": steady_T}))
+                  "first_T": first_T, "steady_T": steady_T, "out_sha": sha}))
 """
 
+# token counts given their own specialised build in the warm-up comparison
+SPECIALISED_TS = (1, 512)
 
-def run_warmup(args):
-    """Warm-up cost of one kernel for every token count: the library's full
-    build (timed into a scratch directory) and one translation unit's compile;
-    then, in a fresh process, the first layer call (library load, kernel
-    attributes, tensor maps, module load, launch) and the first call at each
-    new token count against the steady state, host wall clock with a device
-    synchronise on both sides."""
-    import tempfile
-    from moe_task_scheduling_gb300 import build as B
-    with tempfile.TemporaryDirectory() as d:
-        t0 = time.perf_counter()
-        B.build(force=True, out_dir=d)
-        t_build = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        subprocess.run([B.nvcc()] + B.ARCH + B.NVCC_FLAGS +
-                       ["-c", os.path.join(B.CSRC, "moe_kernel.cu"), "-o", os.path.join(d, "m.o")],
-                       check=True, capture_output=True)
-        t_tu = time.perf_counter() - t0
-    env = dict(os.environ, ET_ROOT=ROOT)
+
+def _warmup_child(env_extra):
+    env = dict(os.environ, ET_ROOT=ROOT, **env_extra)
     r = subprocess.run([sys.executable, "-c", WARMUP_CHILD], capture_output=True, text=True,
                        env=env, timeout=600)
     if r.returncode != 0:
         raise RuntimeError("warm-up child failed: " + r.stderr[-2000:])
-    c = json.loads(r.stdout.strip().splitlines()[-1])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def run_warmup(args):
+    """Warm-up cost of one kernel for every token count against builds
+    specialised per batch size.  Measured: the library's full build (timed
+    into a scratch directory); then, in fresh processes, the first layer call
+    (library load, kernel attributes, tensor maps, module load, launch) and the
+    first call at each new token count against the steady state, host wall
+    clock with a device synchronise on both sides.  The alternative is built
+    for real at a few token counts: the library with the megakernel compiled
+    for one constant T (-DET_FIXED_T), its build timed, its first call timed
+    in a fresh process, and its output checked bit for bit against the
+    general build at that T."""
+    import tempfile
+    from moe_task_scheduling_gb300 import build as B
+    spec = []
+    with tempfile.TemporaryDirectory() as d:
+        t0 = time.perf_counter()
+        B.build(force=True, out_dir=d)
+        t_build = time.perf_counter() - t0
+        for T in SPECIALISED_TS:
+            sd = os.path.join(d, f"T{T}")
+            t0 = time.perf_counter()
+            lib = B.build(force=True, out_dir=sd, defines=(f"ET_FIXED_T={T}",))
+            t_b = time.perf_counter() - t0
+            c = _warmup_child({"ET_LIB": lib, "ET_TS": str(T)})
+            spec.append({"T": T, "build_s": round(t_b, 2),
+                         "first_call_ms": round(c["first_s"] * 1e3, 3),
+                         "steady_ms": round(c["steady_T"][str(T)] * 1e3, 3),
+                         "out_sha": c["out_sha"][str(T)]})
+    c = _warmup_child({})
+    for r in spec:
+        r["same_output_as_general_build"] = r.pop("out_sha") == c["out_sha"][str(r["T"])]
     sweep = [{"T": int(T), "first_call_ms": round(c["first_T"].get(T, c["first_s"]) * 1e3, 3),
               "steady_ms": round(c["steady_T"][T] * 1e3, 3)}
              for T in sorted(c["steady_T"], key=int)]
-    n_var = 32
+    n_sizes = len(wl.MIXTRAL.T_sweep)
+    per_build = statistics.mean(r["build_s"] for r in spec)
     return {
         "metric": "MoE layer warm-up: first call in a fresh process, one compiled kernel for "
                   "every token count (ms)",
@@ -684,10 +714,13 @@ def run_warmup(args):
         "library_load_ms": round(c["load_s"] * 1e3, 3),
         "second_call_ms": round(c["second_s"] * 1e3, 3),
         "sweep": sweep,
-        "build": {"full_library_s": round(t_build, 2), "moe_kernel_unit_s": round(t_tu, 2),
-                  "per_T_variants_analogue_s": round(n_var * t_tu, 1),
-                  "note": f"a build that specialises the kernel per batch size compiles one "
-                          f"variant per size: {n_var} x the measured unit (derived, not run)"},
+        "build": {"full_library_s": round(t_build, 2),
+                  "specialised_builds": spec,
+                  "per_size_builds_for_the_sweep_s": round(n_sizes * per_build, 1),
+                  "note": f"one build serves all {n_sizes} token counts of the sweep; builds "
+                          f"specialised per size were built and timed at T = "
+                          f"{list(SPECIALISED_TS)}, and {n_sizes} of them take {n_sizes} x "
+                          f"their mean build time"},
     }
 
 
@@ -710,8 +743,7 @@ def run_ours(args, world, rank, local):
     for _ in range(args.warmup):
         b.step()
     torch.cuda.synchronize()
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
+    gpu_index = smi_index(local)
     barrier(world)
     torch.cuda.synchronize()
     per_T = {T: [] for T in cfg.T_sweep}
@@ -788,7 +820,88 @@ def run_ours(args, world, rank, local):
                            "GPU (GPU box torch build); not run"}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(b, cfg, args)
+    if world == 1 and args.workload == "mixtral" and not args.no_extra:
+        del b
+        torch.cuda.empty_cache()
+        line.update(secondary_sweeps(args, device))
     return line
+
+
+def moe_sweep_record(cfg, Fs, device, steps, warmup):
+    """A MoE workload's own sweep as a compact record: tokens/s over the sweep,
+    per-T microseconds and roofline fractions, the sweep's HBM roofline."""
+    b = MoeBench(cfg, device, Fs)
+    touched = b.touched()
+    for _ in range(warmup):
+        b.step()
+    torch.cuda.synchronize()
+    per_T = {T: [] for T in cfg.T_sweep}
+    with ClockSampler(smi_index(device.index or 0)) as clk:
+        all_pairs = [b.step(events=True) for _ in range(steps)]
+        torch.cuda.synchronize()
+    for pairs in all_pairs:
+        for T, s0, e0 in pairs:
+            per_T[T].append(s0.elapsed_time(e0) / 1e3)
+    code, detail = b.etmoe.et_status(b.ws)
+    assert code == 0, f"device status {code} ({detail})"
+    pk = peaks()
+    total = sum(sum(v) for v in per_T.values())
+    bytes_total, sweep = 0.0, []
+    for T in cfg.T_sweep:
+        t = statistics.median(per_T[T])
+        by = moe_algorithmic_bytes(cfg, T, touched[T], Fs)
+        bytes_total += by * len(per_T[T])
+        sweep.append({"T": T, "us": round(t * 1e6, 2), "experts_touched": touched[T],
+                      "hbm_frac": round(by / t / 1e9 / pk["hbm_gbs"], 4),
+                      "tensor_frac": round(moe_algorithmic_flops(cfg, T, Fs) / t / 1e12 /
+                                           pk["bf16_tflops"], 4)})
+    achieved = bytes_total / total / 1e9
+    rec = {"value": round(steps * sum(cfg.T_sweep) / total, 1), "unit": "tokens/s",
+           "workload": f"{cfg.name} H={cfg.H} F={cfg.F} E={cfg.E} k={cfg.k}" +
+                       ("" if Fs is None else f", fused block Fs={Fs}"),
+           "sweep": sweep,
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                        "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                        "peak_source": pk["source"] + " (hbm copy, burst)",
+                        "kernel": "moe_megakernel"},
+           "gpu_launches": steps * len(cfg.T_sweep), "clocks": clk.summary()}
+    del b
+    torch.cuda.empty_cache()
+    return rec
+
+
+def dense_sweep_record(kind, device, steps, warmup):
+    b = DenseBench(kind, device)
+    with ClockSampler(smi_index(device.index or 0)) as clk:
+        res = b.measure(steps, warmup)
+    variants = 2 if kind == "splitk" else 1
+    kernel = "splitk_kernel" if kind == "splitk" else "mlp_chain_kernel"
+    rec = {"workload": (f"split-K GEMM Y[M,{b.cfg.N}] = X[M,{b.cfg.K}] W, split {b.cfg.split}"
+                        if kind == "splitk" else
+                        f"MLP chain H={b.cfg.H} F={b.cfg.F} (RMSNorm, gate/up, SiLU*mul, down)"),
+           "kernel": kernel, "sweep": res,
+           "gpu_launches": variants * steps * len(res), "clocks": clk.summary()}
+    del b
+    torch.cuda.empty_cache()
+    return rec
+
+
+def secondary_sweeps(args, device):
+    """The other configurations, measured in the same run as the headline:
+    the fine-grained skewed layer, the split-K GEMM, the MLP chain, the fused
+    Mixtral-shaped block, and the warm-up record."""
+    out = {}
+    steps, warmup = args.steps, args.warmup
+    out["fine"] = moe_sweep_record(wl.FINE, device, None, steps, warmup)
+    out["mixtral_block"] = moe_sweep_record(wl.MIXTRAL, device, 0, steps, warmup)
+    out["splitk"] = dense_sweep_record("splitk", device, steps, warmup)
+    out["mlp"] = dense_sweep_record("mlp", device, steps, warmup)
+    if not args.no_warmup_record:
+        try:
+            out["warmup"] = run_warmup(args)
+        except Exception as e:  # a failed build or child is reported, not fatal
+            out["warmup"] = {"unavailable": f"{type(e).__name__}: {str(e)[-300:]}"}
+    return out
 
 
 def run_single(args, local):
@@ -806,6 +919,76 @@ def run_single(args, local):
     code, detail = b.etmoe.et_status(b.ws)
     return {"single": args.single, "workload": args.workload, "launches": args.warmup + 1,
             "status": [code, detail]}
+
+
+TASK_NAMES = {1: "router", 2: "scan", 3: "permute", 4: "gateup", 5: "down", 6: "combine",
+              7: "norm", 9: "shared_gateup", 10: "shared_down"}
+
+
+def run_trace(args, local):
+    """One traced layer call at token count T (after `warmup` untraced calls,
+    L2 flushed before each): the kernel's own per-task records (et_opts.trace)
+    summarised per task type and role, front-end phase marks, and the
+    untraced CUDA-event time of the same call.  Times are us from the first
+    CTA's start."""
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cfg, Fs = MOE_WORKLOADS[args.workload]
+    if Fs is not None:
+        raise SystemExit("--trace covers the plain MoE layer workloads")
+    b = MoeBench(cfg, device, Fs)
+    T = args.trace
+    b.d_T.fill_(T)
+    for _ in range(args.warmup):
+        b.flush()
+        b.call()
+    ts = []
+    for _ in range(5):
+        b.flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(b.stream)
+        b.call()
+        e.record(b.stream)
+        e.synchronize()
+        ts.append(s.elapsed_time(e) * 1e3)
+    buf = b.etmoe.alloc_trace(200000, device=device)
+    b.flush()
+    i = b.inp
+    b.etmoe.et_moe_layer(i["x"], i["wr"], i["bias"], i["wg"], i["wu"], i["wd"], b.out, k=cfg.k,
+                         T=0, d_T=b.d_T, T_max=cfg.T_max, expert_counts=b.cnt, workspace=b.ws,
+                         stream=b.stream, trace=buf)
+    torch.cuda.synchronize()
+    code, detail = b.etmoe.et_status(b.ws)
+    assert code == 0, f"device status {code} ({detail})"
+    recs = b.etmoe.read_trace(buf)
+    t0 = min(r[5] for r in recs if r[1] == 2)
+
+    def us(t):
+        return round((t - t0) / 1e3, 2)
+
+    res = {"trace": T, "workload": args.workload, "us_event": round(statistics.median(ts), 2),
+           "experts_touched": int((b.cnt > 0).sum().item()), "records": len(recs)}
+    setup = sorted(r[6] for r in recs if r[1] == 2)
+    ex = [r for r in recs if r[1] == 3]
+    res["cta_setup_end"] = [us(setup[0]), us(setup[len(setup) // 2]), us(setup[-1])]
+    res["cta_exit"] = [us(min(r[5] for r in ex)), us(max(r[6] for r in ex))]
+    for role, name in ((0, "producer"), (1, "workers")):
+        d = {}
+        for ty in sorted({r[0] for r in recs if r[1] == role}):
+            rr = [r for r in recs if r[1] == role and r[0] == ty]
+            dur = sorted((r[6] - r[5]) / 1e3 for r in rr)
+            d[TASK_NAMES.get(ty, str(ty))] = {
+                "n": len(rr), "first_begin": us(min(r[5] for r in rr)),
+                "last_end": us(max(r[6] for r in rr)), "dur_median": round(dur[len(dur) // 2], 2),
+                "dur_max": round(dur[-1], 2)}
+        res[name] = d
+    phases = {}
+    for r in recs:
+        if r[1] == 4:
+            ph = phases.setdefault(r[0] - 16, [r[5], r[6], 0])
+            ph[0], ph[1], ph[2] = min(ph[0], r[5]), max(ph[1], r[6]), ph[2] + 1
+    res["front_end_phases"] = {str(k): [us(v[0]), us(v[1]), v[2]] for k, v in sorted(phases.items())}
+    return res
 
 
 def per_op_layer(inp, cfg, T, blk=None):
@@ -848,6 +1031,27 @@ def per_op_layer(inp, cfg, T, blk=None):
     return out.to(torch.bfloat16), sum(1 for c in counts if c)
 
 
+def count_launches(fn):
+    """GPU work items one call of fn enqueues, counted by the PyTorch profiler:
+    kernels, and the memory copies / fills issued as separate operations."""
+    from torch.profiler import ProfilerActivity, profile
+    try:
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+    except Exception as e:  # the profiler could not start (e.g. already in use)
+        return {"unavailable": f"torch.profiler: {type(e).__name__}"}
+    kern = copies = 0
+    for ev in prof.events():
+        if str(getattr(ev, "device_type", "")).endswith("CUDA"):
+            name = ev.name.lower()
+            if name.startswith(("memcpy", "memset")):
+                copies += 1
+            else:
+                kern += 1
+    return {"kernels": kern, "copies": copies}
+
+
 def per_op_baseline(b, cfg, reps=3):
     """Median CUDA-event time per T of per_op_layer over the same sweep (L2
     flushed before each call, host sync included), as tokens/s."""
@@ -864,9 +1068,7 @@ def per_op_baseline(b, cfg, reps=3):
             if i:
                 ts.append(s.elapsed_time(e) / 1e3)
         per_T[T] = statistics.median(ts)
-        launches[T] = 12 + 9 * touched  # router ops + per touched expert (gather, 3 GEMMs, act, add)
-        if b.blk is not None:
-            launches[T] += 8 + (6 if b.blk["sg"] is not None else 0)  # norm, residual, shared
+        launches[T] = count_launches(lambda: per_op_layer(b.inp, cfg, T, b.blk))
     tot = sum(per_T.values())
     return {"value": round(sum(cfg.T_sweep) / tot, 1), "unit": "tokens/s",
             "kind": "same-GPU per-op PyTorch (" + ("RMSNorm, " if b.blk is not None else "") +
@@ -971,6 +1173,13 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-op", action="store_true", help="skip the same-GPU per-op baseline")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="default workload: skip the secondary sweeps (fine, block, split-K, MLP)")
+    ap.add_argument("--no-warmup-record", action="store_true",
+                    help="default workload: skip the warm-up record among the secondary sweeps")
+    ap.add_argument("--trace", type=int, default=None,
+                    help="plain MoE workloads: one traced call at this token count, summarised "
+                         "(prints the summary, not a bench line)")
     ap.add_argument("--single", type=int, default=None,
                     help="MoE workloads: run warmup+1 calls at this token count and exit "
                          "(for profiler captures; prints no bench line)")
@@ -978,7 +1187,9 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
-    if args.single is not None:
+    if args.trace is not None:
+        line = run_trace(args, local) if rank == 0 else None
+    elif args.single is not None:
         if args.workload not in MOE_WORKLOADS:
             ap.error("--single applies to the MoE workloads")
         line = run_single(args, local) if rank == 0 else None

@@ -38,9 +38,11 @@ def _stale(target, deps):
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
-          out_dir: str = None) -> str:
+          out_dir: str = None, defines=()) -> str:
     """Compile (what is stale, or everything with force) into out_dir (default:
-    the in-tree _build) and link libetmoe.so there; returns its path."""
+    the in-tree _build) and link libetmoe.so there; returns its path.
+    `defines` adds -D flags (e.g. "ET_FIXED_T=1": a build specialised for one
+    token count, used only to time the per-batch-size build alternative)."""
     out_dir = out_dir or OUT_DIR
     lib = os.path.join(out_dir, "libetmoe.so")
     os.makedirs(out_dir, exist_ok=True)
@@ -53,7 +55,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
             cmd = [nvcc()] + ARCH + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_info else []) + \
-                ["-c", s, "-o", o]
+                ["-D" + d for d in defines] + ["-c", s, "-o", o]
             jobs.append(cmd)
 
     def run(cmd):

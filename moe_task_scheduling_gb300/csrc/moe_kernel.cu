@@ -1251,8 +1251,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) trace_rec(p0, 0, 2, 0, 0, t_start, globaltimer_ns());
 
+#ifdef ET_FIXED_T
+    // A build specialised for one token count (the per-batch-size builds the
+    // warm-up comparison times): T is a compile-time constant, the host and
+    // device counts are ignored.
+    int T = ET_FIXED_T;
+#else
     int T = p0.T_host;
     if (p0.d_T) T = *reinterpret_cast<const volatile int32_t*>(p0.d_T);
+#endif
     if (T < 0 || T > p0.T_max) {
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(wc, ET_ERR_BOUNDS, kWhereBoundsT);
         T = 0;
