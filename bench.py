@@ -892,8 +892,8 @@ def secondary_sweeps(args, device):
     Mixtral-shaped block, and the warm-up record."""
     out = {}
     steps, warmup = args.steps, args.warmup
-    out["fine"] = moe_sweep_record(wl.FINE, device, None, steps, warmup)
-    out["mixtral_block"] = moe_sweep_record(wl.MIXTRAL, device, 0, steps, warmup)
+    out["fine"] = moe_sweep_record(wl.FINE, None, device, steps, warmup)
+    out["mixtral_block"] = moe_sweep_record(wl.MIXTRAL, 0, device, steps, warmup)
     out["splitk"] = dense_sweep_record("splitk", device, steps, warmup)
     out["mlp"] = dense_sweep_record("mlp", device, steps, warmup)
     if not args.no_warmup_record:
@@ -1068,6 +1068,10 @@ def per_op_baseline(b, cfg, reps=3):
             if i:
                 ts.append(s.elapsed_time(e) / 1e3)
         per_T[T] = statistics.median(ts)
+    # counted after every timing (the profiler slows what runs after it starts),
+    # with one uncounted pass first (its first session records nothing)
+    count_launches(lambda: per_op_layer(b.inp, cfg, cfg.T_sweep[0], b.blk))
+    for T in cfg.T_sweep:
         launches[T] = count_launches(lambda: per_op_layer(b.inp, cfg, T, b.blk))
     tot = sum(per_T.values())
     return {"value": round(sum(cfg.T_sweep) / tot, 1), "unit": "tokens/s",

@@ -74,10 +74,15 @@ typedef struct et_opts {
                             consumers must time out cleanly */
     int32_t fault_arg;
     void* trace;         /* optional DEVICE buffer of 32 + 32*trace_cap bytes,
-                            zeroed by the caller: et_moe_layer appends one
-                            record per task and role -- {int32 type | role<<8,
-                            a, b, cta; uint64 t_begin, t_end} (%globaltimer ns)
-                            after a uint64 record count.  NULL = no trace. */
+                            zeroed by the caller: the MoE calls, et_splitk_gemm
+                            and et_mlp_chain write one record per task and
+                            role (and one per ring fill) -- {int32 type |
+                            role<<8, a, b, cta; uint64 t_begin, t_end}
+                            (%globaltimer ns) -- after a 32-byte header; each
+                            CTA owns trace_cap / grid consecutive records and
+                            drops what does not fit; unused records stay zero.
+                            NULL = no trace.  A diagnostic beyond the
+                            computation: it changes no result. */
 } et_opts;
 
 /* ------------------------------------------------------------------------

@@ -293,7 +293,9 @@ __device__ __forceinline__ bool ev_wait_geq(const WaitCtx& c, const int* ctr, in
 // Bounded mbarrier phase wait (same contract as ev_wait_geq).
 // After a short spin the waiter sleeps between polls, so a long wait (an idle
 // MMA or producer thread while the workers run a SIMT task) does not take
-// issue slots from the warps that share its SM sub-partition.
+// issue slots from the warps that share its SM sub-partition.  (A hardware
+// suspend -- try_wait with a suspend-time hint of 0.3 or 2 us -- measured no
+// faster, the fills' recycle slower.)
 __device__ __forceinline__ bool mbar_wait(const WaitCtx& c, uint64_t* bar, uint32_t parity,
                                        int where) {
     if (mbar_try_wait(bar, parity)) return true;

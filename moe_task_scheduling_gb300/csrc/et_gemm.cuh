@@ -47,6 +47,7 @@ constexpr int kAccSlotCols = 256;  // TMEM columns per accumulator slot
 struct TaskMsg {
     int32_t type, a, b, c;  // type | (split << 8), then task-specific indices
     int32_t e, row0, rows, n;
+    uint32_t aux;           // MoE gate/up tile of a one-router-tile batch: its tokens (bit t)
 };
 
 // Per-CTA control block, after the stage ring and the SIMT scratch in smem.
@@ -68,6 +69,7 @@ struct Ctl {
     int32_t wflag[2];  // worker_wait decisions, double buffered
     int32_t ring_ret;  // ring leases the workers have returned
     int32_t scratch[16];
+    uint32_t post_ns[kSlots];  // trace: low word of %globaltimer when each fill was posted
 };
 
 // The byte ring of stage fills.
@@ -137,6 +139,45 @@ __device__ __forceinline__ uint32_t ring_place(uint32_t& head, uint32_t sb, uint
     head += sb;
     return start;
 }
+
+// ------------------------------------------------------------------ trace
+
+// Optional per-task record (see et_opts.trace): {type | role << 8, a, b, cta,
+// t_begin, t_end}.  Each CTA owns an equal share of the buffer's records and
+// fills it through a shared-memory counter, so a record costs plain stores
+// (no global atomic on the path being timed); records beyond a CTA's share
+// are dropped, unused ones stay zero.
+__device__ __forceinline__ unsigned* trace_counter() {
+    __shared__ unsigned n;
+    return &n;
+}
+__device__ __forceinline__ void trace_init() {  // thread 0, before the CTA's first barrier
+    *trace_counter() = 0;
+}
+__device__ __forceinline__ void trace_put(uint64_t* buf, int cap, int type, int role, int a,
+                                          int b, uint64_t t0, uint64_t t1) {
+    if (!buf) return;
+    const unsigned per = static_cast<unsigned>(cap) / gridDim.x;
+    const unsigned i = atomicAdd(trace_counter(), 1u);
+    if (i >= per) return;
+    int4* r = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(buf) + 32 +
+                                      (static_cast<size_t>(blockIdx.x) * per + i) * 32);
+    r[0] = make_int4(type | (role << 8), a, b, static_cast<int>(blockIdx.x));
+    uint64_t* t = reinterpret_cast<uint64_t*>(r + 1);
+    t[0] = t0;
+    t[1] = t1;
+}
+
+// Records a worker task (role 1) when it leaves scope, on any path.
+struct TraceOnExit {
+    uint64_t* buf;
+    int cap, type, a;
+    uint64_t t0;
+    bool on;
+    __device__ __forceinline__ ~TraceOnExit() {
+        if (on && buf) trace_put(buf, cap, type, 1, a, 0, t0, globaltimer_ns());
+    }
+};
 
 // ------------------------------------------------------------------ producer
 
@@ -231,42 +272,187 @@ __device__ __forceinline__ void load_acts(const GemmTask& t, const Ring& R, Ctl*
     }
 }
 
+// ------------------------------------------------------------------ producer lookahead
+
+// A GEMM task whose fills are being posted.  Fills are posted in task order
+// (every fill of a task before any fill of the next), so the MMA issuer, which
+// walks tasks and fills in order, is unchanged.  While the current task waits
+// on its dependency, the producer requests the weight tiles of the CTA's next
+// task into ring space that is free at that moment -- it never waits for
+// space on the next task's behalf, so the fills the current task needs can
+// always be placed -- and a dependency wait no longer leaves the ring idle.
+struct Flight {
+    GemmTask t;
+    uint32_t f0;    // ring fill number of the task's first fill
+    int nfill;      // fills in all
+    int posted;     // fills whose weight tiles are requested
+    int acts;       // ... whose activation rows are requested too
+    bool ready;     // the dependency is met (or there is none)
+    int type, a, b; // trace: the task
+    uint64_t t_pop; // trace: when the task was taken
+};
+
+__device__ __forceinline__ void flight_begin(Flight& f, const GemmTask& t, int type, int a, int b,
+                                             uint64_t t_pop) {
+    f.t = t;
+    f.f0 = 0;
+    f.nfill = fills_of(t);
+    f.posted = 0;
+    f.acts = 0;
+    f.ready = t.dep == nullptr;
+    if (!f.ready && ld_acquire(t.dep) >= t.dep_target) {
+        f.ready = true;
+        fence_proxy_async_global();  // rows written by other CTAs' generic stores
+    }
+    f.type = type;
+    f.a = a;
+    f.b = b;
+    f.t_pop = t_pop;
+}
+
+// ring_reserve without waiting: true when a fill of `sb` bytes at `start` has
+// a barrier slot and its bytes free right now (released fills are retired).
+__device__ __forceinline__ bool ring_try_reserve(Ctl* ctl, ProdState& ps, uint32_t start,
+                                                 uint32_t sb, uint32_t rb) {
+    while (ps.rel < ps.it && (ps.it - ps.rel >= static_cast<uint32_t>(kSlots) ||
+                              start + sb > ps.tail + rb)) {
+        const uint32_t slot = ps.rel % kSlots;
+        if (!mbar_try_wait(&ctl->empty[slot], (ps.rel / kSlots) & 1u)) return false;
+        ps.tail = ctl->unit_end[slot];
+        ++ps.rel;
+    }
+    return true;
+}
+
+// Post the next fill of f at ring position `start` (space reserved): its byte
+// count and weight tiles, and its activation rows once the dependency is met.
+__device__ __forceinline__ void flight_post(Flight& f, const Ring& R, Ctl* ctl, ProdState& ps,
+                                            uint32_t start, uint64_t pol_w, uint64_t pol_b) {
+    const GemmTask& t = f.t;
+    const uint32_t slot = ps.it % kSlots;
+    ctl->unit_end[slot] = start + unit_bytes(t);
+    ctl->post_ns[slot] = static_cast<uint32_t>(globaltimer_ns());
+    if (f.posted == 0) f.f0 = ps.it;
+    const int u = f.posted, kp = kpack_of(t);
+    int nk;
+    const int kb = fill_kb(t, u, nk);
+    mbar_arrive_expect_tx(&ctl->full[slot], static_cast<uint32_t>(nk) * kblock_bytes(t));
+    uint8_t* dst = R.base + start % R.bytes;
+    for (int j = 0; j < nk; ++j) {
+        const int kx = (t.kb0 + kb + j) * kBlockK;
+        tma_load_2d(dst + j * kABytes, t.a0, &ctl->full[slot], kx, t.a_row, pol_w);
+        if (t.a1)
+            tma_load_2d(dst + (kp + j) * kABytes, t.a1, &ctl->full[slot], kx, t.a_row + t.a1_off,
+                        pol_w);
+    }
+    ++ps.it;
+    ++f.posted;
+    ctl->issued = static_cast<int32_t>(ps.it);
+    if (f.ready) {
+        load_acts(t, R, ctl, ps.it - 1, u, pol_b);
+        ++f.acts;
+    }
+}
+
+// Post fills of f while ring space is free now (never waits).
+__device__ __forceinline__ void flight_post_nowait(Flight& f, const Ring& R, Ctl* ctl,
+                                                   ProdState& ps, uint64_t pol_w, uint64_t pol_b) {
+    const uint32_t sb = unit_bytes(f.t);
+    while (f.posted < f.nfill) {
+        uint32_t h = ps.head;
+        const uint32_t start = ring_place(h, sb, R.bytes);
+        if (!ring_try_reserve(ctl, ps, start, sb, R.bytes)) return;
+        ps.head = h;
+        flight_post(f, R, ctl, ps, start, pol_w, pol_b);
+    }
+}
+
+// Wait (bounded) until f's dependency is met, then request the activation
+// rows of its posted fills.  Between polls f's own weights are posted as ring
+// space frees up; once every fill of f is posted, `idle()` runs instead (the
+// caller looks ahead to its next task there).  Returns false on a timeout
+// (recorded) or an abort.
+template <class Idle>
+__device__ __forceinline__ bool flight_wait(Flight& f, const Ring& R, Ctl* ctl, ProdState& ps,
+                                            const WaitCtx& wc, uint64_t pol_w, uint64_t pol_b,
+                                            Idle&& idle) {
+    if (!f.ready) {
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t ns = 32;
+        for (;;) {
+            if (f.posted < f.nfill)
+                flight_post_nowait(f, R, ctl, ps, pol_w, pol_b);
+            else
+                idle();
+            if (ld_acquire(f.t.dep) >= f.t.dep_target) break;
+            if (aborted(wc)) return false;
+            if (globaltimer_ns() - t0 > wc.timeout_ns) {
+                raise_error(wc, ET_ERR_TIMEOUT, f.t.dep_where);
+                return false;
+            }
+            __nanosleep(ns);
+            if (ns < 256) ns <<= 1;
+        }
+        f.ready = true;
+        fence_proxy_async_global();  // rows written by other CTAs' generic stores
+    }
+    for (; f.acts < f.posted; ++f.acts) load_acts(f.t, R, ctl, f.f0 + f.acts, f.acts, pol_b);
+    return true;
+}
+
+// Post the remaining fills of f (its dependency met), waiting for ring space
+// -- the older fills it waits for all have their activation rows requested.
+__device__ __forceinline__ bool flight_finish(Flight& f, const Ring& R, Ctl* ctl, ProdState& ps,
+                                              const WaitCtx& wc, uint64_t pol_w, uint64_t pol_b) {
+    const uint32_t sb = unit_bytes(f.t);
+    while (f.posted < f.nfill) {
+        const uint32_t start = ring_place(ps.head, sb, R.bytes);
+        if (!ring_reserve(ctl, ps, start, sb, R.bytes, wc)) return false;
+        flight_post(f, R, ctl, ps, start, pol_w, pol_b);
+    }
+    return true;
+}
+
+// A static schedule's producer: the CTA's GEMM tasks in order, `next(t)`
+// giving the next one (false at the end), with one task of lookahead.
+template <class Next>
+__device__ __forceinline__ void produce_static(Next&& next, const Ring& R, Ctl* ctl,
+                                               const WaitCtx& wc, uint64_t pol_w, uint64_t pol_b) {
+    ProdState ps;
+    Flight fc, fn;
+    bool has_next = false;
+    GemmTask t;
+    for (;;) {
+        if (has_next) {
+            fc = fn;
+            has_next = false;
+        } else {
+            if (!next(t)) break;
+            flight_begin(fc, t, 0, 0, 0, 0);
+            flight_post_nowait(fc, R, ctl, ps, pol_w, pol_b);
+        }
+        const bool ok = flight_wait(fc, R, ctl, ps, wc, pol_w, pol_b, [&]() {
+            if (!has_next && next(t)) {
+                flight_begin(fn, t, 0, 0, 0, 0);
+                has_next = true;
+            }
+            if (has_next) flight_post_nowait(fn, R, ctl, ps, pol_w, pol_b);
+        });
+        if (!ok || !flight_finish(fc, R, ctl, ps, wc, pol_w, pol_b)) break;
+    }
+}
+
+// One task, posted whole: its fills that fit now, the dependency, then every
+// remaining fill (waiting for ring space).
 __device__ __forceinline__ bool produce_task(const GemmTask& t, const Ring& R, Ctl* ctl,
                                              ProdState& ps, const WaitCtx& wc, uint64_t pol_w,
                                              uint64_t pol_b) {
     if (!ring_lease_wait(ctl, ps, wc)) return false;
-    const uint32_t sb = unit_bytes(t);
-    const int nfill = fills_of(t);
-    int pre = 0;
-    if (t.dep) {  // fills whose space frees up without any fill of this task
-        uint32_t h = ps.head;
-        const uint32_t limit = ps.head + R.bytes;
-        while (pre < nfill && pre < kSlots) {
-            const uint32_t st = ring_place(h, sb, R.bytes);
-            if (st + sb > limit) break;
-            ++pre;
-        }
-    }
-    const uint32_t f0 = ps.it;
-    bool ok = true;
-    int posted = 0;
-    for (int u = 0; u < pre && ok; ++u) {  // weights first, ahead of the dependency
-        ok = post_weights(t, R, ctl, ps, u, wc, pol_w);
-        if (ok) posted = u + 1;
-    }
-    if (ok && t.dep) {
-        ok = ev_wait_geq(wc, t.dep, t.dep_target, t.dep_where);
-        if (ok) {
-            fence_proxy_async_global();  // rows written by other CTAs' generic stores
-            for (int u = 0; u < posted; ++u) load_acts(t, R, ctl, f0 + u, u, pol_b);
-        }
-    }
-    for (int u = pre; u < nfill && ok; ++u) {
-        ok = post_weights(t, R, ctl, ps, u, wc, pol_w);
-        if (ok) load_acts(t, R, ctl, ps.it - 1, u, pol_b);
-    }
-    ctl->issued = static_cast<int32_t>(ps.it);
-    return ok;
+    Flight f;
+    flight_begin(f, t, 0, 0, 0, 0);
+    flight_post_nowait(f, R, ctl, ps, pol_w, pol_b);
+    return flight_wait(f, R, ctl, ps, wc, pol_w, pol_b, []() {}) &&
+           flight_finish(f, R, ctl, ps, wc, pol_w, pol_b);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -277,8 +463,15 @@ struct MmaState {
     uint32_t acc = 0;   // accumulator slots taken
 };
 
+// A per-fill trace hook of mma_task: called as fn(u, t_posted, t_landed) (ns).
+struct NoFillTrace {
+    __device__ __forceinline__ void operator()(int, uint64_t, uint64_t) const {}
+};
+
+template <class FillTrace = NoFillTrace>
 __device__ __forceinline__ bool mma_task(const GemmTask& t, const Ring& R, Ctl* ctl, MmaState& ms,
-                                         uint32_t tmem, const WaitCtx& wc) {
+                                         uint32_t tmem, const WaitCtx& wc,
+                                         const FillTrace& ftr = FillTrace()) {
     const uint32_t w = acc_slots(t.a1 != nullptr, t.n);
     for (uint32_t i = 0; i < w; ++i) {
         const uint32_t s = ms.acc + i;
@@ -297,6 +490,12 @@ __device__ __forceinline__ bool mma_task(const GemmTask& t, const Ring& R, Ctl* 
         const uint32_t start = ring_place(ms.head, sb, R.bytes);
         const uint32_t slot = ms.it % kSlots;
         if (!mbar_wait(wc, &ctl->full[slot], (ms.it / kSlots) & 1u, kWhereFull)) return false;
+        {
+            const uint64_t now = globaltimer_ns();
+            uint64_t tp = (now & ~0xffffffffull) | ctl->post_ns[slot];
+            if (tp > now) tp -= 1ull << 32;
+            ftr(u, tp, now);
+        }
         ms.it += 1;
         ctl->consumed = static_cast<int32_t>(ms.it);
         tc_fence_after();
@@ -496,6 +695,7 @@ __device__ __forceinline__ Ctl* cta_setup(uint8_t* smem_raw, int scratch, Ring& 
         }
         mbar_init(&ctl->drain, 1);
         mbar_init(&ctl->sbar, 1);
+        trace_init();
         ctl->issued = 0;
         ctl->consumed = 0;
         ctl->ring_ret = 0;

@@ -85,7 +85,8 @@ enum WaitWhere {
 // Task descriptor of the dynamic queue: {type, a, b, c}
 enum TaskType { kTaskExit = 0, kTaskRouter = 1, kTaskScan = 2, kTaskPermute = 3,
                 kTaskGateUp = 4, kTaskDown = 5, kTaskCombine = 6, kTaskNorm = 7,
-                kTaskSplitK = 8, kTaskShGateUp = 9, kTaskShDown = 10 };
+                kTaskSplitK = 8, kTaskShGateUp = 9, kTaskShDown = 10, kTaskReduce = 11,
+                kTaskNone = 15 /* producer only: nothing can be taken yet */ };
 
 // ---------------------------------------------------------------- kernel argument blocks
 
@@ -121,6 +122,8 @@ struct MoeArgs {
     int32_t* ev_gu;       // [mt_max * F/128]: K chunks done per gate/up tile (self-resetting)
     int gu_cap;           // rows of each gu_part half
     int mt_max, split_rows_cap, r_max;
+    int split_mask;       // down splits d in [2, 8] that divide F/128 into chunks of >= 4 k-blocks (bit d)
+    int kc_mask;          // gate/up K splits kc in {2, 4, 8} that divide H/64 into >= 8 k-blocks (bit kc)
     int wr_box;           // router-weight TMA box height (0: the weight is read in place)
     int b_wide;           // the 64-row activation maps are valid (enough rows)
     int num_ctas;
@@ -156,6 +159,8 @@ struct SplitKArgs {
     int num_ctas;
     uint64_t timeout_ns;
     int fault_mode, fault_arg;
+    uint64_t* trace;      // optional per-task trace (see et_opts)
+    int trace_cap;
 };
 
 struct MlpArgs {
@@ -168,9 +173,9 @@ struct MlpArgs {
     EtHeader* hdr;
     bf16* xhat;           // [B_max, H]
     bf16* h;              // [B_max, F]
-    int32_t* ev_h;        // [mt_max * kSplitMax]
+    int32_t* ev_h;        // [mt_max * kMlpSplitMax]
     int32_t* ev_y;        // [mt_max * H/128], self-resetting
-    float* partial;       // [kSplitMax, B_max, H]
+    float* partial;       // [kMlpSplitMax, B_max, H]
     float* gu_part;       // [2][gu_cap, F]: gate then up fp32 partials of K-split tiles
     int32_t* ev_gu;       // [mt_max * F/128]: K chunks done per gate/up tile (self-resetting)
     int gu_cap;           // rows of each gu_part half (K chunks x batch rows)
@@ -179,7 +184,10 @@ struct MlpArgs {
     int num_ctas;
     uint64_t timeout_ns;
     int fault_mode, fault_arg;
+    uint64_t* trace;      // optional per-task trace (see et_opts)
+    int trace_cap;
 };
 constexpr int kMlpGuRowsCap = 256;   // MLP: K chunks x B rows of gate/up partials at most
+constexpr int kMlpSplitMax = 16;     // MLP: largest split of the down projection
 
 }  // namespace et

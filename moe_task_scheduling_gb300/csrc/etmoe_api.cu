@@ -274,11 +274,11 @@ MlpLayout mlp_layout(int B_max, int H, int F) {
     MlpLayout L{};
     L.mt_max = ceil_div(B_max, kWideNMax);
     Carve c;
-    L.ev_h = c.take(sizeof(int) * L.mt_max * kSplitMax);
+    L.ev_h = c.take(sizeof(int) * L.mt_max * kMlpSplitMax);
     L.ev_y = c.take(sizeof(int) * L.mt_max * (H / kTileM));
     L.xhat = c.take(sizeof(uint16_t) * static_cast<size_t>(B_max) * H, 1024);
     L.h = c.take(sizeof(uint16_t) * static_cast<size_t>(B_max) * F, 1024);
-    L.partial = c.take(sizeof(float) * static_cast<size_t>(kSplitMax) * B_max * H, 1024);
+    L.partial = c.take(sizeof(float) * static_cast<size_t>(kMlpSplitMax) * B_max * H, 1024);
     L.gu_cap = B_max * kGuSplitMax < kMlpGuRowsCap ? B_max * kGuSplitMax : kMlpGuRowsCap;
     L.ev_gu = c.take(sizeof(int) * L.mt_max * (F / kTileM));
     L.gu_part = c.take(sizeof(float) * 2 * static_cast<size_t>(L.gu_cap) * F, 1024);
@@ -370,7 +370,8 @@ int moe_run(const void* x, const LayerIn* layers, int nl, int T, const int32_t* 
         st->moe = true;
     }
     MoeArgs args[kMaxLayers];
-    CUtensorMap maps[13 * kMaxLayers];
+    constexpr int kMaps = 14;  // tensor maps a layer (the kernel's MoeLayerMaps)
+    CUtensorMap maps[kMaps * kMaxLayers];
     for (int l = 0; l < nl; ++l) {
         const LayerIn& li = layers[l];
         const BlockIn& b = li.b;
@@ -417,6 +418,12 @@ int moe_run(const void* x, const LayerIn* layers, int nl, int T, const int32_t* 
         a.split_rows_cap = L.split_cap;
         a.r_max = L.r_max;
         a.wr_box = E % 8 == 0 ? (H % 256 == 0 ? 256 : 128) : 0;
+        a.split_mask = 0;
+        for (int d = 2; d <= kSplitMax; ++d)
+            if ((F / kTileM) % d == 0 && F / kBlockK / d >= 4) a.split_mask |= 1 << d;
+        a.kc_mask = 0;
+        for (int kc = 2; kc <= kGuSplitMax; kc *= 2)
+            if ((H / kBlockK) % kc == 0 && H / kBlockK / kc >= 8) a.kc_mask |= 1 << kc;
         a.num_ctas = st->sms;
         a.timeout_ns = timeout_ns_of(opts);
         a.fault_mode = (opts && l == 0) ? opts->fault_mode : 0;
@@ -441,7 +448,7 @@ int moe_run(const void* x, const LayerIn* layers, int nl, int T, const int32_t* 
             }
         }
 
-        CUtensorMap* mp = maps + 13 * l;
+        CUtensorMap* mp = maps + kMaps * l;
         const uint64_t EF = static_cast<uint64_t>(E) * F, EH = static_cast<uint64_t>(E) * H;
         if ((rc = make_map(&mp[0], li.w_gate, EF, H, kTileM, "w_gate"))) return rc;
         if ((rc = make_map(&mp[1], li.w_up, EF, H, kTileM, "w_up"))) return rc;
@@ -470,6 +477,10 @@ int moe_run(const void* x, const LayerIn* layers, int nl, int T, const int32_t* 
             if ((rc = make_map(&mp[11], a.xn, T_max, H, kBBoxRows, "x_hat"))) return rc;
             if ((rc = make_map(&mp[12], a.hs, T_max, Fs, kBBoxRows, "shared h"))) return rc;
         }
+        // the router's input rows (x_hat in a fused block), 16-row boxes
+        if ((rc = make_map(&mp[13], b.on ? static_cast<const void*>(a.xn) : static_cast<const void*>(a.x),
+                           T_max, H, kBBoxRows, "router input")))
+            return rc;
     }
     cudaError_t e = launch_moe(args, maps, nl, st->sms, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "launch of the MoE megakernel");
@@ -643,6 +654,8 @@ int splitk_run(const void* X, const void* Wt, void* Y, int M, const int32_t* d_M
     a.timeout_ns = timeout_ns_of(opts);
     a.fault_mode = opts ? opts->fault_mode : 0;
     a.fault_arg = opts ? opts->fault_arg : 0;
+    a.trace = (opts && opts->trace && opts->trace_cap) ? static_cast<uint64_t*>(opts->trace) : nullptr;
+    a.trace_cap = opts ? static_cast<int>(opts->trace_cap) : 0;
     CUtensorMap maps[3];
     if ((rc = make_map(&maps[0], Wt, N, K, kTileM, "Wt"))) return rc;
     if ((rc = make_map(&maps[1], X, M_max, K, kBBoxRows, "X"))) return rc;
@@ -737,6 +750,8 @@ int et_mlp_chain(const void* x, const void* gamma, float eps, const void* w_gate
     a.timeout_ns = timeout_ns_of(opts);
     a.fault_mode = opts ? opts->fault_mode : 0;
     a.fault_arg = opts ? opts->fault_arg : 0;
+    a.trace = (opts && opts->trace && opts->trace_cap) ? static_cast<uint64_t*>(opts->trace) : nullptr;
+    a.trace_cap = opts ? static_cast<int>(opts->trace_cap) : 0;
     CUtensorMap maps[7];
     if ((rc = make_map(&maps[0], w_gate, F, H, kTileM, "w_gate"))) return rc;
     if ((rc = make_map(&maps[1], w_up, F, H, kTileM, "w_up"))) return rc;

@@ -4,7 +4,7 @@
 //   out  = bf16(h Wd^T)
 // Tasks are bound to CTAs by index (task i runs on CTA i mod grid, in index
 // order) -- no queue, no atomics for distribution.  Index order is
-//   [0, NR)                 NORM i      8 rows each;      releases ev_norm
+//   [0, NR)                 NORM i      row i (the whole worker group); releases ev_norm
 //   [NR, NR + MT*FT*KC)     GATEUP m,f,c waits ev_norm >= NR; with a K split (small
 //                                       batches: K chunks c) stores fp32 partials, and
 //                                       the chunk that completes ev_gu[m][f] sums them;
@@ -26,7 +26,7 @@
 
 namespace et {
 
-constexpr int kNormRows = 8;  // one row per worker warp
+constexpr int kNormRows = 1;  // rows per NORM task (the whole worker group takes a row)
 
 constexpr int kRedRows = 32;  // rows per REDUCE task
 
@@ -39,6 +39,11 @@ struct MlpTile {
     int i, mt, ft, kc, s, ht, rows, n;
 };
 
+// Task index -> task (see the order above).  The down tiles come after
+// every gate/up tile: placed right behind their own chunk's gate/up tiles
+// they were measured slower (88-90 -> 100-113 us at B = 1..8): a down tile
+// that waits for its chunk stalls its CTA's in-order sequence, and with it
+// gate/up tiles other chunks wait for.
 __device__ __forceinline__ MlpTile mlp_tile(const MlpPlan& P, int task) {
     MlpTile t{};
     if (task < P.NR) {
@@ -72,17 +77,28 @@ __device__ __forceinline__ MlpTile mlp_tile(const MlpPlan& P, int task) {
     return t;
 }
 
-__device__ __forceinline__ void norm_rows(const MlpArgs& p, int B, int i) {
-    const int wwarp = (threadIdx.x >> 5) - kEpiWarp0, lane = threadIdx.x & 31;
-    const int H = p.H;
-    for (int r = 0; r < kNormRows / (kWorkers / 32); ++r) {
-        const int row = i * kNormRows + wwarp * (kNormRows / (kWorkers / 32)) + r;
-        if (row >= B) break;
-        const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(row) * H);
-        float ss = 0.0f;
-        for (int c = lane; c < H / 8; c += 32) {
-            const uint4 raw = __ldg(xr + c);
-            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+// RMSNorm of row i by the whole worker group: each thread takes every 256th
+// 16-byte vector of the row (up to four loads in flight), so a cold row costs
+// about one memory round trip (one warp walking a 4096-wide row load after
+// load took 9-13 us, and every gate/up tile waits for the norm).  The sum of
+// squares meets through shared memory (warp partials added in warp order).
+__device__ __forceinline__ void norm_row(const MlpArgs& p, int row, Ctl* ctl) {
+    const int wt = static_cast<int>(threadIdx.x) - kEpiWarp0 * 32, lane = wt & 31;
+    const int H = p.H, nv = H / 8;  // 16-byte vectors a row
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(row) * H);
+    const uint4* gr = reinterpret_cast<const uint4*>(p.gamma);
+    for (int c = wt * 8; c < nv; c += kWorkers * 8)  // gamma, one 128-byte line a prefetch
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(gr + c) : "memory");
+    float ss = 0.0f;
+    for (int c0 = wt; c0 < nv; c0 += kWorkers * 4) {
+        uint4 raw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + u * kWorkers < nv) raw[u] = __ldg(xr + c0 + u * kWorkers);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (c0 + u * kWorkers >= nv) continue;
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float2 f = __bfloat1622float2(b2[q]);
@@ -90,15 +106,30 @@ __device__ __forceinline__ void norm_rows(const MlpArgs& p, int B, int i) {
                 ss = fmaf(f.y, f.y, ss);
             }
         }
+    }
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float rs = rsqrtf(ss / static_cast<float>(H) + p.eps);
-        const uint4* gr = reinterpret_cast<const uint4*>(p.gamma);
-        uint4* outr = reinterpret_cast<uint4*>(p.xhat + static_cast<size_t>(row) * H);
-        for (int c = lane; c < H / 8; c += 32) {
-            const uint4 raw = __ldg(xr + c), graw = __ldg(gr + c);
-            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&graw);
+    for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    float* part = reinterpret_cast<float*>(ctl->scratch);  // [8] warp partials
+    if (lane == 0) part[wt >> 5] = ss;
+    worker_sync();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWorkers / 32; ++w) tot += part[w];
+    const float rs = rsqrtf(tot / static_cast<float>(H) + p.eps);
+    uint4* outr = reinterpret_cast<uint4*>(p.xhat + static_cast<size_t>(row) * H);
+    for (int c0 = wt; c0 < nv; c0 += kWorkers * 4) {
+        uint4 raw[4], graw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + u * kWorkers < nv) {
+                raw[u] = __ldg(xr + c0 + u * kWorkers);
+                graw[u] = __ldg(gr + c0 + u * kWorkers);
+            }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (c0 + u * kWorkers >= nv) continue;
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&graw[u]);
             uint4 o;
             __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
@@ -107,9 +138,10 @@ __device__ __forceinline__ void norm_rows(const MlpArgs& p, int B, int i) {
                 const float2 g = __bfloat1622float2(g2[q]);
                 o2[q] = __floats2bfloat162_rn(f.x * rs * g.x, f.y * rs * g.y);
             }
-            outr[c] = o;
+            outr[c0 + u * kWorkers] = o;
         }
     }
+    worker_sync();  // the partials are read before a later row writes them
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -118,9 +150,11 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                  const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_xhat64,
                  const __grid_constant__ CUtensorMap tm_h64, const __grid_constant__ MlpArgs p) {
     extern __shared__ uint8_t smem_raw[];
+    const uint64_t t_start = globaltimer_ns();
     Ring ring;
     uint8_t* scratch;
     Ctl* ctl = cta_setup(smem_raw, 0, ring, &scratch);
+    if (threadIdx.x == 0) trace_put(p.trace, p.trace_cap, 0, 2, 0, 0, t_start, globaltimer_ns());
     const WaitCtx wc{p.hdr, p.timeout_ns};
     const uint32_t tmem = ctl->tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,17 +170,40 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     P.HT = p.H / kTileM;
     P.NR = ceil_div(P.B, kNormRows);
     P.MT = ceil_div(P.B, kWideNMax);
-    // split of the down projection: none when the down tiles already cover
-    // every CTA, else the smallest divisor of FT (<= 8) that does, else the
-    // largest such divisor
+    // A CTA whose first task is a NORM runs it before anything else: its row
+    // loads then reach memory ahead of the weight tiles every producer posts
+    // (ahead of the norm's release) -- behind them a lone row's loads took
+    // 7-9 us, and every gate/up tile waits for the norms.
+    const bool early_norm = static_cast<int>(blockIdx.x) < P.NR;
+    if (early_norm && warp >= kEpiWarp0) {
+        norm_row(p, blockIdx.x, ctl);
+        fence_proxy_async_global();  // x_hat is read by TMA
+        worker_sync();
+        if (threadIdx.x == kEpiWarp0 * 32) {
+            __threadfence();
+            red_release_add(&p.hdr->ev_norm, 1);
+        }
+    }
+    // split of the down projection over F: the smallest divisor S of FT
+    // (<= 16, chunks of >= 4 k-blocks) that gives every CTA a down tile, at
+    // most 4 above 64 rows, whose fp32 partials (written, then read back,
+    // 2 x B x H x 4 bytes a split) grow with the batch.  Measured on the
+    // configured shape (H 4096, F 14336): S = 7 / 14 / 4 at B = 1 gave 89 /
+    // 89 / 90 us, at B = 64 98 / 109 / 109 us; S = 4 against 7 at B = 128
+    // 104 against 111 us, at B = 256 135 against 139 us.
+#ifndef ET_MLP_SPLIT
     P.S = 1;
     if (P.MT > 0 && P.MT * P.HT < static_cast<int>(gridDim.x)) {
-        for (int d = 2; d <= kSplitMax; ++d) {
-            if (P.FT % d) continue;
+        const int cap = P.B > 64 ? 4 : kMlpSplitMax;
+        for (int d = 2; d <= cap; ++d) {
+            if (P.FT % d || p.F / d / kBlockK < 4) continue;
             P.S = d;
             if (P.MT * P.HT * d >= static_cast<int>(gridDim.x)) break;
         }
     }
+#else
+    P.S = ET_MLP_SPLIT;  // a fixed split (tuning builds only)
+#endif
     // K split of the gate/up tiles: with one row tile, F/128 tiles can leave
     // CTAs idle; the smallest split that gives the grid >= 2.5 tasks a CTA (K
     // chunks of >= 8 k-blocks, partial rows within gu_cap), else none
@@ -176,18 +233,25 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         const int fchunk = p.F / P.S;
         return GemmTask{&tm_wd, nullptr, &tm_h, p.b_wide ? &tm_h64 : nullptr, t.ht * kTileM,
                         t.mt * kWideNMax, t.s * (fchunk / kBlockK), fchunk / kBlockK, t.n,
-                        &p.ev_h[t.mt * kSplitMax + t.s], P.FT / P.S, kWhereH};
+                        &p.ev_h[t.mt * kMlpSplitMax + t.s], P.FT / P.S, kWhereH};
     };
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
-            ProdState ps;
-            for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
-                const MlpTile t = mlp_tile(P, task);
-                if (t.kind == 0 || t.kind == 3) continue;
-                if (!produce_task(gemm_of(t), ring, ctl, ps, wc, pol_w, pol_b)) break;
-            }
+            int task = blockIdx.x;
+            auto next = [&](GemmTask& g) {  // this CTA's next GEMM task
+                for (; task < P.total; task += gridDim.x) {
+                    const MlpTile t = mlp_tile(P, task);
+                    if (t.kind == 1 || t.kind == 2) {
+                        g = gemm_of(t);
+                        task += gridDim.x;
+                        return true;
+                    }
+                }
+                return false;
+            };
+            produce_static(next, ring, ctl, wc, pol_w, pol_b);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -196,7 +260,11 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
                 const MlpTile t = mlp_tile(P, task);
                 if (t.kind == 0 || t.kind == 3) continue;
-                if (!mma_task(gemm_of(t), ring, ctl, ms, tmem, wc)) break;
+                auto ftr = [&](int u, uint64_t tp, uint64_t tl) {
+                    trace_put(p.trace, p.trace_cap, t.kind == 1 ? kTaskGateUp : kTaskDown, 5, task,
+                              u, tp, tl);
+                };
+                if (!mma_task(gemm_of(t), ring, ctl, ms, tmem, wc, ftr)) break;
             }
         }
         __syncwarp();
@@ -205,10 +273,15 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         const int wtid = threadIdx.x - kEpiWarp0 * 32;
         const int H = p.H, F = p.F;
         EpiState es;
-        for (int task = blockIdx.x; task < P.total; task += gridDim.x) {
+        for (int task = blockIdx.x + (early_norm ? gridDim.x : 0); task < P.total;
+             task += gridDim.x) {
             const MlpTile t = mlp_tile(P, task);
+            const uint64_t tw = p.trace ? globaltimer_ns() : 0;
+            const int ttype = t.kind == 0 ? kTaskNorm : t.kind == 1 ? kTaskGateUp
+                            : t.kind == 2 ? kTaskDown : kTaskReduce;
+            TraceOnExit trace_task{p.trace, p.trace_cap, ttype, task, tw, wtid == 0};
             if (t.kind == 0) {
-                norm_rows(p, P.B, t.i);
+                norm_row(p, t.i, ctl);
                 fence_proxy_async_global();
                 worker_sync();
                 if (wtid == 0) {
@@ -225,13 +298,14 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                         ev_wait_geq(wc, p.ev_y + mt * P.HT + t.ht, P.S, kWhereY) ? 1 : 0;
                 worker_sync();
                 if (!ctl->flag) break;
-                reduce_slice(p.partial, static_cast<size_t>(p.B_max) * H, H, P.S, r0, r1,
-                             t.ht * kTileM, p.out, H);
+                reduce_slice4(p.partial, static_cast<size_t>(p.B_max) * H, H, P.S, r0, r1,
+                              t.ht * kTileM, p.out, H);
                 continue;
             }
             const bool two = t.kind == 1;
             uint32_t acc, acc1;
             if (!epi_acquire(ctl, es, two, t.n, tmem, wc, acc, acc1)) break;
+            if (wtid == 0) trace_put(p.trace, p.trace_cap, ttype, 6, task, 0, tw, globaltimer_ns());
             const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
             const uint32_t lane_base = acc + lane_off;
             const size_t m0 = static_cast<size_t>(t.mt) * kWideNMax;
@@ -297,7 +371,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 if (wtid == 0) {
                     const bool skip = p.fault_mode == 1 && t.mt * P.FT + t.ft == p.fault_arg;
                     __threadfence();
-                    if (!skip) red_release_add(&p.ev_h[t.mt * kSplitMax + t.ft / (P.FT / P.S)], 1);
+                    if (!skip) red_release_add(&p.ev_h[t.mt * kMlpSplitMax + t.ft / (P.FT / P.S)], 1);
                 }
                 continue;
             }
@@ -328,10 +402,12 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
     }
 
+    const uint64_t t_exit = globaltimer_ns();
     const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
     cta_teardown(ctl, aborted_run);
     __syncthreads();
     if (threadIdx.x == 0) {
+        trace_put(p.trace, p.trace_cap, 0, 3, 0, 0, t_exit, globaltimer_ns());
         __threadfence();
         ctl->flag = (atomicAdd(&p.hdr->exit_count, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
     }
@@ -340,7 +416,7 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         __threadfence();
         const bool ab = ld_relaxed(&p.hdr->abort) != 0;
         const int mt_clear = ab ? p.mt_max : P.MT;
-        for (int j = threadIdx.x; j < mt_clear * kSplitMax; j += kThreads) p.ev_h[j] = 0;
+        for (int j = threadIdx.x; j < mt_clear * kMlpSplitMax; j += kThreads) p.ev_h[j] = 0;
         const int y_clear = ab ? p.mt_max : (P.S > 1 ? P.MT : 0);
         for (int j = threadIdx.x; j < y_clear * P.HT; j += kThreads) p.ev_y[j] = 0;
         if (ab)  // the K-split counters reset themselves unless the launch aborted

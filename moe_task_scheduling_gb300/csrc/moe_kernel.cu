@@ -16,7 +16,9 @@
 //                          splits and the down-tile width, which it publishes
 //                          -- the queue below is implicit, each producer
 //                          decodes the index it claims -- and, with a single
-//                          router tile, it then permutes inline:
+//                          router tile, it then writes the permutation indices
+//                          (no row moves: that batch's gate/up tiles read the
+//                          tile's token rows in place):
 //   queue:      PERMUTE r,q stable scatter of part q of router tile r's rows;
 //                          releases ev_perm
 //               GATEUP g,f SwiGLU tile of expert row-tile g, F-tile f (waits
@@ -44,10 +46,13 @@ namespace et {
 
 // One layer's tensor maps: its weights and its staging buffers (gate, up,
 // down; permuted x and h in 16- and 64-row boxes; router weight; the fused
-// block's shared expert, x_hat and shared h).
+// block's shared expert, x_hat and shared h; the rows the router reads -- x,
+// or x_hat in a fused block -- in 16-row boxes, the gate/up activations of a
+// batch of one router tile).
 struct MoeLayerMaps {
-    CUtensorMap wg, wu, wd, xp, h, wr, xp64, h64, sg, su, sd, xn, hs;
+    CUtensorMap wg, wu, wd, xp, h, wr, xp64, h64, sg, su, sd, xn, hs, xr;
 };
+constexpr int kMapsPerLayer = 14;
 
 // The kernel parameter: nl <= kN chained layers; layer l + 1 reads layer l's
 // output.  A single layer launches with kN = 1: a 2 KB parameter block instead
@@ -98,17 +103,12 @@ constexpr int kPlanOff = kSelOff + 512;          // MoePlan [kMaxLayers], set on
 
 // Optional per-task record (see et_opts.trace): {type | role << 8, a, b, cta,
 // t_begin, t_end}.  role 0 = producer (pop .. loads issued), 1 = workers
-// (task received .. done), 2 = CTA (start .. set-up done), 3 = CTA exit.
+// (task received .. done), 2 = CTA (start .. set-up done), 3 = CTA exit,
+// 5 = MMA issuer, one per fill (posted .. its bytes landed; b = fill index),
+// 6 = workers (GEMM task received .. its accumulator ready).
 __device__ __forceinline__ void trace_rec(const MoeArgs& p, int type, int role, int a, int b,
                                           uint64_t t0, uint64_t t1) {
-    if (!p.trace) return;
-    const unsigned long long i = atomicAdd(reinterpret_cast<unsigned long long*>(p.trace), 1ull);
-    if (i >= static_cast<unsigned long long>(p.trace_cap)) return;
-    int4* r = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(p.trace) + 32 + i * 32);
-    r[0] = make_int4(type | (role << 8), a, b, static_cast<int>(blockIdx.x));
-    uint64_t* t = reinterpret_cast<uint64_t*>(r + 1);
-    t[0] = t0;
-    t[1] = t1;
+    trace_put(p.trace, p.trace_cap, type, role, a, b, t0, t1);
 }
 
 // Sub-phase marks of the front end (worker thread 0, role 4): type 16 + id
@@ -194,14 +194,15 @@ __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16*
             for (int b = 0; b < EBW; ++b) acc[a][b] = 0.0f;
         const bf16* xr = xb + static_cast<size_t>(tb * TB) * H;
         const bf16* wj = wb + static_cast<size_t>((o + j0) >> 3) * blk + ((o + j0) & 7);
-        // A plain loop, unrolled so the compiler keeps several steps' loads in
-        // flight (each lane's sum is one dependent chain of H/32 fmas, so a
-        // narrow job is latency-bound: unrolling 8 steps instead of 2 took a
-        // 1-token job from 7.1K to 4.5K SM cycles on GB300; the 4x8 job, with
-        // many jobs a CTA on large batches, keeps 2).  Pairs of experts go
-        // through one packed fma.rn.f32x2 (two independent IEEE fmas: the same
-        // sums, half the instructions).
-#pragma unroll(TB * EBW >= 32 ? 2 : 8)
+        // A plain loop unrolled twice.  Each lane's sum is one dependent chain
+        // of H/32 fmas; unrolling 8 steps took a warm 1-token job from 7.1K to
+        // 4.5K SM cycles in isolation, but the launch runs this code once, cold
+        // after the flush, where the longer code costs more than it saves
+        // (measured over the sweeps: unroll 2 against 8 for the narrow jobs,
+        // +0.3 % Mixtral-shaped, +0.9 % fine-grained; unroll 1 -1 % and -3 %).
+        // Pairs of experts go through one packed fma.rn.f32x2 (two independent
+        // IEEE fmas: the same sums, half the instructions).
+#pragma unroll 2
         for (int h = lane; h < H; h += 32) {  // h ascending per lane
             float wv[EBW];
             load_w<EBW>(wj + static_cast<size_t>(h) * rs, wv);
@@ -661,7 +662,12 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
             p.idx[static_cast<size_t>(t) * k + lane] = myE;
             p.gw[static_cast<size_t>(t) * k + lane] = ex / z;
             sel_s[tt * k + lane] = myE;
-            atomicAdd(&hs[myE], 1);
+            // one router tile: the expert's tokens as a mask (bit tt; its count is
+            // the popcount, as a token picks an expert at most once); else counts
+            if (P.R == 1)
+                atomicOr(&hs[myE], 1 << tt);
+            else
+                atomicAdd(&hs[myE], 1);
         }
     }
     tm = phase_mark(p, 11, tm);
@@ -687,19 +693,15 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
 
 // ------------------------------------------------------------------ SCAN
 
-__device__ __forceinline__ bool permute_rows(const MoeArgs& p, const MoePlan& P, int r, int i0,
-                                             int i1, uint8_t* smem, const Ring& ring, Ctl* ctl,
-                                             const WaitCtx& wc, uint32_t& sphase, uint32_t& seq,
-                                             const int* ie_src, const int* base_src, bool x_staged);
-
 // Counts, offsets, expert row tiles, split choice, and the task queue, run by
 // the last router tile to finish (every tile's histogram is visible through
 // the acquire-release count).  The targets the later waits use (permute
 // parts; F-tiles per chunk; the total number of output tiles) are all derived
 // here, on the device, from the routing of this very call.  With one router
-// tile the counts are this CTA's own histogram (smem), the permute is done
-// here from the staged x tile and the top-k picks in smem; otherwise the
-// per-tile histograms are staged in the ring and scanned per expert there.
+// tile the counts are this CTA's own histogram (smem) and the permutation
+// indices follow from the top-k picks in smem (no row is copied: the gate/up
+// tiles read the token rows in place); otherwise the per-tile histograms are
+// staged in the ring and scanned per expert there.
 __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, uint8_t* smem,
                                           const Ring& ring, Ctl* ctl, const WaitCtx& wc,
                                           uint32_t& sphase, uint32_t& seq) {
@@ -711,11 +713,12 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     int* off_s = cnt_s + 256;                   // [257]
     int* n_s = off_s + 264;                     // [256]
     int* mtb_s = n_s + 256;                     // [257]
+    uint32_t* tok_s = reinterpret_cast<uint32_t*>(mtb_s + 264);  // [256]: R == 1, tokens per expert
     const int RE = R * E;
     const bool staged = R > 1 && static_cast<size_t>(RE) * 4 <= ring.bytes;
     int* hs = reinterpret_cast<int*>(ring.base);
-    if (R == 1) {
-        for (int e = wtid_(); e < E; e += kWorkers) cnt_s[e] = hs1[e];
+    if (R == 1) {  // the router tile's token masks
+        for (int e = wtid_(); e < E; e += kWorkers) cnt_s[e] = __popc(hs1[e]);
     } else if (staged) {
         const int n4 = RE / 4;
         const int4* src = reinterpret_cast<const int4*>(p.hist);
@@ -810,25 +813,33 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         // two at most: measured on the Mixtral shape at T = 256, wide tiles in
         // 2 F-chunks take 494 us against 528 us for 128-column tiles in 4 and
         // 500 us for wide ones in 4 (their partials are twice the bytes).
+        // Small tiles that already fill half the grid are not split: a split
+        // adds a reduction chain (partials stored, counted, summed by the last
+        // arriver, ~3 us) that a tile of <= 1 MB does not win back (measured
+        // on the fine-grained shape: 85 -> 80 us at T = 1, 119 -> 111 us at
+        // T = 8, without the splits of the down and gate/up tiles).
+        const int G = p.num_ctas;
         int S = 1;
         const int down = total_mt * (wide ? HT / 2 : HT);
-        if (T * k <= p.split_rows_cap && total_mt > 0 && down < 3 * p.num_ctas) {
+        const bool down_small = p.F * (wide ? 512 : 256) <= (1 << 20) && 2 * down >= G;
+        if (T * k <= p.split_rows_cap && total_mt > 0 && down < 3 * G && !down_small) {
             int best = 1;
             for (int d = 2; d <= (wide ? 2 : kSplitMax); ++d) {
-                if (FT % d) continue;
+                if (!((p.split_mask >> d) & 1)) continue;
                 const int kbc = p.F / kBlockK / d;
-                if (kbc < 4 || (down * best >= 3 * p.num_ctas && kbc < 8)) break;
+                if (down * best >= 3 * G && kbc < 8) break;
                 best = d;
-                if (down * d >= 4 * p.num_ctas) break;
+                if (down * d >= 4 * G) break;
             }
             S = best;
         }
         // K chunks of a gate/up tile: a small batch has few (weight-streaming)
         // tiles, so they are cut along K until the grid has a few per CTA
         int KC = 1;
-        const int nkb = p.H / kBlockK;
-        while (KC < kGuSplitMax && total_mt * FT * KC < 3 * p.num_ctas && nkb % (2 * KC) == 0 &&
-               nkb / (2 * KC) >= 8 && T * k * 2 * KC <= p.gu_cap)
+        const int gu = total_mt * FT;
+        const bool gu_small = p.H * 512 <= (1 << 20) && 2 * gu >= G;
+        while (!gu_small && KC < kGuSplitMax && gu * KC < 3 * G &&
+               ((p.kc_mask >> (2 * KC)) & 1) && T * k * 2 * KC <= p.gu_cap)
             KC *= 2;
         ctl->scratch[0] = total_mt;
         ctl->scratch[1] = S;
@@ -839,14 +850,23 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     tm = phase_mark(p, 6, tm);
     const int total_mt = ctl->scratch[0], S = ctl->scratch[1], KC = ctl->scratch[2];
     const int wide = ctl->scratch[3];
+    // One router tile (R == 1): the gate/up tiles read the tile's token rows
+    // straight from the layer's input -- no row is copied -- and keep, in the
+    // epilogue, the columns of the tokens routed to their expert; the row
+    // tile's entry carries those tokens (bit t, in the upper half of its N
+    // word; an expert has one row tile, as T <= 16).
+    const int* sel1 = reinterpret_cast<const int*>(smem + kSelOff);
     for (int e = wtid_(); e < E; e += kWorkers) {
         p.cnt[e] = cnt_s[e];
         p.off[e] = off_s[e];
         if (e == E - 1) p.off[E] = off_s[E];
         const int n = n_s[e];
+        const uint32_t tok = R == 1 ? static_cast<uint32_t>(hs1[e]) : 0u;
+        tok_s[e] = tok;
         p.e_tile[e] = make_int4(mtb_s[e], n, off_s[e], 0);
         for (int g = mtb_s[e], mt = 0; g < mtb_s[e + 1]; ++g, ++mt)
-            p.g_info[g] = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n), n);
+            p.g_info[g] = make_int4(e, off_s[e] + mt * n, min(n, cnt_s[e] - mt * n),
+                                    static_cast<int>(static_cast<uint32_t>(n) | (tok << 16)));
     }
     if (R == 1) {
         for (int e = wtid_(); e < E; e += kWorkers) p.base[e] = off_s[e];
@@ -877,11 +897,16 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         __threadfence();
         st_release(&p.hdr->q_ready, 1);
     }
-    if (R == 1) {  // permute inline (x rows already staged if the router staged them), after
-                   // the publish: the gate/up tiles wait on its ev_perm release
-        const int* sel = reinterpret_cast<const int*>(smem + kSelOff);
-        if (!permute_rows(p, P, 0, 0, T * k, smem, ring, ctl, wc, sphase, seq, sel, off_s, P.stage))
-            return false;
+    if (R == 1) {  // after the publish: the permutation indices only (no row moves); the
+                   // combine waits on their ev_perm release
+        for (int i = wtid_(); i < T * k; i += kWorkers) {
+            const int e = sel1[i], t = i / k;
+            const int pp = off_s[e] + __popc(tok_s[e] & ((1u << t) - 1u));
+            p.perm[pp] = i;
+            p.pos[i] = pp;
+            p.gpos[i] = mtb_s[e];
+        }
+        worker_sync();
         if (wtid_() == 0) {
             __threadfence();
             red_release_add(&p.hdr->ev_perm, 1);
@@ -896,21 +921,18 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
 // Stable dispatch of router tile r: row (t, j) goes to off[e] + (rank of t
 // among this call's tokens routed to e), and its x row is copied there.  The
 // part's token rows come into the ring by bulk copy (the first batch is
-// issued before the ranks are computed, so it flies meanwhile) unless the
-// router already staged the whole tile there (x_staged); each routed row then
-// leaves with one bulk shared -> global copy.  ie_src / base_src: the tile's
-// top-k picks and first rows per expert when already in smem (else global).
+// issued before the ranks are computed, so it flies meanwhile); each routed
+// row then leaves with one bulk shared -> global copy.
 __device__ __forceinline__ bool permute_rows(const MoeArgs& p, const MoePlan& P, int r, int i0,
                                              int i1, uint8_t* smem, const Ring& ring, Ctl* ctl,
-                                             const WaitCtx& wc, uint32_t& sphase, uint32_t& seq,
-                                             const int* ie_src, const int* base_src, bool x_staged) {
+                                             const WaitCtx& wc, uint32_t& sphase, uint32_t& seq) {
     const int k = p.k, E = p.E, H = p.H;
     const int t0 = r * kRouterTile, nt = min(kRouterTile, P.T - t0), nent = nt * k;
     int* ie = reinterpret_cast<int*>(smem + kPermOff);  // [128]
     int* slot = ie + 128;                               // [128]
     const int tl0 = i0 / k, ntok = i1 > i0 ? (i1 - 1) / k - tl0 + 1 : 0;
     const uint32_t rowb = static_cast<uint32_t>(H) * 2u;
-    const int per = x_staged ? kRouterTile : static_cast<int>(ring.bytes / rowb);  // rows a batch
+    const int per = static_cast<int>(ring.bytes / rowb);  // rows a batch
     auto issue = [&](int c0) {  // worker thread 0: token rows tl0 + c0 .. of the part
         const int nc = min(per, ntok - c0);
         mbar_arrive_expect_tx(&ctl->sbar, nc * rowb);
@@ -918,42 +940,30 @@ __device__ __forceinline__ bool permute_rows(const MoeArgs& p, const MoePlan& P,
                  nc * rowb, &ctl->sbar);
     };
     if ((p.gamma || p.ev_in) && wtid_() == 0) fence_proxy_async_global();  // generic stores
-    if (!x_staged && ntok > 0 && wtid_() == 0) issue(0);
-    const int* iv = ie_src;
-    if (!iv) {
-        for (int i = wtid_(); i < nent; i += kWorkers)
-            ie[i] = __ldcg(p.idx + static_cast<size_t>(t0) * k + i);
-        worker_sync();
-        iv = ie;
-    }
+    if (ntok > 0 && wtid_() == 0) issue(0);
+    for (int i = wtid_(); i < nent; i += kWorkers)
+        ie[i] = __ldcg(p.idx + static_cast<size_t>(t0) * k + i);
+    worker_sync();
     for (int i = i0 + wtid_(); i < i1; i += kWorkers) {
-        const int e = iv[i], tl = i / k;
+        const int e = ie[i], tl = i / k;
         int rank = 0;  // tokens before t in this tile routed to e (each at most once)
-        for (int i2 = 0; i2 < tl * k; ++i2) rank += (iv[i2] == e);
-        const int pp = (base_src ? base_src[e] : __ldcg(p.base + static_cast<size_t>(r) * E + e)) + rank;
+        for (int i2 = 0; i2 < tl * k; ++i2) rank += (ie[i2] == e);
+        const int pp = __ldcg(p.base + static_cast<size_t>(r) * E + e) + rank;
         p.perm[pp] = t0 * k + i;
         p.pos[static_cast<size_t>(t0) * k + i] = pp;
         const int4 et = __ldcg(p.e_tile + e);  // the row's tile: first tile + offset / N
         p.gpos[static_cast<size_t>(t0) * k + i] = et.x + (pp - et.z) / et.y;
         slot[i] = pp;
     }
-    if (x_staged) {  // the tile's rows are at ring.base + (token - t0) * rowb
+    for (int c0 = 0; c0 < ntok; c0 += per) {
+        if (c0 > 0 && wtid_() == 0) issue(c0);
+        if (!staging_wait(ctl, sphase, wc, seq)) return false;
+        const int ia = max(i0, (tl0 + c0) * k), ib = min(i1, (tl0 + c0 + per) * k);
+        for (int i = ia + wtid_(); i < ib; i += kWorkers)
+            bulk_s2g(p.xp + static_cast<size_t>(slot[i]) * H,
+                     ring.base + (i / k - tl0 - c0) * rowb, rowb);
+        bulk_commit_wait_all();  // rows written (and the batch read) before the next one
         worker_sync();
-        for (int i = i0 + wtid_(); i < i1; i += kWorkers)
-            bulk_s2g(p.xp + static_cast<size_t>(slot[i]) * H, ring.base + (i / k) * rowb, rowb);
-        bulk_commit_wait_all();
-        worker_sync();
-    } else {
-        for (int c0 = 0; c0 < ntok; c0 += per) {
-            if (c0 > 0 && wtid_() == 0) issue(c0);
-            if (!staging_wait(ctl, sphase, wc, seq)) return false;
-            const int ia = max(i0, (tl0 + c0) * k), ib = min(i1, (tl0 + c0 + per) * k);
-            for (int i = ia + wtid_(); i < ib; i += kWorkers)
-                bulk_s2g(p.xp + static_cast<size_t>(slot[i]) * H,
-                         ring.base + (i / k - tl0 - c0) * rowb, rowb);
-            bulk_commit_wait_all();  // rows written (and the batch read) before the next one
-            worker_sync();
-        }
     }
     if (ntok > 0) fence_proxy_async_global();  // the rows are read back by TMA
     worker_sync();
@@ -967,7 +977,7 @@ __device__ __forceinline__ bool permute_task(const MoeArgs& p, const MoePlan& P,
     const int t0 = r * kRouterTile, nent = min(kRouterTile, P.T - t0) * p.k;
     wr_cache_drop(ctl);
     if (!permute_rows(p, P, r, part * nent / P.Q, (part + 1) * nent / P.Q, smem, ring, ctl, wc,
-                      sphase, seq, nullptr, nullptr, false))
+                      sphase, seq))
         return false;
     if (wtid_() == 0) {
         __threadfence();
@@ -1136,7 +1146,8 @@ __device__ __forceinline__ TaskMsg queue_task(const MoeArgs& p, const MoePlan& P
         m.b = (c % S) * (FT / S) + r / KC;
         m.c = r % KC;
         const int4 gi = __ldcg(p.g_info + g);
-        m.e = gi.x, m.row0 = gi.y, m.rows = gi.z, m.n = gi.w;
+        m.e = gi.x, m.row0 = gi.y, m.rows = gi.z, m.n = gi.w & 0xffff;
+        m.aux = static_cast<uint32_t>(gi.w) >> 16;
         return m;
     }
     q -= NCH * u;
@@ -1159,7 +1170,7 @@ __device__ __forceinline__ TaskMsg queue_task(const MoeArgs& p, const MoePlan& P
         m.b = c % S;
         m.c = q % d;
         const int4 gi = __ldcg(p.g_info + g);
-        m.e = gi.x, m.row0 = gi.y, m.rows = gi.z, m.n = gi.w;
+        m.e = gi.x, m.row0 = gi.y, m.rows = gi.z, m.n = gi.w & 0xffff;
         return m;
     }
     m.type = kTaskCombine;
@@ -1195,10 +1206,13 @@ __device__ __forceinline__ TaskMsg static_task(const MoeArgs& p, const MoePlan& 
 
 // Producer thread: next task of this CTA (EXIT when every layer's tasks are
 // taken or the launch aborted).  `claim` is a task index taken ahead of time
-// (or -1); claims only grow, so the cursor only moves forward.
+// (or -1); claims only grow, so the cursor only moves forward.  With `nowait`
+// a claim that falls in a queue not yet published gives kTaskNone (the claim
+// stays the caller's) instead of waiting for the scan.
 template <bool kChain>
 __device__ __forceinline__ TaskMsg pop_task(const MoeLaunchOf<kChain>& Lc, const MoePlan* plans,
-                                            const WaitCtx& wc, int claim, QCursor& cur) {
+                                            const WaitCtx& wc, int claim, QCursor& cur,
+                                            bool nowait = false) {
     TaskMsg m{};
     m.type = kTaskExit;
     if (aborted(wc) || plans[0].R == 0) return m;  // T == 0: no task at all
@@ -1213,6 +1227,10 @@ __device__ __forceinline__ TaskMsg pop_task(const MoeLaunchOf<kChain>& Lc, const
             break;
         }
         if (cur.qt < 0) {
+            if (nowait && ld_acquire(&p.hdr->q_ready) < 1) {
+                m.type = kTaskNone;
+                return m;
+            }
             if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
             cur.qt = ld_relaxed(&p.hdr->q_total);
             cur.mt = ld_relaxed(&p.hdr->total_mt);
@@ -1294,6 +1312,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
         }
         if (type == kTaskGateUp) {
             const int nkb = p.H / kBlockK / KC;
+            if (P.R == 1) {  // the router tile's rows (x_hat in a block), all 16 columns
+                const int* dep = p.gamma ? &p.hdr->ev_norm : p.ev_in;
+                return GemmTask{&M.wg, &M.wu, &M.xr, nullptr, m.e * p.F + m.b * kTileM, 0,
+                                m.c * nkb, nkb, kRouterTile, dep, p.gamma ? 1 : P.T,
+                                p.gamma ? kWhereNorm : kWhereInput};
+            }
             return GemmTask{&M.wg, &M.wu, &M.xp, p.b_wide ? &M.xp64 : nullptr,
                             m.e * p.F + m.b * kTileM, m.row0, m.c * nkb, nkb, m.n,
                             &p.hdr->ev_perm, P.NPW, kWherePerm};
@@ -1306,33 +1330,86 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
     };
 
     if (warp == 0) {
-        if (lane == 0) {  // producer: pop, hand over, load
+        if (lane == 0) {  // producer: pop, hand over, load (one GEMM task of lookahead)
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
             ProdState ps;
             QCursor cur;
-            int claim = -1;
-            for (int i = 0;; ++i) {
-                // a SIMT task still out on lease: take no further task before it
-                // is done, so SIMT work spreads over the CTAs that are free
-                if (!ring_lease_wait(ctl, ps, wc)) break;
-                const uint64_t tp = globaltimer_ns();
-                const TaskMsg m = pop_task<kChain>(Lc, plans, wc, claim, cur);
-                claim = -1;
-                const int slot = i % kTaskRing;
-                if (!mbar_wait(wc, &ctl->tq_empty[slot], ((i / kTaskRing) & 1) ^ 1, kWhereQueue))
-                    break;
+            int claim = -1, sent = 0;
+            Flight fc, fn;                     // the current task; the one looked ahead
+            bool has_next = false, end = false;  // end: EXIT handed during a lookahead
+            // hand a task to the MMA issuer and the workers (the slot is free)
+            auto hand = [&](const TaskMsg& m) {
+                const int slot = sent % kTaskRing;
                 ctl->tq[slot] = m;
                 mbar_arrive(&ctl->tq_full[slot]);
-                const int type = m.type & 0xff;
-                if (type == kTaskExit) break;
-                if (is_gemm(type)) {
+                ++sent;
+            };
+            auto slot_free = [&]() {
+                return mbar_try_wait(&ctl->tq_empty[sent % kTaskRing],
+                                     ((sent / kTaskRing) & 1) ^ 1);
+            };
+            // while the current task waits on its dependency: take the next
+            // task if it can be decoded and handed over without waiting, and
+            // post the weights of a GEMM task into free ring space.  A SIMT task
+            // (it leases the whole ring) or EXIT ends the lookahead.
+            auto idle = [&]() {
+                if (!has_next) {
+                    if (end || *reinterpret_cast<volatile int32_t*>(&ctl->ring_ret) <
+                                   static_cast<int32_t>(ps.leases))
+                        return;
+                    if (!slot_free()) return;
+                    const uint64_t tp = globaltimer_ns();
+                    const TaskMsg m = pop_task<kChain>(Lc, plans, wc, claim, cur, true);
+                    const int type = m.type & 0xff;
+                    if (type == kTaskNone) return;
+                    claim = -1;
+                    hand(m);
+                    if (type == kTaskExit) {
+                        end = true;
+                        return;
+                    }
+                    if (!is_gemm(type)) {
+                        ++ps.leases;
+                        trace_rec(p0, type, 0, m.a, m.b, tp, globaltimer_ns());
+                        return;
+                    }
+                    claim = atomicAdd(&p0.hdr->q_head, 1);
+                    flight_begin(fn, gemm_of(m), type, m.a, m.b, tp);
+                    has_next = true;
+                }
+                flight_post_nowait(fn, ring, ctl, ps, pol_w, pol_b);
+            };
+            for (;;) {
+                if (has_next) {
+                    fc = fn;
+                    has_next = false;
+                } else {
+                    if (end) break;
+                    // a SIMT task still out on lease: take no further task before it
+                    // is done, so SIMT work spreads over the CTAs that are free
+                    if (!ring_lease_wait(ctl, ps, wc)) break;
+                    const uint64_t tp = globaltimer_ns();
+                    const TaskMsg m = pop_task<kChain>(Lc, plans, wc, claim, cur);
+                    claim = -1;
+                    if (!mbar_wait(wc, &ctl->tq_empty[sent % kTaskRing],
+                                   ((sent / kTaskRing) & 1) ^ 1, kWhereQueue))
+                        break;
+                    hand(m);
+                    const int type = m.type & 0xff;
+                    if (type == kTaskExit) break;
+                    if (!is_gemm(type)) {
+                        ++ps.leases;  // a SIMT task holds the ring until the workers return it
+                        trace_rec(p0, type, 0, m.a, m.b, tp, globaltimer_ns());
+                        continue;
+                    }
                     // claim the next task now: the atomic's latency hides behind the loads
                     claim = atomicAdd(&p0.hdr->q_head, 1);
-                    if (!produce_task(gemm_of(m), ring, ctl, ps, wc, pol_w, pol_b)) break;
-                } else {
-                    ++ps.leases;  // a SIMT task holds the ring until the workers return it
+                    flight_begin(fc, gemm_of(m), type, m.a, m.b, tp);
+                    flight_post_nowait(fc, ring, ctl, ps, pol_w, pol_b);
                 }
-                trace_rec(p0, type, 0, m.a, m.b, tp, globaltimer_ns());
+                if (!flight_wait(fc, ring, ctl, ps, wc, pol_w, pol_b, idle)) break;
+                if (!flight_finish(fc, ring, ctl, ps, wc, pol_w, pol_b)) break;
+                trace_rec(p0, fc.type, 0, fc.a, fc.b, fc.t_pop, globaltimer_ns());
             }
         }
         __syncwarp();
@@ -1346,8 +1423,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
                 mbar_arrive(&ctl->tq_empty[slot]);
                 const int type = m.type & 0xff;
                 if (type == kTaskExit) break;
-                if (is_gemm(type))
-                    if (!mma_task(gemm_of(m), ring, ctl, ms, tmem, wc)) break;
+                if (!is_gemm(type)) continue;
+                if (p0.trace) {  // role 5: one record per fill, posted .. landed
+                    auto ftr = [&](int u, uint64_t tp, uint64_t tl) {
+                        trace_rec(p0, type, 5, m.a, u, tp, tl);
+                    };
+                    if (!mma_task(gemm_of(m), ring, ctl, ms, tmem, wc, ftr)) break;
+                } else if (!mma_task(gemm_of(m), ring, ctl, ms, tmem, wc)) {
+                    break;
+                }
             }
         }
         __syncwarp();
@@ -1400,6 +1484,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
             wr_cache_drop(ctl);  // the tile's fills went through the ring
             uint32_t acc, acc1;
             if (!epi_acquire(ctl, es, two, m.n, tmem, wc, acc, acc1)) break;
+            if (p.trace && wtid == 0)
+                trace_rec(p, type, 6, m.a, m.b, trace_scope.t0, globaltimer_ns());
             const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
             const uint32_t lane_base = acc + lane_off;
             const int row0 = m.row0, rows = m.rows, n = m.n;
@@ -1475,6 +1561,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
                 const size_t tk = static_cast<size_t>(P.T) * p.k;
                 float* gpart = p.gu_part + (static_cast<size_t>(m.c) * tk) * F;
                 float* upart = gpart + static_cast<size_t>(p.gu_cap) * F;
+                // one router tile: column c is token c; a token routed to this
+                // expert goes to its permuted row (its rank among them)
+                const uint32_t tok = m.aux;
                 for (int c0 = half * 16; c0 < n; c0 += 32) {
                     float gv[16], uv[16];
                     tmem_ld16(lane_base + c0, gv);
@@ -1482,8 +1571,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        if (c0 + c >= rows) continue;
-                        const size_t r = static_cast<size_t>(row0 + c0 + c);
+                        int rr = c0 + c;
+                        if (tok) {
+                            if (!((tok >> rr) & 1u)) continue;
+                            rr = __popc(tok & ((1u << rr) - 1u));
+                        } else if (rr >= rows) {
+                            continue;
+                        }
+                        const size_t r = static_cast<size_t>(row0 + rr);
                         if (KC == 1) {
                             p.h[r * F + f] = __float2bfloat16_rn(silu_mul(gv[c], uv[c]));
                         } else {
@@ -1577,17 +1672,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_megakernel(
                 if (wtid == 0) {
                     __threadfence();
                     const int target = ld_relaxed(&p.hdr->total_mt) * HT;
-                    ctl->flag =
-                        (atom_acq_rel_add(&p.hdr->ev_ydone, ntiles) == target - ntiles) ? 1 : 0;
+                    bool last = atom_acq_rel_add(&p.hdr->ev_ydone, ntiles) == target - ntiles;
+                    // it also needs the permutation indices (a single router tile writes
+                    // them after its gate/up tiles may have started) and the shared
+                    // expert's output tiles
+                    if (last)
+                        last = ev_wait_geq(wc, &p.hdr->ev_perm, P.NPW, kWherePerm) &&
+                               (P.MTS == 0 || ev_wait_geq(wc, &p.hdr->ev_sdone, P.MTS * HT, kWhereY));
+                    ctl->flag = last ? 1 : 0;
                 }
                 worker_sync();
-                if (ctl->flag && P.MTS > 0) {  // the shared expert's tiles too
-                    if (wtid == 0)
-                        ctl->flag =
-                            ev_wait_geq(wc, &p.hdr->ev_sdone, P.MTS * HT, kWhereY) ? 1 : 0;
-                    worker_sync();
-                }
-                if (ctl->flag) {
+                const bool go = ctl->flag != 0;
+                worker_sync();  // the flag is read before any later task writes it
+                if (go) {
                     combine_inline(p, P);
                     release_output(p, 0, P.T);
                 }
@@ -1660,7 +1757,7 @@ int moe_ring_bytes() { return ring_bytes_for(kMoeScratch); }
 // Host-side launch (called by the C ABI after validation).
 cudaError_t launch_moe(const MoeArgs* a, const CUtensorMap* maps, int nl, int grid, int smem,
                        cudaStream_t stream) {
-    static_assert(sizeof(MoeLayerMaps) == 13 * sizeof(CUtensorMap), "13 maps a layer");
+    static_assert(sizeof(MoeLayerMaps) == kMapsPerLayer * sizeof(CUtensorMap), "maps of a layer");
     if (nl < 1 || nl > kMaxLayers) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -1683,7 +1780,7 @@ cudaError_t launch_moe(const MoeArgs* a, const CUtensorMap* maps, int nl, int gr
     MoeLaunchOf<true> L;
     memset(&L, 0, sizeof(L));
     for (int l = 0; l < nl; ++l) {
-        memcpy(&L.m[l], maps + 13 * l, sizeof(MoeLayerMaps));
+        memcpy(&L.m[l], maps + kMapsPerLayer * l, sizeof(MoeLayerMaps));
         L.a[l] = a[l];
     }
     L.nl = nl;

@@ -6,9 +6,11 @@
 //   [0, G)        TILE (mt, nt, s): fp32 partial of a 256 x 128 output tile over
 //                 K chunk s (bf16 Y directly when split == 1); releases
 //                 ev[mt][nt]
-//   [G, G + R)    REDUCE (q, nt), split > 1 only: waits ev[tile] >= split, then
-//                 sums rows [32q, 32q + 32) of the tile's partials in chunk
-//                 order and stores bf16 Y.
+//   [G, G + R)    REDUCE (q, nt), split > 1 and M > 32 only: waits ev[tile] >=
+//                 split, then sums rows [32q, 32q + 32) of the tile's partials
+//                 in chunk order and stores bf16 Y.  With M <= 32 the TILE
+//                 task that completes ev[tile] sums it instead (same order),
+//                 so no task polls for it.
 // Every wait is on a lower task index, and the launch is cooperative (every
 // CTA resident), so the schedule cannot deadlock; the reduction of one tile is
 // spread over many CTAs instead of falling on the last arriver.  The last CTA
@@ -41,9 +43,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ CUtensorMap tm_x64, const __grid_constant__ SplitKArgs p) {
     extern __shared__ uint8_t smem_raw[];
+    const uint64_t t_start = globaltimer_ns();
     Ring ring;
     uint8_t* scratch;
     Ctl* ctl = cta_setup(smem_raw, 0, ring, &scratch);
+    if (threadIdx.x == 0) trace_put(p.trace, p.trace_cap, 0, 2, 0, 0, t_start, globaltimer_ns());
     const WaitCtx wc{p.hdr, p.timeout_ns};
     const uint32_t tmem = ctl->tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -59,7 +63,11 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const int kbs = p.K / kBlockK / split;
     const int total = MT * NT * split;
     constexpr int kRedRows = 32;  // rows per reduce task
-    const int n_red = split > 1 ? ceil_div(M, kRedRows) * NT : 0;
+    // a tile of at most 32 rows is summed by the split that completes its
+    // counter (no reduce task polls for it); taller tiles spread their rows
+    // over reduce tasks
+    const bool last_arriver = split > 1 && M <= kRedRows;
+    const int n_red = (split > 1 && !last_arriver) ? ceil_div(M, kRedRows) * NT : 0;
 
     auto gemm_of = [&](const SplitKTile& t) {
         return GemmTask{&tm_w, nullptr, &tm_x, p.b_wide ? &tm_x64 : nullptr, t.nt * kTileM,
@@ -69,19 +77,26 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
-            ProdState ps;
-            for (int task = blockIdx.x; task < total; task += gridDim.x)
-                if (!produce_task(gemm_of(splitk_tile(task, split, NT, M)), ring, ctl, ps, wc, pol_w,
-                                  pol_b))
-                    break;
+            int task = blockIdx.x;
+            auto next = [&](GemmTask& g) {  // this CTA's next tile task
+                if (task >= total) return false;
+                g = gemm_of(splitk_tile(task, split, NT, M));
+                task += gridDim.x;
+                return true;
+            };
+            produce_static(next, ring, ctl, wc, pol_w, pol_b);
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             MmaState ms;
-            for (int task = blockIdx.x; task < total; task += gridDim.x)
-                if (!mma_task(gemm_of(splitk_tile(task, split, NT, M)), ring, ctl, ms, tmem, wc))
+            for (int task = blockIdx.x; task < total; task += gridDim.x) {
+                auto ftr = [&](int u, uint64_t tp, uint64_t tl) {
+                    trace_put(p.trace, p.trace_cap, kTaskSplitK, 5, task, u, tp, tl);
+                };
+                if (!mma_task(gemm_of(splitk_tile(task, split, NT, M)), ring, ctl, ms, tmem, wc, ftr))
                     break;
+            }
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
@@ -89,6 +104,7 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int wtid = threadIdx.x - kEpiWarp0 * 32;
         EpiState es;
         for (int task = blockIdx.x; task < total + n_red; task += gridDim.x) {
+            const uint64_t tw = p.trace ? globaltimer_ns() : 0;
             if (task >= total) {  // REDUCE: row slice qs of tile column nt
                 const int r = task - total, nt = r % NT, qs = r / NT;
                 const int r0 = qs * kRedRows, r1 = min(M, r0 + kRedRows), mt = r0 / kWideNMax;
@@ -98,11 +114,13 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 if (!ctl->flag) break;
                 reduce_slice(p.partial, static_cast<size_t>(p.M_max) * N, N, split, r0, r1,
                              nt * kTileM, p.Y, N);
+                if (wtid == 0) trace_put(p.trace, p.trace_cap, kTaskReduce, 1, task, 0, tw, globaltimer_ns());
                 continue;
             }
             const SplitKTile t = splitk_tile(task, split, NT, M);
             uint32_t acc, acc1;
             if (!epi_acquire(ctl, es, false, t.n, tmem, wc, acc, acc1)) break;
+            if (wtid == 0) trace_put(p.trace, p.trace_cap, kTaskSplitK, 6, task, 0, tw, globaltimer_ns());
             const int col = t.nt * kTileM + q * 32 + lane;
             const uint32_t lane_base = acc + (static_cast<uint32_t>(q * 32) << 16);
             const size_t m0 = static_cast<size_t>(t.mt) * kWideNMax;
@@ -121,20 +139,39 @@ splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 }
             }
             epi_release(ctl, es, false, t.n);
-            if (split > 1) {  // the partial is stored: count it on the tile's event
+            if (last_arriver) {  // the split that completes the tile sums its partials
+                int* ev = p.ev + t.mt * NT + t.nt;
+                worker_sync();
+                if (wtid == 0) {
+                    __threadfence();
+                    ctl->flag = (atom_acq_rel_add(ev, 1) == split - 1) ? 1 : 0;
+                }
+                worker_sync();
+                const bool last = ctl->flag != 0;
+                worker_sync();  // the flag is read before any later task writes it
+                if (last) {
+                    if (wtid == 0) *ev = 0;  // every split arrived: reset for the next call
+                    reduce_slice4(p.partial, static_cast<size_t>(p.M_max) * N, N, split,
+                                  static_cast<int>(m0), static_cast<int>(m0) + t.rows,
+                                  t.nt * kTileM, p.Y, N);
+                }
+            } else if (split > 1) {  // the partial is stored: count it on the tile's event
                 worker_sync();
                 if (wtid == 0) {
                     __threadfence();
                     red_release_add(p.ev + t.mt * NT + t.nt, 1);
                 }
             }
+            if (wtid == 0) trace_put(p.trace, p.trace_cap, kTaskSplitK, 1, task, 0, tw, globaltimer_ns());
         }
     }
 
+    const uint64_t t_exit = globaltimer_ns();
     const bool aborted_run = ld_relaxed(&p.hdr->abort) != 0;
     cta_teardown(ctl, aborted_run);
     __syncthreads();
     if (threadIdx.x == 0) {
+        trace_put(p.trace, p.trace_cap, 0, 3, 0, 0, t_exit, globaltimer_ns());
         __threadfence();
         if (atomicAdd(&p.hdr->exit_count, 1) == static_cast<int>(gridDim.x) - 1) {
             // the tile counters go back to zero (all of them after an abort)

@@ -126,16 +126,16 @@ def alloc_trace(records: int, device="cuda"):
 
 
 def read_trace(buf):
-    """Decode a trace buffer: list of (type, role, a, b, cta, t_begin_ns, t_end_ns)."""
+    """Decode a trace buffer: list of (type, role, a, b, cta, t_begin_ns, t_end_ns).
+    The records sit in per-CTA shares of the buffer; unused slots are zero."""
     import numpy as np
     raw = buf.cpu().numpy()
-    n = int(raw[:8].view(np.uint64)[0])
     cap = (raw.size - 32) // 32
-    rec = raw[32:32 + 32 * min(n, cap)].reshape(-1, 32)
+    rec = raw[32:32 + 32 * cap].reshape(-1, 32)
     ints = rec[:, :16].copy().view(np.int32).reshape(-1, 4)
     ts = rec[:, 16:].copy().view(np.uint64).reshape(-1, 2)
     return [(int(i[0]) & 0xff, int(i[0]) >> 8, int(i[1]), int(i[2]), int(i[3]), int(t[0]), int(t[1]))
-            for i, t in zip(ints, ts)]
+            for i, t in zip(ints, ts) if t[1] != 0]
 
 
 def _check(rc):
@@ -252,13 +252,13 @@ def et_moe_chain(layers, x, *, H, F, E, k, T=None, d_T=None, T_max=None, workspa
 
 
 def et_splitk_gemm(X, Wt, Y, *, split, M=None, d_M=None, M_max=None, workspace, stream=None,
-                   timeout_us=0, check=True):
+                   timeout_us=0, trace=None, check=True):
     K = X.shape[1]
     N = Wt.shape[0]
     M_max = M_max if M_max is not None else X.shape[0]
     M = M if M is not None else X.shape[0]
     rc = load().et_splitk_gemm(_ptr(X), _ptr(Wt), _ptr(Y), M, _ptr(d_M), M_max, N, K, split,
-                               _ptr(workspace), workspace.numel(), _opts(timeout_us),
+                               _ptr(workspace), workspace.numel(), _opts(timeout_us, trace=trace),
                                _stream(stream))
     if check:
         _check(rc)
@@ -301,14 +301,15 @@ def et_splitk_noalloc_status(stream=None):
 
 
 def et_mlp_chain(x, gamma, eps, w_gate, w_up, w_down, out, *, B=None, d_B=None, B_max=None,
-                 workspace, stream=None, timeout_us=0, fault_mode=0, fault_arg=0, check=True):
+                 workspace, stream=None, timeout_us=0, fault_mode=0, fault_arg=0, trace=None,
+                 check=True):
     H = x.shape[1]
     F = w_gate.shape[0]
     B_max = B_max if B_max is not None else x.shape[0]
     B = B if B is not None else x.shape[0]
     rc = load().et_mlp_chain(_ptr(x), _ptr(gamma), float(eps), _ptr(w_gate), _ptr(w_up),
                              _ptr(w_down), _ptr(out), B, _ptr(d_B), B_max, H, F, _ptr(workspace),
-                             workspace.numel(), _opts(timeout_us, fault_mode, fault_arg),
+                             workspace.numel(), _opts(timeout_us, fault_mode, fault_arg, trace),
                              _stream(stream))
     if check:
         _check(rc)

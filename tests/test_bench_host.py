@@ -33,3 +33,35 @@ def test_profiled_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     f.write_text("source_hash: fedcba9876543210\ntraffic_bytes_per_launch: 2334009830\n")
     assert bench.profiled_traffic("mixtral") is None
     assert bench.profiled_traffic("fine") is None  # no summary at all
+
+
+def test_default_line_carries_the_secondary_sweeps(monkeypatch):
+    """The default run adds the other configurations' records (fine-grained
+    layer, fused Mixtral-shaped block, split-K GEMM, MLP chain, warm-up) to
+    its line; here each measurement is a fake that checks what it is given."""
+    import argparse
+
+    import torch
+
+    seen = []
+
+    def fake_moe(cfg, Fs, device, steps, warmup):
+        assert Fs is None or isinstance(Fs, int)
+        assert isinstance(device, torch.device)
+        seen.append((cfg.name, Fs, steps, warmup))
+        return {"value": 1.0}
+
+    def fake_dense(kind, device, steps, warmup):
+        assert kind in ("splitk", "mlp") and isinstance(device, torch.device)
+        seen.append((kind, steps, warmup))
+        return {"sweep": []}
+
+    monkeypatch.setattr(bench, "moe_sweep_record", fake_moe)
+    monkeypatch.setattr(bench, "dense_sweep_record", fake_dense)
+    monkeypatch.setattr(bench, "run_warmup", lambda args: {"value": 2.0})
+    args = argparse.Namespace(steps=7, warmup=3, no_warmup_record=False)
+    out = bench.secondary_sweeps(args, torch.device("cpu"))
+    assert set(out) == {"fine", "mixtral_block", "splitk", "mlp", "warmup"}
+    assert ("fine_skewed", None, 7, 3) in seen and ("mixtral", 0, 7, 3) in seen
+    assert ("splitk", 7, 3) in seen and ("mlp", 7, 3) in seen
+    assert out["warmup"] == {"value": 2.0}
