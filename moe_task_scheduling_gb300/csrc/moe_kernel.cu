@@ -99,6 +99,13 @@ constexpr int kSelOff = kHistOff + 256 * 4;      // int [16 * 8]
 constexpr int kPermOff = 8192;                   // int [128] entries, int [128] rows
 constexpr int kPlanOff = kSelOff + 512;          // MoePlan [kMaxLayers], set once per launch
 
+// Speculative L2 prefetch of a producer's predicted first gate/up tile while
+// routing runs (see spec_prefetch): KB of weights a producer.
+#ifndef ET_SPEC_PREFETCH_KB
+#define ET_SPEC_PREFETCH_KB 512
+#endif
+constexpr int kSpecPrefetchKb = ET_SPEC_PREFETCH_KB;
+
 // ------------------------------------------------------------------ trace
 
 // Optional per-task record (see et_opts.trace): {type | role << 8, a, b, cta,
@@ -281,6 +288,7 @@ struct MoePlan {
     // down split; the static prefix [norm][router][shared gate/up] precedes the
     // routing-driven queue, which holds the shared down tiles
     int NRN, MTS, FTS, SS, NSG, NSD, NS0;
+    bool spec;     // idle producers prefetch their predicted first gate/up tile (see pop_task)
 };
 static_assert(kPlanOff + kMaxLayers * sizeof(MoePlan) <= kMoeScratch, "plans fit the scratch");
 
@@ -354,6 +362,14 @@ __device__ __forceinline__ MoePlan moe_plan(const MoeArgs& p, int T, int G, uint
     P.NSG = P.MTS * P.FTS;
     P.NSD = P.MTS * P.SS * HT;
     P.NS0 = P.NRN + P.R * P.C + P.NSG;  // shared down tiles are queued by the scan
+    // With few experts and many tokens every expert is active (each expects
+    // >= 4 rows; one row tile an expert up to 256 rows) and there are enough
+    // gate/up tiles that they are not split along K, so the queue's first
+    // gate/up tasks are known before routing: expert 0's F-tiles in order, then
+    // expert 1's ... (see queue_task).
+    const int FTp = p.F / kTileM;
+    P.spec = kSpecPrefetchKb > 0 && E <= 16 && T * k >= 4 * E && T * k <= kMoeNMax * E &&
+             E * FTp >= 3 * G && !p.gamma && !p.ev_in;
     return P;
 }
 
@@ -1204,6 +1220,23 @@ __device__ __forceinline__ TaskMsg static_task(const MoeArgs& p, const MoePlan& 
     return m;
 }
 
+// While routing runs, HBM is idle.  A producer that has claimed gate/up
+// queue entry q (after the permute parts) before the queue is published
+// prefetches into L2 the first kSpecPrefetchKb of the gate/up weights the
+// entry is predicted to need (plan.spec: expert q / (F/128), F-tile
+// q % (F/128)), so the first wave of gate/up tiles reads them from L2.  A
+// wrong prediction costs only bandwidth that was idle.
+__device__ __forceinline__ void spec_prefetch(const MoeArgs& p, const MoeLayerMaps& M, int q) {
+    const int FT = p.F / kTileM;
+    if (q < 0 || q >= p.E * FT) return;
+    const int row = (q / FT) * p.F + (q % FT) * kTileM;
+    const int nkb = min(p.H / kBlockK, kSpecPrefetchKb / (2 * kABytes / 1024));
+    for (int kb = 0; kb < nkb; ++kb) {
+        tma_prefetch_l2(&M.wg, kb * kBlockK, row);
+        tma_prefetch_l2(&M.wu, kb * kBlockK, row);
+    }
+}
+
 // Producer thread: next task of this CTA (EXIT when every layer's tasks are
 // taken or the launch aborted).  `claim` is a task index taken ahead of time
 // (or -1); claims only grow, so the cursor only moves forward.  With `nowait`
@@ -1231,6 +1264,8 @@ __device__ __forceinline__ TaskMsg pop_task(const MoeLaunchOf<kChain>& Lc, const
                 m.type = kTaskNone;
                 return m;
             }
+            if (P.spec && ld_acquire(&p.hdr->q_ready) < 1)
+                spec_prefetch(p, Lc.m[kChain ? cur.layer : 0], j - P.NS0 - P.NP);
             if (!ev_wait_geq(wc, &p.hdr->q_ready, 1, kWhereQueue)) return m;
             cur.qt = ld_relaxed(&p.hdr->q_total);
             cur.mt = ld_relaxed(&p.hdr->total_mt);
