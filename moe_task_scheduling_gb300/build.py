@@ -62,14 +62,22 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
         r = subprocess.run(cmd, capture_output=True, text=True)
         return cmd, r
 
+    def crashed(r):  # the compiler died of a signal (not a compile error)
+        return r.returncode < 0 or "Segmentation fault" in r.stderr or r.returncode >= 128
+
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
-            for cmd, r in ex.map(run, jobs):
-                if verbose or ptxas_info or r.returncode != 0:
-                    sys.stdout.write(r.stdout)
-                    sys.stderr.write(r.stderr)
-                if r.returncode != 0:
-                    raise RuntimeError("nvcc failed: " + " ".join(cmd))
+            results = list(ex.map(run, jobs))
+        for cmd, r in results:
+            if r.returncode != 0 and crashed(r):
+                # a compiler crash seen once on the Arm GPU hosts with the units
+                # built in parallel: build the unit again, alone
+                cmd, r = run(cmd)
+            if verbose or ptxas_info or r.returncode != 0:
+                sys.stdout.write(r.stdout)
+                sys.stderr.write(r.stderr)
+            if r.returncode != 0:
+                raise RuntimeError("nvcc failed: " + " ".join(cmd))
     if force or jobs or _stale(lib, objs):
         tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lpthread"]

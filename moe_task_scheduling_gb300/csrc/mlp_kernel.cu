@@ -191,7 +191,6 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     // configured shape (H 4096, F 14336): S = 7 / 14 / 4 at B = 1 gave 89 /
     // 89 / 90 us, at B = 64 98 / 109 / 109 us; S = 4 against 7 at B = 128
     // 104 against 111 us, at B = 256 135 against 139 us.
-#ifndef ET_MLP_SPLIT
     P.S = 1;
     if (P.MT > 0 && P.MT * P.HT < static_cast<int>(gridDim.x)) {
         const int cap = P.B > 64 ? 4 : kMlpSplitMax;
@@ -201,9 +200,6 @@ mlp_chain_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             if (P.MT * P.HT * d >= static_cast<int>(gridDim.x)) break;
         }
     }
-#else
-    P.S = ET_MLP_SPLIT;  // a fixed split (tuning builds only)
-#endif
     // K split of the gate/up tiles: with one row tile, F/128 tiles can leave
     // CTAs idle; the smallest split that gives the grid >= 2.5 tasks a CTA (K
     // chunks of >= 8 k-blocks, partial rows within gu_cap), else none

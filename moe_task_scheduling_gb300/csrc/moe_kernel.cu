@@ -100,11 +100,9 @@ constexpr int kPermOff = 8192;                   // int [128] entries, int [128]
 constexpr int kPlanOff = kSelOff + 512;          // MoePlan [kMaxLayers], set once per launch
 
 // Speculative L2 prefetch of a producer's predicted first gate/up tile while
-// routing runs (see spec_prefetch): KB of weights a producer.
-#ifndef ET_SPEC_PREFETCH_KB
-#define ET_SPEC_PREFETCH_KB 512
-#endif
-constexpr int kSpecPrefetchKb = ET_SPEC_PREFETCH_KB;
+// routing runs (see spec_prefetch): KB of weights a producer (measured on the
+// Mixtral shape: +0.7 % over the sweep with 512 or 1024, T >= 16 gaining).
+constexpr int kSpecPrefetchKb = 512;
 
 // ------------------------------------------------------------------ trace
 
@@ -142,23 +140,6 @@ struct TraceScope {  // records the workers' task on scope exit (worker thread 0
 
 // ------------------------------------------------------------------ ROUTER
 
-template <int EBW>
-__device__ __forceinline__ void load_w(const bf16* wrow, float (&w)[EBW]) {
-    if constexpr (EBW == 8) {
-        unpack8(*reinterpret_cast<const uint4*>(wrow), w);
-    } else if constexpr (EBW == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(wrow);
-        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
-        w[0] = f0.x; w[1] = f0.y; w[2] = f1.x; w[3] = f1.y;
-    } else if constexpr (EBW == 2) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(wrow));
-        w[0] = f.x; w[1] = f.y;
-    } else {
-        w[0] = bf2f(*wrow);
-    }
-}
-
 // Fixed-order logits of nt (<= 16) tokens x `ec` experts (global experts
 // e0 .. e0+ec).  A job is TB tokens x EBW experts on one warp: lane l owns
 // partial sum l and accumulates h = l, l+32, ... in ascending order with fp32
@@ -170,18 +151,22 @@ __device__ __forceinline__ void load_w(const bf16* wrow, float (&w)[EBW]) {
 // and the staged one (blocks of 8 experts, 16 bytes a row).  EBW divides
 // both ec and 8, so a job's EBW columns never straddle a block.  Logit
 // (t, e0 + j) goes to out[t * E + e0 + j].
-// c0 = fma(x, w0, c0), c1 = fma(x, w1, c1) in one packed fp32x2 instruction.
-__device__ __forceinline__ void fma2(float& c0, float& c1, float x, float w0, float w1) {
-    uint64_t d;
-    asm("{\n\t.reg .b64 xa, wa, ca;\n\t"
-        "mov.b64 xa, {%1, %1};\n\t"
-        "mov.b64 wa, {%2, %3};\n\t"
-        "mov.b64 ca, {%4, %5};\n\t"
-        "fma.rn.f32x2 %0, xa, wa, ca;\n\t}"
-        : "=l"(d)
-        : "f"(x), "f"(w0), "f"(w1), "f"(c0), "f"(c1));
-    c0 = __uint_as_float(static_cast<uint32_t>(d));
-    c1 = __uint_as_float(static_cast<uint32_t>(d >> 32));
+// Weights of EBW experts at one h as EBW/2 fp32 pairs (EBW even).
+template <int EBW>
+__device__ __forceinline__ void load_w2(const bf16* wrow, float2 (&w)[EBW / 2]) {
+    if constexpr (EBW == 8) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(wrow);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = __bfloat1622float2(b2[i]);
+    } else if constexpr (EBW == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(wrow);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        w[0] = __bfloat1622float2(b2[0]);
+        w[1] = __bfloat1622float2(b2[1]);
+    } else {
+        w[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(wrow));
+    }
 }
 
 template <int EBW, int TB>
@@ -191,14 +176,19 @@ __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16*
     const int H = p.H, E = p.E;
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
     const int neb = ec / EBW, ntb = ceil_div(nt, TB);
+    constexpr int EP = EBW >= 2 ? EBW / 2 : 1;  // accumulator pairs (EBW even) or singles
     for (int job = warp; job < neb * ntb; job += kWorkers / 32) {
         const int tb = job / neb, j0 = (job % neb) * EBW;
         const int tn = min(TB, nt - tb * TB);
-        float acc[TB][EBW];
+        // accumulators: pairs of experts as float2 (EBW even), else one float
+        float2 acc2[TB][EP];
+        float acc1[TB];
 #pragma unroll
-        for (int a = 0; a < TB; ++a)
+        for (int a = 0; a < TB; ++a) {
+            acc1[a] = 0.0f;
 #pragma unroll
-            for (int b = 0; b < EBW; ++b) acc[a][b] = 0.0f;
+            for (int b = 0; b < EP; ++b) acc2[a][b] = make_float2(0.0f, 0.0f);
+        }
         const bf16* xr = xb + static_cast<size_t>(tb * TB) * H;
         const bf16* wj = wb + static_cast<size_t>((o + j0) >> 3) * blk + ((o + j0) & 7);
         // A plain loop unrolled twice.  Each lane's sum is one dependent chain
@@ -207,22 +197,41 @@ __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16*
         // after the flush, where the longer code costs more than it saves
         // (measured over the sweeps: unroll 2 against 8 for the narrow jobs,
         // +0.3 % Mixtral-shaped, +0.9 % fine-grained; unroll 1 -1 % and -3 %).
-        // Pairs of experts go through one packed fma.rn.f32x2 (two independent
-        // IEEE fmas: the same sums, half the instructions).
+        // Pairs of experts go through one packed fp32x2 fma (__ffma2_rn: two
+        // independent IEEE fmas, so the same sums) on float2 accumulators,
+        // which needs no packing moves around it.
 #pragma unroll 2
         for (int h = lane; h < H; h += 32) {  // h ascending per lane
-            float wv[EBW];
-            load_w<EBW>(wj + static_cast<size_t>(h) * rs, wv);
+            if constexpr (EBW % 2 == 0) {
+                float2 wv[EP];
+                load_w2<EBW>(wj + static_cast<size_t>(h) * rs, wv);
 #pragma unroll
-            for (int a = 0; a < TB; ++a) {
-                const float xv = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
-                if constexpr (EBW % 2 == 0) {
+                for (int a = 0; a < TB; ++a) {
+                    const float xv = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
+                    const float2 x2 = make_float2(xv, xv);
 #pragma unroll
-                    for (int b = 0; b < EBW; b += 2) fma2(acc[a][b], acc[a][b + 1], xv, wv[b], wv[b + 1]);
-                } else {
-#pragma unroll
-                    for (int b = 0; b < EBW; ++b) acc[a][b] = fmaf(xv, wv[b], acc[a][b]);
+                    for (int b = 0; b < EP; ++b) acc2[a][b] = __ffma2_rn(x2, wv[b], acc2[a][b]);
                 }
+            } else {
+                const float wv = bf2f(wj[static_cast<size_t>(h) * rs]);
+#pragma unroll
+                for (int a = 0; a < TB; ++a) {
+                    const float xv = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
+                    acc1[a] = fmaf(xv, wv, acc1[a]);
+                }
+            }
+        }
+        float acc[TB][EBW];
+#pragma unroll
+        for (int a = 0; a < TB; ++a) {
+            if constexpr (EBW % 2 == 0) {
+#pragma unroll
+                for (int b = 0; b < EP; ++b) {
+                    acc[a][2 * b] = acc2[a][b].x;
+                    acc[a][2 * b + 1] = acc2[a][b].y;
+                }
+            } else {
+                acc[a][0] = acc1[a];
             }
         }
 #pragma unroll
