@@ -151,88 +151,70 @@ struct TraceScope {  // records the workers' task on scope exit (worker thread 0
 // and the staged one (blocks of 8 experts, 16 bytes a row).  EBW divides
 // both ec and 8, so a job's EBW columns never straddle a block.  Logit
 // (t, e0 + j) goes to out[t * E + e0 + j].
-// Weights of EBW experts at one h as EBW/2 fp32 pairs (EBW even).
-template <int EBW>
-__device__ __forceinline__ void load_w2(const bf16* wrow, float2 (&w)[EBW / 2]) {
+// Weights of EBW experts at one h as bf16 bit patterns.  SH: the row is in
+// shared memory at window address `sa`; otherwise it is read through `g`.
+template <int EBW, bool SH>
+__device__ __forceinline__ void load_w16(const bf16* g, uint32_t sa, uint16_t (&w)[EBW]) {
+    uint32_t u[(EBW + 1) / 2];
     if constexpr (EBW == 8) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(wrow);
-        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = __bfloat1622float2(b2[i]);
+        const uint4 v = SH ? lds_v4(sa) : *reinterpret_cast<const uint4*>(g);
+        u[0] = v.x, u[1] = v.y, u[2] = v.z, u[3] = v.w;
     } else if constexpr (EBW == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(wrow);
-        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        w[0] = __bfloat1622float2(b2[0]);
-        w[1] = __bfloat1622float2(b2[1]);
+        const uint2 v = SH ? lds_v2(sa) : *reinterpret_cast<const uint2*>(g);
+        u[0] = v.x, u[1] = v.y;
+    } else if constexpr (EBW == 2) {
+        u[0] = SH ? lds_u32(sa) : *reinterpret_cast<const uint32_t*>(g);
     } else {
-        w[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(wrow));
+        u[0] = SH ? lds_u16(sa) : __bfloat16_as_ushort(*g);
     }
+#pragma unroll
+    for (int b = 0; b < EBW; ++b)
+        w[b] = static_cast<uint16_t>((b & 1) ? (u[b >> 1] >> 16) : (u[b >> 1] & 0xffffu));
 }
 
-template <int EBW, int TB>
+template <int EBW, int TB, bool SH>
 __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16* xb,
                                                    const bf16* wb, int o, int rs, int blk, int nt,
                                                    int e0, int ec, float* out) {
     const int H = p.H, E = p.E;
     const int warp = wtid_() >> 5, lane = wtid_() & 31;
     const int neb = ec / EBW, ntb = ceil_div(nt, TB);
-    constexpr int EP = EBW >= 2 ? EBW / 2 : 1;  // accumulator pairs (EBW even) or singles
     for (int job = warp; job < neb * ntb; job += kWorkers / 32) {
         const int tb = job / neb, j0 = (job % neb) * EBW;
         const int tn = min(TB, nt - tb * TB);
-        // accumulators: pairs of experts as float2 (EBW even), else one float
-        float2 acc2[TB][EP];
-        float acc1[TB];
-#pragma unroll
-        for (int a = 0; a < TB; ++a) {
-            acc1[a] = 0.0f;
-#pragma unroll
-            for (int b = 0; b < EP; ++b) acc2[a][b] = make_float2(0.0f, 0.0f);
-        }
-        const bf16* xr = xb + static_cast<size_t>(tb * TB) * H;
-        const bf16* wj = wb + static_cast<size_t>((o + j0) >> 3) * blk + ((o + j0) & 7);
-        // A plain loop unrolled twice.  Each lane's sum is one dependent chain
-        // of H/32 fmas; unrolling 8 steps took a warm 1-token job from 7.1K to
-        // 4.5K SM cycles in isolation, but the launch runs this code once, cold
-        // after the flush, where the longer code costs more than it saves
-        // (measured over the sweeps: unroll 2 against 8 for the narrow jobs,
-        // +0.3 % Mixtral-shaped, +0.9 % fine-grained; unroll 1 -1 % and -3 %).
-        // Pairs of experts go through one packed fp32x2 fma (__ffma2_rn: two
-        // independent IEEE fmas, so the same sums) on float2 accumulators,
-        // which needs no packing moves around it.
-#pragma unroll 2
-        for (int h = lane; h < H; h += 32) {  // h ascending per lane
-            if constexpr (EBW % 2 == 0) {
-                float2 wv[EP];
-                load_w2<EBW>(wj + static_cast<size_t>(h) * rs, wv);
-#pragma unroll
-                for (int a = 0; a < TB; ++a) {
-                    const float xv = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
-                    const float2 x2 = make_float2(xv, xv);
-#pragma unroll
-                    for (int b = 0; b < EP; ++b) acc2[a][b] = __ffma2_rn(x2, wv[b], acc2[a][b]);
-                }
-            } else {
-                const float wv = bf2f(wj[static_cast<size_t>(h) * rs]);
-#pragma unroll
-                for (int a = 0; a < TB; ++a) {
-                    const float xv = a < tn ? bf2f(xr[static_cast<size_t>(a) * H + h]) : 0.0f;
-                    acc1[a] = fmaf(xv, wv, acc1[a]);
-                }
-            }
-        }
         float acc[TB][EBW];
 #pragma unroll
-        for (int a = 0; a < TB; ++a) {
-            if constexpr (EBW % 2 == 0) {
+        for (int a = 0; a < TB; ++a)
 #pragma unroll
-                for (int b = 0; b < EP; ++b) {
-                    acc[a][2 * b] = acc2[a][b].x;
-                    acc[a][2 * b + 1] = acc2[a][b].y;
-                }
-            } else {
-                acc[a][0] = acc1[a];
-            }
+            for (int b = 0; b < EBW; ++b) acc[a][b] = 0.0f;
+        // rows past the tile's last token repeat that token (in bounds; their
+        // sums are never stored)
+        int xrow[TB];
+#pragma unroll
+        for (int a = 0; a < TB; ++a) xrow[a] = (tb * TB + min(a, tn - 1)) * H;
+        const bf16* wj = wb + static_cast<size_t>((o + j0) >> 3) * blk + ((o + j0) & 7);
+        const uint32_t xs = SH ? smem_u32(xb) : 0u, ws = SH ? smem_u32(wj) : 0u;
+        // One fp32 fma with bf16 operands (fma.rn.f32.bf16) per product: the
+        // operands need no widening moves.  Measured in isolation on GB300, a
+        // 16-token x 32-expert tile over H = 2048 on 8 warps: 15.0K SM cycles,
+        // against 18.6K for packed fp32x2 fmas fed by bf16 -> fp32 unpacking,
+        // and 24.4K for the latter through generic pointers into shared memory
+        // (hence the shared-window loads).  Unrolled twice: this code often
+        // runs once per call, cold after the flush.
+#pragma unroll 2
+        for (int h = lane; h < H; h += 32) {  // h ascending per lane
+            uint16_t wv[EBW];
+            load_w16<EBW, SH>(wj + static_cast<size_t>(h) * rs,
+                              ws + static_cast<uint32_t>(h * rs) * 2u, wv);
+            uint16_t xv[TB];
+#pragma unroll
+            for (int a = 0; a < TB; ++a)
+                xv[a] = SH ? lds_u16(xs + static_cast<uint32_t>(xrow[a] + h) * 2u)
+                           : __bfloat16_as_ushort(xb[static_cast<size_t>(xrow[a]) + h]);
+#pragma unroll
+            for (int a = 0; a < TB; ++a)
+#pragma unroll
+                for (int b = 0; b < EBW; ++b) acc[a][b] = fma_bf16(xv[a], wv[b], acc[a][b]);
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1)
@@ -253,23 +235,26 @@ __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16*
     }
 }
 
-// Narrow jobs (up to 16 accumulators, their loop unrolled 8 steps) run out of
-// line, so their registers do not add to the kernel's; the 4x8 job (many to a
-// CTA on large batches) stays inline, which measured faster there.
-template <int EBW, int TB>
+// Narrow jobs (up to 16 accumulators) run out of line, so their registers do
+// not add to the kernel's; the 4x8 job (many to a CTA on large batches) stays
+// inline, which measured faster there.  Tiles read in place (not staged) take
+// the out-of-line generic-pointer form.
+template <int EBW, int TB, bool SH>
 static __device__ __noinline__ void router_logits_narrow(const MoeArgs& p, const bf16* xb,
                                                          const bf16* wb, int o, int rs, int blk,
                                                          int nt, int e0, int ec, float* out) {
-    router_logits_body<EBW, TB>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    router_logits_body<EBW, TB, SH>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
 }
 template <int EBW, int TB>
-__device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, const bf16* wb,
-                                              int o, int rs, int blk, int nt, int e0, int ec,
-                                              float* out) {
-    if constexpr (TB * EBW >= 32)
-        router_logits_body<EBW, TB>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+__device__ __forceinline__ void router_logits(bool staged, const MoeArgs& p, const bf16* xb,
+                                              const bf16* wb, int o, int rs, int blk, int nt,
+                                              int e0, int ec, float* out) {
+    if (!staged)
+        router_logits_narrow<EBW, TB, false>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    else if constexpr (TB * EBW >= 32)
+        router_logits_body<EBW, TB, true>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
     else
-        router_logits_narrow<EBW, TB>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+        router_logits_narrow<EBW, TB, true>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
 }
 
 // Router-weight staging geometry: 8-expert column blocks, rows padded to the
@@ -602,22 +587,22 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     const int ebw = ew % 8 == 0 ? 8 : (ew % 4 == 0 ? 4 : (ew % 2 == 0 ? 2 : 1));
     if (nt == 1) {
         if (ebw == 8)
-            router_logits<8, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<8, 1>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else if (ebw == 4)
-            router_logits<4, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<4, 1>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else if (ebw == 2)
-            router_logits<2, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<2, 1>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else
-            router_logits<1, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<1, 1>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
     } else {
         if (ebw == 8)
-            router_logits<8, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<8, 4>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else if (ebw == 4)
-            router_logits<4, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<4, 4>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else if (ebw == 2)
-            router_logits<2, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<2, 4>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else
-            router_logits<1, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<1, 4>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
     }
     worker_sync();
     tm = phase_mark(p, 1, tm);
