@@ -69,9 +69,12 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
         with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
             results = list(ex.map(run, jobs))
         for cmd, r in results:
-            if r.returncode != 0 and crashed(r):
-                # a compiler crash seen once on the Arm GPU hosts with the units
-                # built in parallel: build the unit again, alone
+            # the device front end has died of a signal now and then on both
+            # hosts, on sources that build on the next attempt: build the unit
+            # again, alone, a few times
+            for _ in range(3):
+                if r.returncode == 0 or not crashed(r):
+                    break
                 cmd, r = run(cmd)
             if verbose or ptxas_info or r.returncode != 0:
                 sys.stdout.write(r.stdout)

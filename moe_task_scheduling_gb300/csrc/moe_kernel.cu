@@ -151,28 +151,28 @@ struct TraceScope {  // records the workers' task on scope exit (worker thread 0
 // and the staged one (blocks of 8 experts, 16 bytes a row).  EBW divides
 // both ec and 8, so a job's EBW columns never straddle a block.  Logit
 // (t, e0 + j) goes to out[t * E + e0 + j].
-// Weights of EBW experts at one h as bf16 bit patterns.  SH: the row is in
-// shared memory at window address `sa`; otherwise it is read through `g`.
-template <int EBW, bool SH>
-__device__ __forceinline__ void load_w16(const bf16* g, uint32_t sa, uint16_t (&w)[EBW]) {
+// Weights of EBW experts at one h (shared-window address `sa`) as bf16 bit
+// patterns.
+template <int EBW>
+__device__ __forceinline__ void load_w16(uint32_t sa, uint16_t (&w)[EBW]) {
     uint32_t u[(EBW + 1) / 2];
     if constexpr (EBW == 8) {
-        const uint4 v = SH ? lds_v4(sa) : *reinterpret_cast<const uint4*>(g);
+        const uint4 v = lds_v4(sa);
         u[0] = v.x, u[1] = v.y, u[2] = v.z, u[3] = v.w;
     } else if constexpr (EBW == 4) {
-        const uint2 v = SH ? lds_v2(sa) : *reinterpret_cast<const uint2*>(g);
+        const uint2 v = lds_v2(sa);
         u[0] = v.x, u[1] = v.y;
     } else if constexpr (EBW == 2) {
-        u[0] = SH ? lds_u32(sa) : *reinterpret_cast<const uint32_t*>(g);
+        u[0] = lds_u32(sa);
     } else {
-        u[0] = SH ? lds_u16(sa) : __bfloat16_as_ushort(*g);
+        u[0] = lds_u16(sa);
     }
 #pragma unroll
     for (int b = 0; b < EBW; ++b)
         w[b] = static_cast<uint16_t>((b & 1) ? (u[b >> 1] >> 16) : (u[b >> 1] & 0xffffu));
 }
 
-template <int EBW, int TB, bool SH>
+template <int EBW, int TB>
 __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16* xb,
                                                    const bf16* wb, int o, int rs, int blk, int nt,
                                                    int e0, int ec, float* out) {
@@ -193,7 +193,7 @@ __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16*
 #pragma unroll
         for (int a = 0; a < TB; ++a) xrow[a] = (tb * TB + min(a, tn - 1)) * H;
         const bf16* wj = wb + static_cast<size_t>((o + j0) >> 3) * blk + ((o + j0) & 7);
-        const uint32_t xs = SH ? smem_u32(xb) : 0u, ws = SH ? smem_u32(wj) : 0u;
+        const uint32_t xs = smem_u32(xb), ws = smem_u32(wj);
         // One fp32 fma with bf16 operands (fma.rn.f32.bf16) per product: the
         // operands need no widening moves.  Measured in isolation on GB300, a
         // 16-token x 32-expert tile over H = 2048 on 8 warps: 15.0K SM cycles,
@@ -204,13 +204,10 @@ __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16*
 #pragma unroll 2
         for (int h = lane; h < H; h += 32) {  // h ascending per lane
             uint16_t wv[EBW];
-            load_w16<EBW, SH>(wj + static_cast<size_t>(h) * rs,
-                              ws + static_cast<uint32_t>(h * rs) * 2u, wv);
+            load_w16<EBW>(ws + static_cast<uint32_t>(h * rs) * 2u, wv);
             uint16_t xv[TB];
 #pragma unroll
-            for (int a = 0; a < TB; ++a)
-                xv[a] = SH ? lds_u16(xs + static_cast<uint32_t>(xrow[a] + h) * 2u)
-                           : __bfloat16_as_ushort(xb[static_cast<size_t>(xrow[a]) + h]);
+            for (int a = 0; a < TB; ++a) xv[a] = lds_u16(xs + static_cast<uint32_t>(xrow[a] + h) * 2u);
 #pragma unroll
             for (int a = 0; a < TB; ++a)
 #pragma unroll
@@ -235,26 +232,44 @@ __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16*
     }
 }
 
-// Narrow jobs (up to 16 accumulators) run out of line, so their registers do
-// not add to the kernel's; the 4x8 job (many to a CTA on large batches) stays
-// inline, which measured faster there.  Tiles read in place (not staged) take
-// the out-of-line generic-pointer form.
-template <int EBW, int TB, bool SH>
+// Tiles read in place (the router weight could not be staged): the same
+// order through generic pointers, one (token, expert) logit a warp at a time
+// (a fallback for expert counts without 8-expert weight blocks).
+static __device__ __noinline__ void router_logits_inplace(int H, int E, const float* bias,
+                                                          const bf16* xb, const bf16* wb, int o,
+                                                          int rs, int blk, int nt, int e0, int ec,
+                                                          float* out) {
+    const int warp = wtid_() >> 5, lane = wtid_() & 31;
+    for (int job = warp; job < nt * ec; job += kWorkers / 32) {
+        const int t = job / ec, j = job % ec;
+        const bf16* xr = xb + static_cast<size_t>(t) * H;
+        const bf16* wj = wb + static_cast<size_t>((o + j) >> 3) * blk + ((o + j) & 7);
+        float acc = 0.0f;
+        for (int h = lane; h < H; h += 32)
+            acc = fmaf(bf2f(xr[h]), bf2f(wj[static_cast<size_t>(h) * rs]), acc);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) acc = acc + __shfl_down_sync(0xffffffffu, acc, off);
+        if (lane == 0) out[t * E + e0 + j] = bias ? acc + bias[e0 + j] : acc;
+    }
+}
+
+// Narrow staged jobs (up to 16 accumulators) run out of line, so their
+// registers do not add to the kernel's; the 4x8 job (many to a CTA on large
+// batches) stays inline, which measured faster there.
+template <int EBW, int TB>
 static __device__ __noinline__ void router_logits_narrow(const MoeArgs& p, const bf16* xb,
                                                          const bf16* wb, int o, int rs, int blk,
                                                          int nt, int e0, int ec, float* out) {
-    router_logits_body<EBW, TB, SH>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+    router_logits_body<EBW, TB>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
 }
 template <int EBW, int TB>
-__device__ __forceinline__ void router_logits(bool staged, const MoeArgs& p, const bf16* xb,
-                                              const bf16* wb, int o, int rs, int blk, int nt,
-                                              int e0, int ec, float* out) {
-    if (!staged)
-        router_logits_narrow<EBW, TB, false>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
-    else if constexpr (TB * EBW >= 32)
-        router_logits_body<EBW, TB, true>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+__device__ __forceinline__ void router_logits(const MoeArgs& p, const bf16* xb, const bf16* wb,
+                                              int o, int rs, int blk, int nt, int e0, int ec,
+                                              float* out) {
+    if constexpr (TB * EBW >= 32)
+        router_logits_body<EBW, TB>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
     else
-        router_logits_narrow<EBW, TB, true>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
+        router_logits_narrow<EBW, TB>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
 }
 
 // Router-weight staging geometry: 8-expert column blocks, rows padded to the
@@ -585,24 +600,26 @@ __device__ __forceinline__ bool router_task(const MoeArgs& p, const MoePlan& P, 
     // experts as one 1x2 job 60 % of the time of one 4x2 job.
     const int ew = (P.stage && !P.wr_whole) ? ec : (ec | E);
     const int ebw = ew % 8 == 0 ? 8 : (ew % 4 == 0 ? 4 : (ew % 2 == 0 ? 2 : 1));
-    if (nt == 1) {
+    if (!P.stage) {
+        router_logits_inplace(p.H, p.E, p.bias, xb, wb, o, rs, blk, nt, e0, ec, out);
+    } else if (nt == 1) {
         if (ebw == 8)
-            router_logits<8, 1>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<8, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else if (ebw == 4)
-            router_logits<4, 1>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<4, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else if (ebw == 2)
-            router_logits<2, 1>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<2, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else
-            router_logits<1, 1>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<1, 1>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
     } else {
         if (ebw == 8)
-            router_logits<8, 4>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<8, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else if (ebw == 4)
-            router_logits<4, 4>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<4, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else if (ebw == 2)
-            router_logits<2, 4>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<2, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
         else
-            router_logits<1, 4>(P.stage, p, xb, wb, o, rs, blk, nt, e0, ec, out);
+            router_logits<1, 4>(p, xb, wb, o, rs, blk, nt, e0, ec, out);
     }
     worker_sync();
     tm = phase_mark(p, 1, tm);
