@@ -28,6 +28,15 @@ constexpr int kSplitMax = 8;         // largest split of the MoE / MLP down proj
 
 // MoE
 constexpr int kMoeNMax = 256;        // token rows per expert tile (UMMA N)
+// Row-tile cap of an expert whose weights (gate, up, down) are at most
+// kSmallExpertBytes: its tiles re-read them from L2, and more, shorter tiles
+// balance the grid (measured on the fine-grained shape, 9.4 MB an expert:
+// T = 256 / 512 / 1024 / 4096 from 191 / 228 / 310 / 725 us with 256-row
+// tiles to 174 / 213 / 300 / 718 us; a cap of 64 lost at T >= 256; the
+// Mixtral-shaped experts, 352 MB each, keep 256-row tiles: 128-row tiles
+// re-read them from HBM, 538 -> 715 us at T = 512).
+constexpr int kMoeNSmall = 128;
+constexpr long long kSmallExpertBytes = 64ll << 20;
 constexpr int kRouterTile = 16;      // tokens per router tile (router and permute tasks)
 constexpr int kCombineTile = 16;     // most tokens per combine task
 constexpr int kMoeSplitRowsCap = 512;  // split the down projection only up to T*k rows

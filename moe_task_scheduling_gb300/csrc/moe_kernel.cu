@@ -787,6 +787,11 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     const int FT = p.F / kTileM, HT = p.H / kTileM;
     // offsets and row-tile starts: one warp, a block of experts per lane and a
     // shuffle scan across lanes
+    // Row tiles: an expert's rows split evenly over ceil(cnt / cap) tiles.  The
+    // cap is kMoeNMax, or kMoeNSmall for experts whose weights are small
+    // enough to be read again from L2 by each of their tiles: their tiles then
+    // spread over more CTAs.
+    const int ncap = 3ll * p.F * p.H * 2 <= kSmallExpertBytes ? kMoeNSmall : kMoeNMax;
     if (wtid_() < 32) {
         const int lane = wtid_(), per = ceil_div(E, 32);
         int csum = 0, msum = 0;
@@ -794,7 +799,8 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
             const int e = lane * per + i;
             if (e >= E) break;
             const int c = cnt_s[e];
-            const int n = c == 0 ? 0 : min(kMoeNMax, (c + 15) / 16 * 16);
+            const int t = c == 0 ? 0 : ceil_div(c, ncap);  // the expert's row tiles
+            const int n = c == 0 ? 0 : min(ncap, (ceil_div(c, t) + 15) / 16 * 16);
             n_s[e] = n;
             csum += c;
             msum += c == 0 ? 0 : ceil_div(c, n);
