@@ -31,7 +31,10 @@ def _run(etmoe, X, W, split, M=None, d_M=None, M_max=None, ws=None, Y=None):
 @pytest.mark.parametrize("M,N,K,split", [
     (1, 128, 64, 1), (1, 256, 512, 8), (3, 128, 1024, 16), (17, 256, 1024, 4),
     (64, 384, 2048, 2), (129, 256, 1024, 8), (200, 128, 512, 1), (256, 256, 768, 3),
-    (300, 256, 512, 2), (513, 128, 256, 4)])
+    (300, 256, 512, 2), (513, 128, 256, 4),
+    # more tile tasks than CTAs (several per CTA), with the last arriver (M <= 32) or
+    # reduce tasks over several row tiles
+    (40, 16384, 1024, 4), (600, 4096, 2048, 8), (8, 32768, 256, 2), (100, 32768, 256, 2)])
 def test_splitk_small_shapes(cuda_lib, oracle, M, N, K, split):
     X = _rand((M, K), 1.0, 1 + M)
     W = _rand((N, K), 1.0 / np.sqrt(K), 2 + N)
