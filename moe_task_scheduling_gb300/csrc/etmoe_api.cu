@@ -163,7 +163,7 @@ MoeLayout moe_layout(int T_max, int H, int F, int E, int k, bool block = false, 
     MoeLayout L{};
     L.Tk = T_max * k;
     L.r_max = ceil_div(T_max, kRouterTile);
-    L.mt_max = ceil_div(L.Tk, kMoeNSmall) + E;  // row tiles at the smallest cap
+    L.mt_max = ceil_div(L.Tk, kMoeNSmall / 2) + E;  // row tiles at the smallest cap
     const int FT = F / kTileM, HT = H / kTileM;
     L.mts_max = (block && Fs > 0) ? ceil_div(T_max, kWideNMax) : 0;
     L.split_cap = L.Tk < kMoeSplitRowsCap ? L.Tk : kMoeSplitRowsCap;

@@ -790,8 +790,11 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
     // Row tiles: an expert's rows split evenly over ceil(cnt / cap) tiles.  The
     // cap is kMoeNMax, or kMoeNSmall for experts whose weights are small
     // enough to be read again from L2 by each of their tiles: their tiles then
-    // spread over more CTAs.
-    const int ncap = 3ll * p.F * p.H * 2 <= kSmallExpertBytes ? kMoeNSmall : kMoeNMax;
+    // spread over more CTAs -- half of it up to 1024 routed rows, where a hot
+    // expert's tiles are the last to finish (fine-grained shape, T = 128:
+    // 162 -> 154 us; no change elsewhere).
+    const bool small_e = 3ll * p.F * p.H * 2 <= kSmallExpertBytes;
+    const int ncap = small_e ? (T * k <= 1024 ? kMoeNSmall / 2 : kMoeNSmall) : kMoeNMax;
     if (wtid_() < 32) {
         const int lane = wtid_(), per = ceil_div(E, 32);
         int csum = 0, msum = 0;
