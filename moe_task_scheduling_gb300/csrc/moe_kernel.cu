@@ -220,14 +220,24 @@ __device__ __forceinline__ void router_logits_body(const MoeArgs& p, const bf16*
 #pragma unroll
                 for (int b = 0; b < EBW; ++b)
                     acc[a][b] = acc[a][b] + __shfl_down_sync(0xffffffffu, acc[a][b], off);
-        if (lane == 0) {
-            for (int a = 0; a < tn; ++a)
+        // Lane i (< TB * EBW) takes logit (i / EBW, i % EBW) from lane 0, where
+        // the halving tree left every sum, and stores it with its bias: one
+        // load and one store for the job.  (Lane 0 storing them one by one
+        // took ~2.7K SM cycles a 4 x 8 job: each bias load waited for the
+        // previous logit's store, as the two arrays may alias.)
+        float v = 0.0f;
 #pragma unroll
-                for (int b = 0; b < EBW; ++b) {
-                    float L = acc[a][b];
-                    if (p.bias) L = L + p.bias[e0 + j0 + b];
-                    out[(tb * TB + a) * E + e0 + j0 + b] = L;
-                }
+        for (int a = 0; a < TB; ++a)
+#pragma unroll
+            for (int b = 0; b < EBW; ++b) {
+                const float sum = __shfl_sync(0xffffffffu, acc[a][b], 0);
+                if (lane == a * EBW + b) v = sum;
+            }
+        const int la = lane / EBW, lb = lane % EBW;
+        if (lane < TB * EBW && la < tn) {
+            float L = v;
+            if (p.bias) L = L + p.bias[e0 + j0 + lb];
+            out[(tb * TB + la) * E + e0 + j0 + lb] = L;
         }
     }
 }
