@@ -859,6 +859,8 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
         // two at most: measured on the Mixtral shape at T = 256, wide tiles in
         // 2 F-chunks take 494 us against 528 us for 128-column tiles in 4 and
         // 500 us for wide ones in 4 (their partials are twice the bytes).
+        // A single token aims at two tasks a CTA (measured on the Mixtral
+        // shape: 163 -> 157 us at T = 1; at T >= 2 the aim of four is faster).
         // Small tiles that already fill half the grid are not split: a split
         // adds a reduction chain (partials stored, counted, summed by the last
         // arriver, ~3 us) that a tile of <= 1 MB does not win back (measured
@@ -873,18 +875,19 @@ __device__ __forceinline__ bool scan_task(const MoeArgs& p, const MoePlan& P, ui
             for (int d = 2; d <= (wide ? 2 : kSplitMax); ++d) {
                 if (!((p.split_mask >> d) & 1)) continue;
                 const int kbc = p.F / kBlockK / d;
-                if (down * best >= 3 * G && kbc < 8) break;
+                if (down * best >= (T == 1 ? 2 : 3) * G && kbc < 8) break;
                 best = d;
-                if (down * d >= 4 * G) break;
+                if (down * d >= (T == 1 ? 2 : 4) * G) break;
             }
             S = best;
         }
         // K chunks of a gate/up tile: a small batch has few (weight-streaming)
-        // tiles, so they are cut along K until the grid has a few per CTA
+        // tiles, so they are cut along K until the grid has two per CTA (three
+        // measured 2 us slower on the Mixtral shape at T = 1)
         int KC = 1;
         const int gu = total_mt * FT;
         const bool gu_small = p.H * 512 <= (1 << 20) && 2 * gu >= G;
-        while (!gu_small && KC < kGuSplitMax && gu * KC < 3 * G &&
+        while (!gu_small && KC < kGuSplitMax && gu * KC < 2 * G &&
                ((p.kc_mask >> (2 * KC)) & 1) && T * k * 2 * KC <= p.gu_cap)
             KC *= 2;
         ctl->scratch[0] = total_mt;
